@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of the OSDN forward pass (Phase 1 + Phase 2) on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one pass of the whole forward path -- the preconditioner scan
+(osdn_precond_scan) then the chunkwise delta-rule pass (osdn_chunk_fwd) --
+over one batch of seeded synthetic input already resident in HBM.  The
+default workload is the 1.3B-class layer shape with adaptive preconditioner
+forgetting: B=2, H=16 heads of d_k = d_v = 128, T=8192, bf16 I/O.
+
+Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K
+steps, each preceded by an L2 flush (a write of twice the L2 size, outside
+the timed events); device time from CUDA events on the launching stream.
+`value` is tokens/s (B*T tokens per step, all H heads) over all ranks.
+`e2e` times the same step through the C ABI from pinned host buffers, with
+the host->device copies of the inputs and the device->host copies of
+(o, d_T, S_T) inside the timed region.  `--impl reference` times the fp64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from preconditioned_delta_rule_phase1_gb300 import synth  # noqa: E402
+
+METRIC = "OSDN fwd tokens/s (phase1+2) at 16×128 heads; % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "lm1p3b_apf_bf16"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (what the method must move), per launch
+# ---------------------------------------------------------------------------
+def io_bytes(w):
+    return 2 if w.io == "bf16" else 4
+
+
+def phase1_bytes(w, x):
+    BH, T, K, e = w.B * w.H, w.T, w.K, io_bytes(w)
+    b = BH * T * (2 * K * e + 4)                      # read k, write ktilde, read beta
+    b += BH * T * 4 if x["r"] is not None else 0      # retention gate
+    b += BH * K * 4                                   # write d_T
+    b += BH * K * 4 if x["d0"] is not None else 0
+    return b
+
+
+def phase2_bytes(w, x):
+    BH, T, K, V, e = w.B * w.H, w.T, w.K, w.V, io_bytes(w)
+    b = BH * T * ((3 * K + V) * e + V * e + 4)        # read q,k,ktilde,v; write o; read beta
+    b += BH * T * 4 if x["alpha"] is not None else 0
+    b += BH * V * K * 4                               # write S_T
+    b += BH * V * K * 4 if x["S0"] is not None else 0
+    return b
+
+
+def phase2_flops(w):
+    # per token-head: K S^T, Q S^T, U^T Ktilde (2KV each) plus the chunk-local
+    # Gram, scores, solve and intra-chunk output (2 C (K + V)), C = 64
+    C = 64
+    return w.B * w.H * w.T * (6 * w.K * w.V + 2 * C * (w.K + w.V))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        hbm = p.get("hbm_gbs")
+        bf16 = p.get("bf16_tflops")
+        if hbm:
+            return float(hbm), float(bf16 or FALLBACK_BF16_TFLOPS), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+def gpu_smi_id(dev, fallback):
+    """The nvidia-smi id (PCI bus id) of a torch device."""
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        return str(fallback)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline leg)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, x, n_seq, t_len, nthreads):
+    """Time the fp64 oracle on n_seq sequences x t_len tokens of the workload."""
+    import oracle
+    heads = list(range(min(n_seq, w.B * w.H)))
+    xs = synth.slice_heads(x, heads)
+    cut = lambda t: None if t is None else t[:, :, :t_len].contiguous()
+    args = dict(q=cut(xs["q"]), k=cut(xs["k"]), v=cut(xs["v"]), beta=cut(xs["beta"]),
+                r=cut(xs["r"]), alpha=cut(xs["alpha"]))
+    f64 = {n: (None if t is None else t.double().numpy()) for n, t in args.items()}
+    S0 = None if xs["S0"] is None else xs["S0"].double().numpy()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward(f64["q"], f64["k"], f64["v"], f64["beta"], f64["r"], w.eta, None,
+                   f64["alpha"], S0, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    token_heads = len(heads) * t_len
+    return dt, token_heads
+
+
+def cpu_sample_shape(w, nthreads, budget_s=12.0):
+    """A sample sized for roughly budget_s of oracle time on nthreads cores."""
+    flop_per_th = 6.0 * w.K * w.V + 8.0 * w.K
+    rate = 2.0e9 * nthreads          # rough fp64 rate of the plain oracle
+    work = budget_s * rate / flop_per_th          # token-heads that fit the budget
+    n_seq = int(min(w.B * w.H, max(1, work // w.T)))
+    t_len = int(min(w.T, max(64, work / n_seq)))
+    return n_seq, t_len
+
+
+# ---------------------------------------------------------------------------
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def run_reference(args, w, x, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.default_threads()
+    n_seq, t_len = cpu_sample_shape(w, cores, budget_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, n_seq, min(t_len, 64), cores)
+    times = []
+    th = 0
+    for _ in range(args.steps):
+        dt, th = oracle_sample(w, x, n_seq, t_len, cores)
+        times.append(dt)
+    per_step = sum(times) / len(times)
+    value = (th / w.H) / per_step
+    sample = "%d of %d sequences x first %d of %d tokens per step" % (n_seq, w.B * w.H, t_len, w.T)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.K, "d_v": w.V,
+                   "io": w.io, "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, x, rank, world, local_rank):
+    from preconditioned_delta_rule_phase1_gb300 import ops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    B, H, T, K, V = w.B, w.H, w.T, w.K, w.V
+    ws = ops.Workspace(device=dev)
+    ws.ensure(max(ops.precond_scan_workspace_bytes(B, H, T, K),
+                  ops.chunk_fwd_workspace_bytes(int(w.io == "bf16"), B, H, T, K, V)))
+    kt = torch.empty_like(g["k"])
+    dT = torch.empty(B, H, K, device=dev)
+    o = torch.empty(B, H, T, V, dtype=g["v"].dtype, device=dev)
+    ST = torch.empty(B, H, V, K, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step(s):
+        ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], kt, dT, ws, s)
+        ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], o, ST, ws, s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step(stream)
+    stream.synchronize()
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status after warm-up: %d" % ws.status(stream))
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_smi_id(dev, local_rank))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler attach before the timed region
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], kt, dT, ws, stream)
+            ev[i][1].record(stream)
+            ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], o, ST, ws,
+                          stream)
+            ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    st = ws.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after timed steps: %d" % st)
+    p1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    p2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    ms = [a + b for a, b in zip(p1, p2)]
+    ms_step = sum(ms) / len(ms)
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # ---- end to end through the C ABI from pinned host memory -------------
+    host_in = {n: (t.pin_memory() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                "dT": torch.empty(dT.shape).pin_memory(),
+                "ST": torch.empty(ST.shape).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values() if isinstance(t, torch.Tensor))
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    dev_in = {n: (torch.empty_like(t, device=dev) if isinstance(t, torch.Tensor) else t)
+              for n, t in host_in.items()}
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps + 2):
+            if i == 2:
+                e0.record(stream)
+            for n, t in host_in.items():
+                if isinstance(t, torch.Tensor):
+                    dev_in[n].copy_(t, non_blocking=True)
+            ops.precond_scan(dev_in["k"], dev_in["beta"], dev_in["r"], w.eta, dev_in["d0"], kt,
+                             dT, ws, stream)
+            ops.chunk_fwd(dev_in["q"], dev_in["k"], kt, dev_in["v"], dev_in["beta"],
+                          dev_in["alpha"], dev_in["S0"], o, ST, ws, stream)
+            host_out["o"].copy_(o, non_blocking=True)
+            host_out["dT"].copy_(dT, non_blocking=True)
+            host_out["ST"].copy_(ST, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- roofline of the dominant kernel ------------------------------------
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    b1, b2 = phase1_bytes(w, x), phase2_bytes(w, x)
+    t1, t2 = statistics.mean(p1), statistics.mean(p2)
+    dom = ("osdn_chunk_fwd", b2, t2) if t2 >= t1 else ("osdn_precond_scan", b1, t1)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    traffic = load_traffic(dom[0], w.name)
+
+    if rank != 0:
+        return
+    tokens = B * T * world
+    cores = None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.default_threads()
+        n_seq, t_len = cpu_sample_shape(w, cores)
+        dt, th = oracle_sample(w, x, n_seq, t_len, cores)
+        cpu = {"value": (th / w.H) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "%d of %d sequences x first %d of %d tokens (%.1f s)"
+                         % (n_seq, B * H, t_len, T, dt)}
+    line = {
+        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.io, "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "config": {"workload": w.name, "B": B, "H": H, "T": T, "d_k": K, "d_v": V,
+                   "io": w.io, "apf": w.apf, "gated": w.gated, "eta": w.eta,
+                   "l2": "flushed before every timed step (write of 2x L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "phases_ms": {"precond_scan": t1, "chunk_fwd": t2},
+        "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes": dom[1], "peak_source": peak_src},
+        "roofline_phases": {
+            "precond_scan": {"achieved_gbs": b1 / (t1 * 1e-3) / 1e9,
+                             "frac": b1 / (t1 * 1e-3) / 1e9 / hbm_peak},
+            "chunk_fwd": {"achieved_gbs": b2 / (t2 * 1e-3) / 1e9,
+                          "frac_hbm": b2 / (t2 * 1e-3) / 1e9 / hbm_peak,
+                          "tflops": phase2_flops(w) / (t2 * 1e-3) / 1e12,
+                          "frac_tensor": phase2_flops(w) / (t2 * 1e-3) / 1e12 / bf16_peak}},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if one exists."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s_%s.txt" % (kernel, workload))
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("dram_bytes_per_launch"):
+                    return float(line.split("=", 1)[1].split()[0])
+    except OSError:
+        pass
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, local_rank = env_rank()
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    if args.impl == "reference":
+        run_reference(args, w, x, rank, world)
+    else:
+        run_ours(args, w, x, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * osdn.h -- C ABI of the GB300 (sm_103a) Online Scaled DeltaNet forward pass.
+ *
+ * The method: "OSDN: Improving Delta Rule with Provable Online
+ * Preconditioning in Linear Attention" (arXiv 2605.13473), as summarised on
+ * the gist.science pages.  Section 2.2 states the forward pass as two phases,
+ * and the library has one call per phase:
+ *
+ *   Phase 1  osdn_precond_scan  -- the O(K) scan over the key stream that
+ *            produces the preconditioned keys ktilde_t = d_t (.) k_t and
+ *            updates the diagonal preconditioner d (sections 2.1-2.3);
+ *   Phase 2  osdn_chunk_fwd     -- the chunkwise delta-rule pass with ktilde
+ *            in place of k in the chunk Gram matrix and the intra-chunk scores
+ *            (section 2.1), producing o_t = S_t q_t and the final state.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the
+ *    library allocates no device or host memory and keeps no pointer after a
+ *    call returns.  Every tensor is dense, row-major, with the layouts named
+ *    below, and must start on a 16-byte boundary.
+ *  - Shapes: B, H, T >= 0 (a call with B*H*T == 0 is valid; see each call);
+ *    K = d_k and V = d_v must each be 64 or 128.
+ *  - Layouts: q, k, ktilde  [B][H][T][K]      v, o        [B][H][T][V]
+ *             beta, r, alpha [B][H][T] fp32   d0, dT      [B][H][K] fp32
+ *             S0, ST [B][H][V][K] fp32, S[i][j] with i the value row and j
+ *             the key column, so that S k is a V-vector.
+ *  - io selects the element type of q, k, ktilde, v and o: OSDN_F32 (fp32)
+ *    or OSDN_BF16 (bfloat16).  Gates and states are always fp32.
+ *  - stream is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Calls are asynchronous: they validate on the host, enqueue
+ *    their kernels and return.
+ *  - Return value: OSDN_OK, or a negative osdn_status.  Every argument check
+ *    happens before anything is enqueued, so a non-zero return means nothing
+ *    ran.  OSDN_ERR_CUDA means a launch was rejected by the CUDA runtime.
+ *  - Device-side faults never trap: a kernel that detects a problem (a wait
+ *    that ran out, an impossible index) writes its code into the status word
+ *    at the start of the workspace and exits.  osdn_check_status reads it.
+ *  - No C++ exception crosses this boundary and the library never exits or
+ *    aborts the process.
+ *
+ * Workspace
+ * ---------
+ *  Each call takes a caller-allocated device workspace of at least the size
+ *  its *_workspace_bytes function returns.  Its first 256 bytes hold the
+ *  device status word and are shared by all calls; the rest is scratch for
+ *  the call in flight (calls that use one workspace concurrently on
+ *  different streams race on it).  Zero the first 256 bytes once before the
+ *  first call (osdn_workspace_init does that on a stream); the status word is
+ *  sticky until the caller zeroes it again.
+ */
+#ifndef OSDN_H
+#define OSDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1 } osdn_dtype;
+
+typedef enum {
+    OSDN_OK = 0,
+    OSDN_ERR_NULL = -1,      /* a required pointer is NULL                     */
+    OSDN_ERR_DIMS = -2,      /* negative size, or K / V not in {64, 128}       */
+    OSDN_ERR_DTYPE = -3,     /* io is not OSDN_F32 / OSDN_BF16                 */
+    OSDN_ERR_ALIGN = -4,     /* a pointer is not 16-byte aligned               */
+    OSDN_ERR_WORKSPACE = -5, /* workspace NULL or smaller than required        */
+    OSDN_ERR_CUDA = -6,      /* the CUDA runtime rejected a launch or query    */
+    OSDN_ERR_TIMEOUT = -7,   /* device: a bounded wait ran out (status word)   */
+    OSDN_ERR_DEVICE = -8,    /* device: an internal consistency check failed   */
+    OSDN_ERR_ALIAS = -9,     /* an output overlaps an input it must not alias  */
+    OSDN_ERR_ARCH = -10      /* the current device is not sm_103 (GB300)       */
+} osdn_status;
+
+/* Bytes of workspace osdn_precond_scan needs for this shape (>= 256). */
+size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K);
+
+/*
+ * Phase 1: the preconditioner scan (sections 2.2 and 2.3).
+ *
+ * For each sequence (b,h), starting from d_0 (d0, or all ones if d0 is NULL),
+ * for t = 0 .. T-1:
+ *     ktilde_t = d_t (.) k_t
+ *     d_{t+1}  = r_t d_t + eta beta_t (1 - beta_t <d_t, k_t^2>) k_t^2 / ||k_t||^2
+ * which is d_{t+1} = r_t d_t - eta grad_d h_t(d_t) for the closed-form
+ * surrogate h_t(d) = ((1 - beta_t <d, k_t^2>)^2 - 1) / (2 ||k_t||^2)
+ * (section 2.2), taken as a DESCENT step (section 2.3 prints "+eta grad h";
+ * section 2.2 calls the update online gradient descent on h).  A zero key
+ * contributes no gradient.  r is the adaptive-preconditioner-forgetting
+ * retention gate (section 2.3); r == NULL means r = 1 (plain OSDN).
+ *
+ *   k      in   [B][H][T][K] io
+ *   beta   in   [B][H][T] fp32
+ *   r      in   [B][H][T] fp32, or NULL
+ *   eta    in   scalar step size of the preconditioner update
+ *   d0     in   [B][H][K] fp32, or NULL (all ones)
+ *   ktilde out  [B][H][T][K] io; must not overlap k
+ *   dT     out  [B][H][K] fp32, or NULL (not written)
+ * With T == 0 the call writes dT = d0 and nothing else.
+ */
+int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const float *beta,
+                      const float *r, float eta, const float *d0, void *ktilde, float *dT,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256). */
+size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V);
+
+/*
+ * Phase 2: the chunkwise delta-rule pass with preconditioned keys
+ * (section 2.1; section 2.2, item 2).
+ *
+ * For each sequence (b,h), starting from S_0 (S0, or zeros if S0 is NULL),
+ * for t = 0 .. T-1:
+ *     S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) ktilde_t^T
+ *     o_t = S_t q_t
+ * alpha == NULL means alpha = 1, the update S_t = S_{t-1} + beta_t (v_t -
+ * S_{t-1} k_t) ktilde_t^T of section 2.1.  A non-NULL alpha is a per-token
+ * state decay in the style of the Gated DeltaNet backbone named in section 4
+ * (the pages print no formula for it; this is the plainest reading).  The
+ * output is read from the state after token t and q is not scaled.
+ *
+ * The kernels evaluate this chunk by chunk: with the keys of a chunk in the
+ * rows of K, Ktilde, Q and the scaled residuals in U,
+ *     (I + tril(diag(beta) (Gamma . K Ktilde^T), -1)) U
+ *                                  = diag(beta) (V - diag(gamma) K S_0^T),
+ *     O = diag(gamma) Q S_0^T + tril(Gamma . Q Ktilde^T) U,
+ *     S = gamma_C S_0 + U^T diag(gamma_C / gamma) Ktilde,
+ * gamma the within-chunk cumulative product of alpha and Gamma_ij =
+ * gamma_i / gamma_j -- the stored keys replaced by Ktilde in the Gram matrix
+ * and the intra-chunk scores exactly as section 2.1 says.
+ *
+ *   q, k, ktilde in [B][H][T][K] io
+ *   v            in [B][H][T][V] io
+ *   beta         in [B][H][T] fp32
+ *   alpha        in [B][H][T] fp32, or NULL
+ *   S0           in [B][H][V][K] fp32, or NULL (zeros)
+ *   o            out [B][H][T][V] io; must not overlap any input
+ *   ST           out [B][H][V][K] fp32, or NULL (not written)
+ * io == OSDN_BF16 runs on the tensor cores (bf16 operands, fp32
+ * accumulation, state carried in fp32); io == OSDN_F32 runs in fp32 FFMA.
+ * With T == 0 the call writes ST = S0 and nothing else.
+ */
+int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                   const void *ktilde, const void *v, const float *beta, const float *alpha,
+                   const float *S0, void *o, float *ST, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Zero the 256-byte status area at the start of a workspace (async). */
+int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, read the device status word of `workspace` and
+ * return it (OSDN_OK if no kernel reported a problem).  Returns
+ * OSDN_ERR_CUDA if the stream itself reports an error.
+ */
+int osdn_check_status(const void *workspace, void *stream);
+
+/* A static, human-readable name for a status code. */
+const char *osdn_status_string(int code);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int osdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSDN_H */

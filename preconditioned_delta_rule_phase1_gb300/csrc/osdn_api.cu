@@ -1,0 +1,160 @@
+// osdn_api.cu -- the extern "C" boundary declared in include/osdn.h:
+// argument validation, workspace sizing, kernel dispatch and status.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "osdn.h"
+
+namespace osdn {
+cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
+                                const float *r, float eta, const float *d0, void *ktilde,
+                                float *dT, int *status, cudaStream_t stream);
+cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,
+                              cudaStream_t stream);
+cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
+                              const void *kt, const void *v, const float *beta,
+                              const float *alpha, const float *S0, void *o, float *ST,
+                              cudaStream_t stream);
+}  // namespace osdn
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool dims_ok(int B, int H, int T) { return B >= 0 && H >= 0 && T >= 0; }
+bool width_ok(int x) { return x == 64 || x == 128; }
+size_t io_bytes(int io) { return io == OSDN_BF16 ? 2 : 4; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// The kernels are built for sm_103a only: refuse other devices up front.
+int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return OSDN_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return OSDN_ERR_CUDA;
+    if (major != 10 || minor != 3) return OSDN_ERR_ARCH;
+    return OSDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osdn_version(void) { return 100; }
+
+const char *osdn_status_string(int code) {
+    switch (code) {
+    case OSDN_OK: return "ok";
+    case OSDN_ERR_NULL: return "a required pointer is NULL";
+    case OSDN_ERR_DIMS: return "bad dimensions (negative size, or K/V not 64 or 128)";
+    case OSDN_ERR_DTYPE: return "unsupported io dtype";
+    case OSDN_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case OSDN_ERR_WORKSPACE: return "workspace NULL or too small";
+    case OSDN_ERR_CUDA: return "CUDA runtime error";
+    case OSDN_ERR_TIMEOUT: return "device wait timed out";
+    case OSDN_ERR_DEVICE: return "device-side consistency check failed";
+    case OSDN_ERR_ALIAS: return "output overlaps an input";
+    case OSDN_ERR_ARCH: return "device is not sm_103 (GB300)";
+    default: return "unknown status";
+    }
+}
+
+size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K) {
+    (void)B; (void)H; (void)T; (void)K;
+    return kStatusBytes;
+}
+
+size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V) {
+    (void)io; (void)B; (void)H; (void)T; (void)K; (void)V;
+    return kStatusBytes;
+}
+
+int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace) return OSDN_ERR_NULL;
+    if (workspace_bytes < kStatusBytes) return OSDN_ERR_WORKSPACE;
+    if (misaligned(workspace)) return OSDN_ERR_ALIGN;
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream) != cudaSuccess)
+        return OSDN_ERR_CUDA;
+    return OSDN_OK;
+}
+
+int osdn_check_status(const void *workspace, void *stream) {
+    if (!workspace) return OSDN_ERR_NULL;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return OSDN_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return OSDN_ERR_CUDA;
+    return code;
+}
+
+int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const float *beta,
+                      const float *r, float eta, const float *d0, void *ktilde, float *dT,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K)) return OSDN_ERR_DIMS;
+    if (!workspace) return OSDN_ERR_WORKSPACE;
+    if (workspace_bytes < osdn_precond_scan_workspace_bytes(B, H, T, K)) return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (T > 0 && (!k || !beta || !ktilde)) return OSDN_ERR_NULL;
+    if (misaligned(k) || misaligned(beta) || misaligned(r) || misaligned(d0) ||
+        misaligned(ktilde) || misaligned(dT) || misaligned(workspace))
+        return OSDN_ERR_ALIGN;
+    const size_t kbytes = BH * (size_t)T * K * io_bytes(io);
+    if (overlap(k, kbytes, ktilde, kbytes) || overlap(dT, BH * K * 4, ktilde, kbytes) ||
+        overlap(dT, BH * K * 4, k, kbytes))
+        return OSDN_ERR_ALIAS;
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaError_t e = osdn::precond_scan_launch(io, (int)BH, T, K, k, beta, r, eta, d0, ktilde, dT,
+                                              static_cast<int *>(workspace), (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                   const void *ktilde, const void *v, const float *beta, const float *alpha,
+                   const float *S0, void *o, float *ST, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (!workspace) return OSDN_ERR_WORKSPACE;
+    if (workspace_bytes < osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V))
+        return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (T > 0 && (!q || !k || !ktilde || !v || !beta || !o)) return OSDN_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(ktilde) || misaligned(v) ||
+        misaligned(beta) || misaligned(alpha) || misaligned(S0) || misaligned(o) ||
+        misaligned(ST) || misaligned(workspace))
+        return OSDN_ERR_ALIGN;
+    const size_t es = io_bytes(io);
+    const size_t kb = BH * (size_t)T * K * es, vb = BH * (size_t)T * V * es;
+    const size_t sb = BH * (size_t)V * K * 4, gb = BH * (size_t)T * 4;
+    const void *ins[7] = {q, k, ktilde, v, beta, alpha, S0};
+    const size_t insz[7] = {kb, kb, kb, vb, gb, gb, sb};
+    for (int i = 0; i < 7; ++i)
+        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]))
+            return OSDN_ERR_ALIAS;
+    if (overlap(o, vb, ST, sb)) return OSDN_ERR_ALIAS;
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaError_t e;
+    if (T == 0)
+        e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, (cudaStream_t)stream);
+    else
+        e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
+                                    (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+}  // extern "C"

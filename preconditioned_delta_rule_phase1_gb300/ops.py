@@ -1,0 +1,180 @@
+"""Thin ctypes binding of ``libosdn.so`` (include/osdn.h).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels behind the C ABI.  PyTorch provides device memory and the stream.
+There is no CPU path: if the library is not built, or the tensors are not
+on a CUDA device, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+OSDN_F32, OSDN_BF16 = 0, 1
+STATUS_BYTES = 256
+_lock = threading.Lock()
+_lib = None
+
+_SIGS = {
+    "osdn_version": (ctypes.c_int, []),
+    "osdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "osdn_precond_scan_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 4),
+    "osdn_chunk_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "osdn_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_check_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "osdn_precond_scan": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
+                          [ctypes.c_float] + [ctypes.c_void_p] * 4 +
+                          [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_chunk_fwd": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
+                       [ctypes.c_size_t, ctypes.c_void_p]),
+}
+
+
+class OsdnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (where, status_string(code), code))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError("libosdn.so is not built (%s): run "
+                                   "`python -m preconditioned_delta_rule_phase1_gb300.build`" % path)
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype, fn.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().osdn_status_string(int(code)).decode()
+
+
+def _io(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return OSDN_F32
+    if t.dtype == torch.bfloat16:
+        return OSDN_BF16
+    raise TypeError("io tensors must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("OSDN operates on CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("OSDN needs contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise OsdnError(code, where)
+
+
+class Workspace:
+    """A caller-owned device workspace (status word + per-call scratch)."""
+
+    def __init__(self, nbytes: int = STATUS_BYTES, device=None, stream=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self.ensure(max(nbytes, STATUS_BYTES), stream)
+
+    def ensure(self, nbytes: int, stream=None):
+        if self.buf.numel() < nbytes:
+            old = self.buf
+            self.buf = torch.zeros(((nbytes + 255) // 256) * 256, dtype=torch.uint8,
+                                   device=self.device)
+            if old.numel() >= STATUS_BYTES:  # keep a sticky status already raised
+                self.buf[:STATUS_BYTES].copy_(old[:STATUS_BYTES])
+        return self
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+    def reset(self, stream=None):
+        _check(lib().osdn_workspace_init(self.ptr, self.nbytes, _stream(stream)), "workspace_init")
+
+    def status(self, stream=None) -> int:
+        return lib().osdn_check_status(self.ptr, _stream(stream))
+
+
+def precond_scan_workspace_bytes(B, H, T, K) -> int:
+    return int(lib().osdn_precond_scan_workspace_bytes(B, H, T, K))
+
+
+def chunk_fwd_workspace_bytes(io, B, H, T, K, V) -> int:
+    return int(lib().osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V))
+
+
+def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, workspace=None,
+                 stream=None):
+    """Phase 1 (osdn_precond_scan): returns (ktilde, dT)."""
+    B, H, T, K = k.shape
+    io = _io(k)
+    if ktilde is None:
+        ktilde = torch.empty_like(k)
+    if dT is None:
+        dT = torch.empty(B, H, K, dtype=torch.float32, device=k.device)
+    ws = workspace or Workspace(device=k.device)
+    ws.ensure(precond_scan_workspace_bytes(B, H, T, K))
+    code = lib().osdn_precond_scan(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r), float(eta),
+                                   _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr, ws.nbytes,
+                                   _stream(stream))
+    _check(code, "osdn_precond_scan")
+    return ktilde, dT
+
+
+def chunk_fwd(q, k, ktilde, v, beta, alpha=None, S0=None, o=None, ST=None, workspace=None,
+              stream=None):
+    """Phase 2 (osdn_chunk_fwd): returns (o, ST)."""
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    io = _io(k)
+    if o is None:
+        o = torch.empty(B, H, T, V, dtype=k.dtype, device=k.device)
+    if ST is None:
+        ST = torch.empty(B, H, V, K, dtype=torch.float32, device=k.device)
+    ws = workspace or Workspace(device=k.device)
+    ws.ensure(chunk_fwd_workspace_bytes(io, B, H, T, K, V))
+    code = lib().osdn_chunk_fwd(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v),
+                                _ptr(beta), _ptr(alpha), _ptr(S0), _ptr(o), _ptr(ST), ws.ptr,
+                                ws.nbytes, _stream(stream))
+    _check(code, "osdn_chunk_fwd")
+    return o, ST
+
+
+def forward(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, workspace=None,
+            stream=None):
+    """Both phases: returns (ktilde, dT, o, ST)."""
+    ws = workspace or Workspace(device=k.device)
+    ktilde, dT = precond_scan(k, beta, r, eta, d0, workspace=ws, stream=stream)
+    o, ST = chunk_fwd(q, k, ktilde, v, beta, alpha, S0, workspace=ws, stream=stream)
+    return ktilde, dT, o, ST

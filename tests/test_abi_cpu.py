@@ -1,0 +1,91 @@
+"""The C-ABI library loads, exports every symbol include/osdn.h declares, and
+rejects bad arguments on the host before touching the device.  No compute
+call runs here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from preconditioned_delta_rule_phase1_gb300 import build as osdn_build
+from preconditioned_delta_rule_phase1_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    osdn_build.build()
+    return ops.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(osdn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "osdn_precond_scan" in names and "osdn_chunk_fwd" in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    assert ops.status_string(0) == "ok"
+    for code in range(-1, -11, -1):
+        s = ops.status_string(code)
+        assert s and s != "unknown status", code
+    assert ops.status_string(12345) == "unknown status"
+    assert L.osdn_version() >= 100
+
+
+def test_workspace_sizes(L):
+    assert ops.precond_scan_workspace_bytes(2, 16, 8192, 128) >= 256
+    assert ops.chunk_fwd_workspace_bytes(1, 2, 16, 8192, 128, 128) >= 256
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+def scan(L, io=1, B=1, H=1, T=8, K=64, k=FAKE, beta=FAKE, r=None, d0=None, kt=2 * FAKE,
+         dT=None, ws=3 * FAKE, wsb=256):
+    return L.osdn_precond_scan(io, B, H, T, K, k, beta, r, 0.1, d0, kt, dT, ws, wsb, None)
+
+
+def chunk(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, kt=3 * FAKE, v=4 * FAKE,
+          beta=5 * FAKE, alpha=None, S0=None, o=6 * FAKE, ST=None, ws=7 * FAKE, wsb=256):
+    return L.osdn_chunk_fwd(io, B, H, T, K, V, q, k, kt, v, beta, alpha, S0, o, ST, ws, wsb, None)
+
+
+def test_host_validation_precond_scan(L):
+    assert scan(L, io=7) == -3
+    assert scan(L, K=96) == -2 and scan(L, K=32) == -2 and scan(L, T=-1) == -2
+    assert scan(L, ws=None) == -5 and scan(L, wsb=8) == -5
+    assert scan(L, k=None) == -1 and scan(L, beta=None) == -1 and scan(L, kt=None) == -1
+    assert scan(L, k=FAKE + 4) == -4 and scan(L, d0=FAKE + 8) == -4
+    assert scan(L, kt=FAKE) == -9          # ktilde aliases k
+    assert scan(L, B=0) == 0               # empty batch: nothing to do
+
+
+def test_host_validation_chunk_fwd(L):
+    assert chunk(L, io=2) == -3
+    assert chunk(L, V=32) == -2 and chunk(L, H=-2) == -2
+    assert chunk(L, q=None) == -1 and chunk(L, o=None) == -1
+    assert chunk(L, v=4 * FAKE + 2) == -4
+    assert chunk(L, o=FAKE) == -9          # o aliases q
+    assert chunk(L, wsb=0) == -5
+    assert chunk(L, H=0) == 0
+
+
+def test_no_gpu_means_cuda_error_not_crash(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert scan(L) in (-6, -10)
+    assert chunk(L) in (-6, -10)

@@ -1,0 +1,134 @@
+"""GPU-vs-oracle parity through the C ABI.
+
+Every output of both phases (ktilde, d_T, o, S_T) is compared element by
+element with the fp64 oracle on the same seeded inputs, within the
+normwise tolerance of the I/O type (1e-4 fp32, 2e-2 bf16).  The five named
+workloads run at full size on the GPU; the oracle checks a sample of their
+sequences.  Small shapes cover every chunk-tail case and the optional
+inputs.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from preconditioned_delta_rule_phase1_gb300 import build as osdn_build
+from preconditioned_delta_rule_phase1_gb300 import ops, synth
+from tests._util import TOL, oracle_forward, pick, rel_err, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    osdn_build.build()
+    ops.lib()
+
+
+def run_gpu(x, ws=None):
+    g = to_cuda(x)
+    ws = ws or ops.Workspace()
+    kt, dT, o, ST = ops.forward(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"],
+                                g["alpha"], g["S0"], workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, ops.status_string(ws.status())
+    return kt, dT, o, ST
+
+
+def check_all(x, io, heads=None, label=""):
+    kt, dT, o, ST = run_gpu(x)
+    okt, odT, oo, oST = oracle_forward(x, heads)
+    sel = (lambda t: pick(t, heads)) if heads is not None else (lambda t: t)
+    tol = TOL[io]
+    errs = {"ktilde": rel_err(sel(kt), okt), "dT": rel_err(sel(dT), odT),
+            "o": rel_err(sel(o), oo), "ST": rel_err(sel(ST), oST)}
+    for name, e in errs.items():
+        assert e <= tol, "%s %s: %.3e > %.1e (%s)" % (label, name, e, tol, errs)
+    # Phase 2 alone, fed the GPU's own (io-rounded) ktilde
+    xs = synth.slice_heads(x, heads) if heads is not None else x
+    o2, ST2 = oracle.delta_fwd(xs["q"], xs["k"], sel(kt).cpu(), xs["v"], xs["beta"],
+                               xs["alpha"], xs["S0"])
+    assert rel_err(sel(o), o2) <= tol and rel_err(sel(ST), ST2) <= tol, label
+    return errs
+
+
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_workload_parity_full_size(name):
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    BH = w.B * w.H
+    heads = None if BH * w.T <= 4096 else sorted({0, BH // 2, BH - 1})
+    errs = check_all(x, w.io, heads, name)
+    print(name, {k: "%.2e" % v for k, v in errs.items()})
+
+
+SHAPES = [1, 15, 63, 64, 65, 127, 200]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("T", SHAPES)
+def test_chunk_tails(io, T):
+    for K, V in itertools.product([64, 128], [64, 128]):
+        x = synth.make_random(2, 3, T, K, V, io=io, apf=True, gated=(T % 2 == 1), s0=True,
+                              d0=True, seed=T + K + V)
+        check_all(x, io, None, "%s T=%d K=%d V=%d" % (io, T, K, V))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_optional_inputs_null(io):
+    # r, alpha, S0, d0 all NULL: the plain OSDN recurrence from d0 = 1, S0 = 0
+    x = synth.make_random(1, 4, 300, 128, 64, io=io, seed=11)
+    check_all(x, io, None, "null optionals")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_state_chaining_on_gpu(io):
+    x = synth.make_random(1, 2, 400, 64, 128, io=io, apf=True, gated=True, s0=True, seed=12)
+    g = to_cuda(x)
+    kt, dT, o, ST = ops.forward(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], None,
+                                g["alpha"], g["S0"])
+    T1 = 137
+    cut = lambda t, lo, hi: t[:, :, lo:hi].contiguous()
+    kt1, dT1, o1, ST1 = ops.forward(cut(g["q"], 0, T1), cut(g["k"], 0, T1), cut(g["v"], 0, T1),
+                                    cut(g["beta"], 0, T1), cut(g["r"], 0, T1), g["eta"], None,
+                                    cut(g["alpha"], 0, T1), g["S0"])
+    kt2, dT2, o2, ST2 = ops.forward(cut(g["q"], T1, 400), cut(g["k"], T1, 400),
+                                    cut(g["v"], T1, 400), cut(g["beta"], T1, 400),
+                                    cut(g["r"], T1, 400), g["eta"], dT1,
+                                    cut(g["alpha"], T1, 400), ST1)
+    tol = TOL[io]
+    assert rel_err(torch.cat([kt1, kt2], 2), kt.double().cpu().numpy()) <= tol
+    assert rel_err(torch.cat([o1, o2], 2), o.double().cpu().numpy()) <= tol
+    assert rel_err(dT2, dT.double().cpu().numpy()) <= tol
+    assert rel_err(ST2, ST.double().cpu().numpy()) <= tol
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_deterministic_bitwise(io):
+    x = synth.make_random(2, 2, 333, 128, 128, io=io, apf=True, gated=True, s0=True, seed=13)
+    a = run_gpu(x)
+    b = run_gpu(x)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_empty_sequence_copies_initial_state(io):
+    x = synth.make_random(1, 3, 0, 64, 64, io=io, s0=True, d0=True, seed=14)
+    g = to_cuda(x)
+    kt, dT, o, ST = ops.forward(g["q"], g["k"], g["v"], g["beta"], None, 0.1, g["d0"], None,
+                                g["S0"])
+    torch.cuda.synchronize()
+    assert torch.equal(dT, g["d0"]) and torch.equal(ST, g["S0"])
+    assert kt.numel() == 0 and o.numel() == 0
+
+
+def test_alias_rejected_before_launch():
+    x = to_cuda(synth.make_random(1, 1, 16, 64, 64, io="bf16", seed=15))
+    with pytest.raises(ops.OsdnError) as ei:
+        ops.precond_scan(x["k"], x["beta"], ktilde=x["k"])
+    assert ei.value.code == -9
