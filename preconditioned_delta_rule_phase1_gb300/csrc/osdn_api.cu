@@ -16,6 +16,9 @@ cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q
                               const void *kt, const void *v, const float *beta,
                               const float *alpha, const float *S0, void *o, float *ST,
                               cudaStream_t stream);
+cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                            const void *kt, const void *v, const float *beta, const float *alpha,
+                            const float *S0, void *o, float *ST, int *status, cudaStream_t stream);
 }  // namespace osdn
 
 namespace {
@@ -151,7 +154,10 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
     cudaError_t e;
     if (T == 0)
         e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, (cudaStream_t)stream);
-    else
+    else if (io == OSDN_BF16)  // tensor cores: bf16 operands, fp32 accumulation
+        e = osdn::delta_tc_launch((int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
+                                  static_cast<int *>(workspace), (cudaStream_t)stream);
+    else  // fp32 I/O: fp32 FFMA (tensor-core operand rounding would not meet fp32 accuracy)
         e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
                                     (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
