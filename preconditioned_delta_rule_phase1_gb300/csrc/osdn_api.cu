@@ -9,7 +9,8 @@
 namespace osdn {
 cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
                                 const float *r, float eta, const float *d0, void *ktilde,
-                                float *dT, int *status, cudaStream_t stream);
+                                float *dT, void *scratch, int *status, cudaStream_t stream);
+size_t precond_scratch_bytes(int BH, int T, int K);
 cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,
                               cudaStream_t stream);
 cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
@@ -73,8 +74,8 @@ const char *osdn_status_string(int code) {
 }
 
 size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K) {
-    (void)B; (void)H; (void)T; (void)K;
-    return kStatusBytes;
+    if (B < 0 || H < 0 || T < 0 || !width_ok(K)) return kStatusBytes;
+    return kStatusBytes + osdn::precond_scratch_bytes(B * H, T, K);
 }
 
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V) {
@@ -119,8 +120,10 @@ int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const f
         return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
+    void *scratch = static_cast<char *>(workspace) + kStatusBytes;
     cudaError_t e = osdn::precond_scan_launch(io, (int)BH, T, K, k, beta, r, eta, d0, ktilde, dT,
-                                              static_cast<int *>(workspace), (cudaStream_t)stream);
+                                              scratch, static_cast<int *>(workspace),
+                                              (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

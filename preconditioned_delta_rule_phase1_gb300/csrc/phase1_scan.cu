@@ -1,87 +1,348 @@
 // phase1_scan.cu -- Phase 1 of OSDN: the O(K) preconditioner scan over the
 // key stream (gist.science summary of arXiv 2605.13473, sections 2.2-2.3).
 //
-// Per sequence (b,h) and token t, with w_t = k_t (.) k_t, n_t = ||k_t||^2 and
-// a_t = <d_t, w_t>:
+// Per sequence and token t, with w_t = k_t (.) k_t and n_t = ||k_t||^2:
 //     ktilde_t = d_t (.) k_t
-//     d_{t+1}  = r_t d_t + e_t w_t,   e_t = eta beta_t (1 - beta_t a_t) / n_t
-// (e_t = 0 for a zero key), i.e. a descent step on the closed-form surrogate
-// h_t(d) = ((1 - beta_t <d, w_t>)^2 - 1) / (2 n_t) with retention r_t.
+//     d_{t+1}  = r_t d_t + e_t w_t,   e_t = c_t (1 - beta_t <d_t, w_t>),
+//     c_t      = eta beta_t / n_t      (c_t = 0 for a zero key)
+// i.e. a descent step on h_t(d) = ((1 - beta_t <d, w_t>)^2 - 1) / (2 n_t)
+// with retention r_t.
 //
-// Kernel: one warp per sequence.  Lane l owns the K/32 consecutive key
-// columns [l*K/32, (l+1)*K/32) of d, k and ktilde, so every token is one
-// coalesced K-wide load of k and store of ktilde.  n_t and a_t are reduced
-// together by a shuffle butterfly; the serial chain per token is that
-// reduction plus two FMAs.  The gates of 32 tokens are fetched with one
-// coalesced load and broadcast by shuffle.
+// Chunked evaluation (16 tokens per step; exact algebra, no approximation).
+// Inside a chunk starting from d, with p_t = <d, w_t>, G_tu = <w_t, w_u>,
+// rho_t = prod_{v<t} r_v and pi_ut = prod_{u<v<t} r_v:
+//     <d_t, w_t> = rho_t p_t + sum_{u<t} pi_ut e_u G_tu
+// so the 16 scalars e_t follow from one lower-triangular substitution,
+//     e_t = c_t (1 - beta_t rho_t p_t) - c_t beta_t sum_{u<t} pi_ut G_tu e_u,
+// after which every column of d steps through the chunk independently
+// (ktilde_t = d (.) k_t, d <- r_t d + e_t w_t).  The chain from one chunk to
+// the next is one K-wide reduction (p), the 16-step substitution and the
+// column updates.  G only enters through the small coupling c beta G, so it
+// is formed on the tensor cores (mma.sync, tf32 inputs, fp32 accumulation);
+// p and n, which enter e directly, are reduced in fp32.
+//
+// Time segments.  With a retention gate the map d -> d_{t+1} contracts, so a
+// segment can start from a state estimated by running the scan over the W
+// tokens before it from d = 0 ("warm-up").  Every segment records its
+// estimated start and its end state; a second kernel checks each start
+// against the predecessor's end (exact by induction from d_0) and recomputes
+// any segment whose estimate is off by more than 2^-21 relative, or all
+// segments after a token whose one-step map could expand (||A_t||_2 > 1).
+// The result is therefore the exact recurrence to fp32 rounding on every
+// input; speculation only decides how much runs in parallel.
 #include "osdn_device.cuh"
 
 namespace osdn {
+namespace p1 {
 
-template <int E> struct Vec;
-template <> struct Vec<2> {
-    template <typename T> __device__ static void ld(const T *p, float (&x)[2]) { load2(p, x); }
-    template <typename T> __device__ static void st(T *p, const float (&x)[2]) { store2(p, x); }
-};
-template <> struct Vec<4> {
-    template <typename T> __device__ static void ld(const T *p, float (&x)[4]) { load4(p, x); }
-    template <typename T> __device__ static void st(T *p, const float (&x)[4]) { store4(p, x); }
-};
+constexpr int C = 16;          // tokens per chunk
+constexpr int NSTAGE = 4;      // key chunks in flight
+constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment
+constexpr float kRelTol = 4.76837158203125e-07f;  // 2^-21
 
 template <typename io_t, int K>
-__global__ void __launch_bounds__(128)
-precond_scan_warp_kernel(int BH, int T, const io_t *__restrict__ k, const float *__restrict__ beta,
-                         const float *__restrict__ r, float eta, const float *__restrict__ d0,
-                         io_t *__restrict__ ktilde, float *__restrict__ dT) {
-    constexpr int E = K / 32;
-    const int seq = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (seq >= BH) return;
+struct Smem {
+    static constexpr int NW = K / 32;
+    io_t keys[NSTAGE][C][K];
+    float gb[NSTAGE][C], gr[NSTAGE][C];   // beta, r of the staged chunk
+    float wS[C][K + 4];                   // w = k^2 for the Gram fragments
+    float gpart[NW][C][C + 1];            // per-warp partial Gram
+    float part[NW][2 * C];                // per-warp partial p (0..15) and n (16..31)
+    float sE[C], sR[C];
+    float red[NW][2];
+    int flag;
+};
 
-    const size_t base = (size_t)seq * T * K + (size_t)lane * E;
-    const io_t *kp = k + base;
-    io_t *ktp = ktilde + base;
-    const float *bp = beta + (size_t)seq * T;
-    const float *rp = r ? r + (size_t)seq * T : nullptr;
+struct Params {
+    int BH, T, L, nseg;
+    const void *k;
+    const float *beta, *r, *d0;
+    float eta;
+    void *ktilde;
+    float *dT;
+    float *ws_start, *ws_end;   // [BH][nseg][K]
+    int *ws_flag;               // [BH][nseg]
+    int *status;
+};
 
-    float d[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) d[e] = d0 ? d0[(size_t)seq * K + lane * E + e] : 1.0f;
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const int sz = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(src), "r"(sz)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const int sz = valid ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(src), "r"(sz)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
-    for (int t0 = 0; t0 < T; t0 += 32) {
-        const int tn = min(32, T - t0);
-        const float b_l = lane < tn ? bp[t0 + lane] : 0.0f;
-        const float r_l = (rp && lane < tn) ? rp[t0 + lane] : 1.0f;
-#pragma unroll 4
-        for (int i = 0; i < tn; ++i) {
-            const size_t off = (size_t)(t0 + i) * K;
-            float kv[E];
-            Vec<E>::ld(kp + off, kv);
-            const float bt = __shfl_sync(kFullMask, b_l, i);
-            const float rt = __shfl_sync(kFullMask, r_l, i);
-            float w[E], kt[E], n = 0.0f, a = 0.0f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                w[e] = kv[e] * kv[e];
-                n += w[e];
-                a = fmaf(d[e], w[e], a);
-                kt[e] = d[e] * kv[e];
+// Scan tokens [tb, te) of sequence `seq` starting from the state in `d`
+// (this thread's column); ktilde is written for tokens >= te_emit0.  Returns
+// the state after te in `d`.  Sets sm.flag if some token's one-step map
+// could expand.  All K threads of the CTA call this together.
+template <typename io_t, int K>
+__device__ void scan_range(const Params &p, Smem<io_t, K> &sm, int seq, int tb, int tseg, int te,
+                           float &d) {
+    constexpr int NW = K / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const io_t *kseq = static_cast<const io_t *>(p.k) + (size_t)seq * p.T * K;
+    io_t *ktseq = static_cast<io_t *>(p.ktilde) + (size_t)seq * p.T * K;
+    const float *bseq = p.beta + (size_t)seq * p.T;
+    const float *rseq = p.r ? p.r + (size_t)seq * p.T : nullptr;
+    const int nc = (te - tb + C - 1) / C;
+
+    auto issue = [&](int j) {
+        if (j < nc) {
+            const int s = j % NSTAGE, t0 = tb + j * C;
+            constexpr int PER_ROW = K * (int)sizeof(io_t) / 16;   // 16-byte pieces per key row
+            for (int i = tid; i < C * PER_ROW; i += K) {
+                const int t = i / PER_ROW, pc = i % PER_ROW;
+                const bool valid = t0 + t < te;
+                const io_t *src = valid ? kseq + (size_t)(t0 + t) * K + pc * (16 / sizeof(io_t)) : kseq;
+                cp_async16(&sm.keys[s][t][pc * (16 / sizeof(io_t))], src, valid);
             }
-            Vec<E>::st(ktp + off, kt);
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) {
-                n += __shfl_xor_sync(kFullMask, n, m);
-                a += __shfl_xor_sync(kFullMask, a, m);
+            if (tid < C) {
+                const bool valid = t0 + tid < te;
+                cp_async4(&sm.gb[s][tid], valid ? bseq + t0 + tid : bseq, valid);
+            } else if (tid < 2 * C && rseq) {
+                const int t = tid - C;
+                const bool valid = t0 + t < te;
+                cp_async4(&sm.gr[s][t], valid ? rseq + t0 + t : rseq, valid);
             }
-            const float et = n > 0.0f ? eta * bt * (1.0f - bt * a) / n : 0.0f;
+        }
+        cp_commit();
+    };
 #pragma unroll
-            for (int e = 0; e < E; ++e) d[e] = fmaf(rt, d[e], et * w[e]);
+    for (int j = 0; j < NSTAGE - 1; ++j) issue(j);
+
+    for (int j = 0; j < nc; ++j) {
+        issue(j + NSTAGE - 1);
+        cp_wait<NSTAGE - 1>();
+        __syncthreads();
+        const int s = j % NSTAGE, t0 = tb + j * C;
+        const int nv = min(C, te - t0);
+
+        // ---- 1. this column of the chunk; p and n partials ---------------------
+        float kv[C], w[C];
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+            kv[t] = to_f32(sm.keys[s][t][tid]);
+            w[t] = kv[t] * kv[t];
+            sm.wS[t][tid] = w[t];
+        }
+        {
+            // transpose-reduce 32 partials across the warp: lane l ends with index l
+            float v[2 * C];
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                v[t] = d * w[t];
+                v[C + t] = w[t];
+            }
+#pragma unroll
+            for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
+                const bool hi = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    const float keep = hi ? v[i + n] : v[i];
+                    const float send = hi ? v[i] : v[i + n];
+                    v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
+                }
+            }
+            sm.part[warp][lane] = v[0];
+        }
+        __syncthreads();
+
+        // ---- 2. partial Gram of this warp's 32 key columns (tensor cores) -------
+        {
+            const int g = lane >> 2, tq = lane & 3;
+            float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int k0 = warp * 32 + ks * 8;
+                uint32_t a[4];
+                a[0] = to_tf32(sm.wS[g][k0 + tq]);
+                a[1] = to_tf32(sm.wS[g + 8][k0 + tq]);
+                a[2] = to_tf32(sm.wS[g][k0 + tq + 4]);
+                a[3] = to_tf32(sm.wS[g + 8][k0 + tq + 4]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t b0 = to_tf32(sm.wS[8 * nt + g][k0 + tq]);
+                    const uint32_t b1 = to_tf32(sm.wS[8 * nt + g][k0 + tq + 4]);
+                    mma_tf32(acc[nt], a, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                sm.gpart[warp][g][8 * nt + 2 * tq] = acc[nt][0];
+                sm.gpart[warp][g][8 * nt + 2 * tq + 1] = acc[nt][1];
+                sm.gpart[warp][g + 8][8 * nt + 2 * tq] = acc[nt][2];
+                sm.gpart[warp][g + 8][8 * nt + 2 * tq + 1] = acc[nt][3];
+            }
+        }
+        __syncthreads();
+
+        // ---- 3. the 16 coefficients e_t (warp 0, lane t) -------------------------
+        if (warp == 0) {
+            const int t = lane & (C - 1);
+            float pt = 0.f, nt_ = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                pt += sm.part[ww][t];
+                nt_ += sm.part[ww][C + t];
+            }
+            const float bt = sm.gb[s][t];
+            const float rt = rseq ? sm.gr[s][t] : 1.0f;
+            const float ct = nt_ > 0.0f ? p.eta * bt / nt_ : 0.0f;
+            // coupling row t: coef_u = c_t beta_t pi_ut G_tu (u < t); rho_t
+            float coef[C];
+            float pi = 1.0f;
+#pragma unroll
+            for (int u = C - 1; u >= 0; --u) {
+                float gtu = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < NW; ++ww) gtu += sm.gpart[ww][t][u];
+                coef[u] = (u < t) ? ct * bt * pi * gtu : 0.0f;
+                if (u < t) pi *= (rseq ? sm.gr[s][u] : 1.0f);
+            }
+            const float rho = pi;  // prod_{v < t} r_v
+            // can this token's one-step map expand?  ||A_t|| = max(|r|, |r - lambda|)
+            {
+                float gtt = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < NW; ++ww) gtt += sm.gpart[ww][t][t];
+                const float lam = nt_ > 0.0f ? p.eta * bt * bt * gtt / nt_ : 0.0f;
+                const float nrm = fmaxf(fabsf(rt), fabsf(rt - lam));
+                if (lane < C && t < nv && nrm > 1.0f + 1e-6f) sm.flag = 1;
+            }
+            float acc = ct * (1.0f - bt * rho * pt);
+#pragma unroll
+            for (int u = 0; u < C; ++u) {
+                const float eu = __shfl_sync(kFullMask, acc, u);
+                if (t > u) acc = fmaf(-coef[u], eu, acc);
+            }
+            if (lane < C) {
+                sm.sE[t] = t < nv ? acc : 0.0f;
+                sm.sR[t] = rt;
+            }
+        }
+        __syncthreads();
+
+        // ---- 4. this column through the chunk; emit ktilde ----------------------
+        const bool emit = t0 >= tseg;
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+            if (t < nv) {
+                if (emit) from_f32(ktseq[(size_t)(t0 + t) * K + tid], d * kv[t]);
+                d = fmaf(sm.sR[t], d, sm.sE[t] * w[t]);
+            }
         }
     }
-    if (dT) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) dT[(size_t)seq * K + lane * E + e] = d[e];
+    cp_wait<0>();
+    __syncthreads();
+}
+
+// Grid (nseg, BH): segment `seg` of sequence `seq`.
+template <typename io_t, int K>
+__global__ void __launch_bounds__(K) precond_segment_kernel(Params p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem<io_t, K> &sm = *reinterpret_cast<Smem<io_t, K> *>(smem_raw);
+    const int seg = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
+    if (tid == 0) sm.flag = 0;
+    const int tseg = seg * p.L;
+    const int te = min(p.T, tseg + p.L);
+    float d;
+    int tb;
+    if (seg == 0) {
+        d = p.d0 ? p.d0[(size_t)seq * K + tid] : 1.0f;
+        tb = 0;
+    } else {
+        d = 0.0f;  // speculative: the warm-up forgets this guess
+        tb = tseg - kWarm;
     }
+    __syncthreads();
+    if (seg > 0) {
+        scan_range<io_t, K>(p, sm, seq, tb, tseg, tseg, d);  // warm-up, nothing emitted
+    }
+    if (p.nseg > 1) p.ws_start[((size_t)seq * p.nseg + seg) * K + tid] = d;
+    scan_range<io_t, K>(p, sm, seq, tseg, tseg, te, d);
+    if (p.nseg > 1) {
+        p.ws_end[((size_t)seq * p.nseg + seg) * K + tid] = d;
+        if (tid == 0) p.ws_flag[(size_t)seq * p.nseg + seg] = sm.flag;
+    } else if (p.dT) {
+        p.dT[(size_t)seq * K + tid] = d;
+    }
+}
+
+// Grid (BH): verify every speculative segment start against its predecessor's
+// end; recompute (exactly) the segments that do not match; write d_T.
+template <typename io_t, int K>
+__global__ void __launch_bounds__(K) precond_verify_kernel(Params p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem<io_t, K> &sm = *reinterpret_cast<Smem<io_t, K> *>(smem_raw);
+    constexpr int NW = K / 32;
+    const int seq = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t base = (size_t)seq * p.nseg;
+    __shared__ int any_flag;
+    if (tid == 0) {
+        int f = 0;
+        for (int i = 0; i < p.nseg; ++i) f |= p.ws_flag[base + i];
+        any_flag = f;
+        sm.flag = 0;
+    }
+    __syncthreads();
+    const bool all_suspect = any_flag != 0;
+    float prev_end = p.ws_end[base * K + tid];
+    for (int i = 1; i < p.nseg; ++i) {
+        const float st = p.ws_start[(base + i) * K + tid];
+        float diff = fabsf(prev_end - st), mag = fabsf(st);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
+            mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
+        }
+        if (lane == 0) {
+            sm.red[warp][0] = diff;
+            sm.red[warp][1] = mag;
+        }
+        __syncthreads();
+        float dmax = 0.f, mmax = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) {
+            dmax = fmaxf(dmax, sm.red[ww][0]);
+            mmax = fmaxf(mmax, sm.red[ww][1]);
+        }
+        __syncthreads();
+        const bool ok = !all_suspect && dmax <= kRelTol * mmax;
+        float d = p.ws_end[(base + i) * K + tid];
+        if (!ok) {  // recompute segment i from the exact end of segment i-1
+            d = prev_end;
+            const int tseg = i * p.L, te = min(p.T, tseg + p.L);
+            scan_range<io_t, K>(p, sm, seq, tseg, tseg, te, d);
+            p.ws_end[(base + i) * K + tid] = d;
+        }
+        prev_end = d;
+    }
+    if (p.dT) p.dT[(size_t)seq * K + tid] = prev_end;
 }
 
 // T == 0: the final preconditioner is the initial one.
@@ -93,34 +354,81 @@ __global__ void copy_or_fill_kernel(size_t n, const float *__restrict__ src, flo
 }
 
 template <typename io_t, int K>
-static cudaError_t launch_precond_scan_warp(int BH, int T, const void *k, const float *beta,
-                                            const float *r, float eta, const float *d0,
-                                            void *ktilde, float *dT, cudaStream_t stream) {
-    const int threads = 128;
-    const int blocks = (BH * 32 + threads - 1) / threads;
-    precond_scan_warp_kernel<io_t, K><<<blocks, threads, 0, stream>>>(
-        BH, T, static_cast<const io_t *>(k), beta, r, eta, d0, static_cast<io_t *>(ktilde), dT);
+static cudaError_t launch(const Params &p, cudaStream_t stream) {
+    const int smem = (int)sizeof(Smem<io_t, K>);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    precond_segment_kernel<io_t, K><<<dim3(p.nseg, p.BH), K, smem, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.nseg == 1) return e;
+    precond_verify_kernel<io_t, K><<<p.BH, K, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace p1
+
+// Segment length: long enough that the warm-up costs little extra reading,
+// short enough to give the GPU a few waves of CTAs.  Only a retention gate
+// (r != NULL) makes the warm-up converge, so without one there is a single
+// segment per sequence.
+int precond_segments(int BH, int T, bool has_r, int *L_out) {
+    int L = T;
+    if (has_r && T > 2 * p1::kWarm) {
+        L = 1024;
+        if ((long long)BH * ((T + L - 1) / L) < 4LL * 152) L = 512;
+        if (L >= T) L = T;
+    }
+    if (L < 1) L = 1;
+    if (L_out) *L_out = L;
+    return (T + L - 1) / L;
+}
+
+size_t precond_scratch_bytes(int BH, int T, int K) {
+    int L;
+    const int nseg = precond_segments(BH, T, true, &L);
+    if (nseg <= 1) return 0;
+    const size_t n = (size_t)BH * nseg;
+    return n * K * 4 * 2 + ((n * 4 + 255) / 256) * 256;
 }
 
 cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
                                 const float *r, float eta, const float *d0, void *ktilde,
-                                float *dT, int *status, cudaStream_t stream) {
-    (void)status;
+                                float *dT, void *scratch, int *status, cudaStream_t stream) {
     if (T == 0) {
         if (!dT) return cudaSuccess;
         size_t n = (size_t)BH * K;
-        copy_or_fill_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(n, d0, 1.0f, dT);
+        p1::copy_or_fill_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(n, d0, 1.0f, dT);
         return cudaGetLastError();
     }
-    if (io == OSDN_BF16) {
-        if (K == 64)
-            return launch_precond_scan_warp<__nv_bfloat16, 64>(BH, T, k, beta, r, eta, d0, ktilde, dT, stream);
-        return launch_precond_scan_warp<__nv_bfloat16, 128>(BH, T, k, beta, r, eta, d0, ktilde, dT, stream);
-    }
-    if (K == 64)
-        return launch_precond_scan_warp<float, 64>(BH, T, k, beta, r, eta, d0, ktilde, dT, stream);
-    return launch_precond_scan_warp<float, 128>(BH, T, k, beta, r, eta, d0, ktilde, dT, stream);
+    p1::Params p;
+    p.BH = BH;
+    p.T = T;
+    p.nseg = precond_segments(BH, T, r != nullptr, &p.L);
+    p.k = k;
+    p.beta = beta;
+    p.r = r;
+    p.d0 = d0;
+    p.eta = eta;
+    p.ktilde = ktilde;
+    p.dT = dT;
+    p.status = status;
+    float *f = static_cast<float *>(scratch);
+    const size_t n = (size_t)BH * p.nseg;
+    p.ws_start = p.nseg > 1 ? f : nullptr;
+    p.ws_end = p.nseg > 1 ? f + n * K : nullptr;
+    p.ws_flag = p.nseg > 1 ? reinterpret_cast<int *>(f + 2 * n * K) : nullptr;
+    if (io == OSDN_BF16)
+        return K == 64 ? p1::launch<__nv_bfloat16, 64>(p, stream)
+                       : p1::launch<__nv_bfloat16, 128>(p, stream);
+    return K == 64 ? p1::launch<float, 64>(p, stream) : p1::launch<float, 128>(p, stream);
 }
 
 cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,
@@ -128,7 +436,7 @@ cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst
     if (n == 0 || !dst) return cudaSuccess;
     unsigned blocks = (unsigned)((n + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    copy_or_fill_kernel<<<blocks, 256, 0, stream>>>(n, src, fill, dst);
+    p1::copy_or_fill_kernel<<<blocks, 256, 0, stream>>>(n, src, fill, dst);
     return cudaGetLastError();
 }
 

@@ -132,3 +132,26 @@ def test_alias_rejected_before_launch():
     with pytest.raises(ops.OsdnError) as ei:
         ops.precond_scan(x["k"], x["beta"], ktilde=x["k"])
     assert ei.value.code == -9
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["converging", "slow_retention", "expansive_token", "short_tail"])
+def test_segmented_scan_exact(io, case):
+    """The time-segmented scan (used when a retention gate is given) equals the
+    token recurrence whether the speculative segment starts verify or must be
+    recomputed."""
+    T = 3001 if case == "short_tail" else 3000
+    x = synth.make_random(1, 4, T, 128, 64, io=io, apf=True, d0=True, seed=21)
+    if case == "slow_retention":      # warm-up cannot forget the guess: every start is repaired
+        x["r"] = torch.full_like(x["r"], 0.99995)
+    if case == "expansive_token":     # one map with ||A_t|| > 1: all segments recomputed
+        x["r"][:, :, 1700] = 1.5
+    g = to_cuda(x)
+    ws = ops.Workspace()
+    kt, dT = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    okt, odT = oracle.precond_scan(x["k"], x["beta"], x["r"], x["eta"], x["d0"])
+    tol = TOL[io]
+    assert rel_err(kt, okt) <= tol, rel_err(kt, okt)
+    assert rel_err(dT, odT) <= tol, rel_err(dT, odT)
