@@ -71,7 +71,9 @@ typedef enum {
     OSDN_ERR_TIMEOUT = -7,   /* device: a bounded wait ran out (status word)   */
     OSDN_ERR_DEVICE = -8,    /* device: an internal consistency check failed   */
     OSDN_ERR_ALIAS = -9,     /* an output overlaps an input it must not alias  */
-    OSDN_ERR_ARCH = -10      /* the current device is not sm_103 (GB300)       */
+    OSDN_ERR_ARCH = -10,     /* the current device is not sm_103 (GB300)       */
+    OSDN_ERR_SCRATCH = -11   /* osdn_precond_scan_noalloc: shape needs more
+                                scratch than its static buffer holds         */
 } osdn_status;
 
 /* Bytes of workspace osdn_precond_scan needs for this shape (>= 256). */
@@ -103,6 +105,32 @@ size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K);
 int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const float *beta,
                       const float *r, float eta, const float *d0, void *ktilde, float *dT,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Phase 1 without a workspace, for callers that cannot allocate device
+ * memory: code running where cudaMalloc is off limits (inside a region being
+ * captured under a memory pool that forbids new allocations, a plugin whose
+ * host owns every allocation, or a caller that must never fail with
+ * out-of-memory after start-up).  The paper has no counterpart to this call;
+ * it computes exactly what osdn_precond_scan computes, with the same
+ * arguments minus the workspace.
+ *
+ * Scratch: a file-scope device array of 2 MiB, present on every GPU that
+ * loads the library until the process exits.  The first call on a device
+ * resolves the array's device address there (cudaGetSymbolAddress), so that
+ * first call should be made before any stream capture.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Shapes whose speculative segments need more than 2 MiB of scratch (about
+ * B*H*ceil(T/L)*8*K bytes, L the segment length of 512 or 1024 tokens, and
+ * none without a retention gate) return OSDN_ERR_SCRATCH before anything is
+ * enqueued.  All calls share the array and it keeps the last call's
+ * contents: calls whose kernels may overlap on the GPU (unordered streams)
+ * race on it and must be serialised by the caller.  Kernels of this call
+ * report no device status word.
+ */
+int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
+                              const float *beta, const float *r, float eta, const float *d0,
+                              void *ktilde, float *dT, void *stream);
 
 /* Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256). */
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V);

@@ -11,6 +11,12 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
                                 const float *r, float eta, const float *d0, void *ktilde,
                                 float *dT, void *scratch, int *status, cudaStream_t stream);
 size_t precond_scratch_bytes(int BH, int T, int K);
+size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r);
+size_t precond_noalloc_capacity();
+cudaError_t precond_scan_noalloc_launch(int io, int BH, int T, int K, const void *k,
+                                        const float *beta, const float *r, float eta,
+                                        const float *d0, void *ktilde, float *dT,
+                                        cudaStream_t stream);
 cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,
                               cudaStream_t stream);
 cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
@@ -69,6 +75,7 @@ const char *osdn_status_string(int code) {
     case OSDN_ERR_DEVICE: return "device-side consistency check failed";
     case OSDN_ERR_ALIAS: return "output overlaps an input";
     case OSDN_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case OSDN_ERR_SCRATCH: return "problem needs more scratch than the static buffer holds";
     default: return "unknown status";
     }
 }
@@ -124,6 +131,31 @@ int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const f
     cudaError_t e = osdn::precond_scan_launch(io, (int)BH, T, K, k, beta, r, eta, d0, ktilde, dT,
                                               scratch, static_cast<int *>(workspace),
                                               (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
+                              const float *beta, const float *r, float eta, const float *d0,
+                              void *ktilde, float *dT, void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K)) return OSDN_ERR_DIMS;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (T > 0 && (!k || !beta || !ktilde)) return OSDN_ERR_NULL;
+    if (misaligned(k) || misaligned(beta) || misaligned(r) || misaligned(d0) ||
+        misaligned(ktilde) || misaligned(dT))
+        return OSDN_ERR_ALIGN;
+    const size_t kbytes = BH * (size_t)T * K * io_bytes(io);
+    if (overlap(k, kbytes, ktilde, kbytes) || overlap(dT, BH * K * 4, ktilde, kbytes) ||
+        overlap(dT, BH * K * 4, k, kbytes))
+        return OSDN_ERR_ALIAS;
+    if (osdn::precond_scratch_bytes_for((int)BH, T, K, r != nullptr) >
+        osdn::precond_noalloc_capacity())
+        return OSDN_ERR_SCRATCH;
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaError_t e = osdn::precond_scan_noalloc_launch(io, (int)BH, T, K, k, beta, r, eta, d0,
+                                                      ktilde, dT, (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

@@ -30,6 +30,8 @@
 // segments after a token whose one-step map could expand (||A_t||_2 > 1).
 // The result is therefore the exact recurrence to fp32 rounding on every
 // input; speculation only decides how much runs in parallel.
+#include <mutex>
+
 #include "osdn_device.cuh"
 
 namespace osdn {
@@ -429,6 +431,64 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
         return K == 64 ? p1::launch<__nv_bfloat16, 64>(p, stream)
                        : p1::launch<__nv_bfloat16, 128>(p, stream);
     return K == 64 ? p1::launch<float, 64>(p, stream) : p1::launch<float, 128>(p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the scan, for callers that may not allocate
+// device memory.  Its scratch (the speculative segment starts and ends) lives
+// in this file-scope device array instead of a caller workspace.  The array
+// exists on every GPU that loads the library until the process exits.  All
+// calls share it and it keeps the last call's contents; the scan writes every
+// entry it later reads, so nothing needs clearing between calls, but calls
+// whose kernels overlap on the GPU (different streams, no ordering) race on it.
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+size_t precond_noalloc_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch array on the current device.  Resolved once
+// per device (with that device current) on the first call there; host code
+// must not pass the array's name itself to a kernel.
+static cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t precond_scan_noalloc_launch(int io, int BH, int T, int K, const void *k,
+                                        const float *beta, const float *r, float eta,
+                                        const float *d0, void *ktilde, float *dT,
+                                        cudaStream_t stream) {
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    return precond_scan_launch(io, BH, T, K, k, beta, r, eta, d0, ktilde, dT, scratch, nullptr,
+                               stream);
+}
+
+// Bytes of scratch the scan needs for this call (0 without a retention gate).
+size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r) {
+    int L;
+    const int nseg = precond_segments(BH, T, has_r, &L);
+    if (nseg <= 1 || T == 0) return 0;
+    const size_t n = (size_t)BH * nseg;
+    return n * K * 4 * 2 + ((n * 4 + 255) / 256) * 256;
 }
 
 cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,

@@ -32,6 +32,8 @@ _SIGS = {
                           [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_chunk_fwd": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
                        [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_precond_scan_noalloc": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
+                                  [ctypes.c_float] + [ctypes.c_void_p] * 4),
 }
 
 
@@ -149,6 +151,21 @@ def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, worksp
                                    _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr, ws.nbytes,
                                    _stream(stream))
     _check(code, "osdn_precond_scan")
+    return ktilde, dT
+
+
+def precond_scan_noalloc(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, stream=None):
+    """Phase 1 through osdn_precond_scan_noalloc: no workspace, no device
+    allocation inside the call (outputs are allocated here only when not given)."""
+    B, H, T, K = k.shape
+    if ktilde is None:
+        ktilde = torch.empty_like(k)
+    if dT is None:
+        dT = torch.empty(B, H, K, dtype=torch.float32, device=k.device)
+    code = lib().osdn_precond_scan_noalloc(_io(k), B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
+                                           float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
+                                           _stream(stream))
+    _check(code, "osdn_precond_scan_noalloc")
     return ktilde, dT
 
 
