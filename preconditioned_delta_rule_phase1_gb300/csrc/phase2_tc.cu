@@ -8,26 +8,28 @@
 // Per chunk of C = 64 tokens, with g the inclusive within-chunk product of
 // alpha (g = 1 without decay), G_ij = g_i / g_j and S the state entering the
 // chunk:
-//   L  = tril(diag(b) (G . K Kt^T), -1),   X = (I + L)^-1
-//   U  = X diag(b) V - X diag(b g) K S^T           (the chunk's scaled residuals)
+//   L  = tril(diag(b) (G . K Kt^T), -1),   X = (I + L)^-1,   Xb = X diag(b)
+//   U  = Xb V - Xb diag(g) K S^T                    (the chunk's scaled residuals)
 //   O  = diag(g) Q S^T + tril(G . Q Kt^T) U
 //   S' = g_C S + U^T diag(g_C / g) Kt
 //
-// Work split: one CTA per (sequence, 64-row slice of S); 256 threads.  The
-// state slice lives in fp32 registers of the epilogue threads and in a bf16
-// copy in shared memory that feeds the MMAs; nothing of it leaves the SM
-// between chunks.  Products on the tensor cores, all bf16 x bf16 -> fp32 in
-// TMEM (M = rows of the accumulator):
-//   [K;Q] Kt^T   M=128 N=64   Gram (rows 0-63) and scores (rows 64-127)
-//   S Q^T        M=64  N=64   the inter-chunk part of O (transposed)
-//   K^T Xh^T     M=K   N=64   Kw^T, Xh = X diag(b g)
-//   V^T Xb^T     M=64  N=64   initialises U^T, Xb = X diag(b)
-//   -S Kw^T      M=64  N=64   accumulates U^T = (XbV - Kw S^T)^T
-//   Uh^T Kt      M=64  N=K    state increment, Uh = diag(g_C/g) U
-//   U^T A^T      M=64  N=64   the intra-chunk part of O, A = tril(G . Q Kt^T)
-// The unit lower-triangular inverse X is formed in fp32 by 16x16 blocks.
-// Input tiles (Q, K, Kt, V) arrive by TMA with 128-byte swizzle, double
-// buffered so the next chunk streams in while this one computes.
+// One CTA per (sequence, 64-row slice of S), 448 threads in four roles that
+// run concurrently and hand work over through mbarriers:
+//   warp 0      TMA producer: Q/Kt tiles (3-deep ring) and K/V tiles (2-deep
+//               ring), plus the chunk's gates (beta, cumulative log alpha);
+//   warp 1      MMA issuer (one thread): every tcgen05.mma and commit;
+//   warps 2-9   "prep", one chunk ahead of the chain: Gram and scores out of
+//               TMEM, L and the masked scores A, the diagonal gate scalings of
+//               Q, K and Kt in place, X = (I + L)^-1 (16x16 diagonal blocks in
+//               fp32, off-diagonal blocks with mma.sync tf32), Xb, and
+//               Kw^T = (Xb diag(g) K)^T back to shared memory;
+//   warps 10-13 "chain": U, the state S (fp32 accumulator in TMEM, bf16 copy
+//               in shared memory for the MMAs) and the output O.
+// Tensor-core products (bf16 operands, fp32 accumulation in TMEM):
+//   prep : K Kt^T, Q Kt^T (M=64, N=64);  K^T Xb^T -> Kw^T (M=K);  V^T Xb^T -> U^T init
+//   chain: U^T -= S Kw^T;  O^T = S Q^T;  S += U^T Kt;  O^T += U^T A^T   (M=64)
+// Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
+// status word and all roles leave their loops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,37 +39,56 @@
 namespace osdn {
 namespace tc {
 
-constexpr int C = 64;          // tokens per chunk
-constexpr int BV = 64;         // rows of S per CTA
-constexpr int kThreads = 256;
-constexpr int kLP = 65;        // fp32 pitch of the solver tiles
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int C = 64;     // tokens per chunk
+constexpr int BV = 64;    // rows of S per CTA
+constexpr int NS = 2;     // depth of the input ring (one slot per chunk)
+constexpr int kThreads = 448;
+constexpr int kPrepThreads = 256;
+constexpr int kChainThreads = 128;
+constexpr int kLP = 68;   // fp32 pitch of the solver tile
+constexpr uint32_t kWaitLimit = 1u << 15;      // sleeping polls before a wait gives up
+constexpr uint32_t kSleepNs = 1u << 16;         // longest sleep per poll (~65 us)
 
-// TMEM columns of the accumulators
-constexpr uint32_t kColG = 0, kColKw = 64, kColU = 128, kColO1 = 192, kColO2 = 256, kColDS = 320;
+// TMEM columns
+constexpr uint32_t kColG = 0;      // [K;Q] Kt^T (M=128): Gram rows 0-63, score rows 64-127
+constexpr uint32_t kColKw = 64;    // Kw^T (M=K)
+constexpr uint32_t kColU = 128;    // U^T, two buffers of 64 (M=64)
+constexpr uint32_t kColO = 256;    // O^T, two buffers of 64 (M=64)
+constexpr uint32_t kColS = 384;    // S (M=64, K columns)
 constexpr uint32_t kTmemCols = 512;
 
+// Input slot: [K;Q] stacked in 128-row blocks of 64 columns (K rows 0-63,
+// Q rows 64-127), then Kt (64-row blocks), then the value slice.
 template <int K>
-struct Smem {
-    // input stage (double buffered)
-    static constexpr int kKQ = 128 * K * 2;   // [K;Q] rows, K/64 blocks of 128 rows x 128 B
-    static constexpr int kKt = C * K * 2;     // Ktilde
-    static constexpr int kV = C * BV * 2;     // value slice
-    static constexpr int kStage = kKQ + kKt + kV;
-    // per-chunk operand tiles
-    static constexpr int oStage0 = 0;
-    static constexpr int oStage1 = kStage;
-    static constexpr int oXh = 2 * kStage;
-    static constexpr int oXb = oXh + C * C * 2;
-    static constexpr int oA = oXb + C * C * 2;
-    static constexpr int oKw = oA + C * C * 2;        // K rows x 128 B
-    static constexpr int oS = oKw + K * 128;          // BV rows, K/64 blocks of 8 KB
-    static constexpr int oU = oS + BV * K * 2;
-    static constexpr int oUh = oU + BV * C * 2;
-    static constexpr int oL = oUh + BV * C * 2;       // fp32 64 x 65
-    static constexpr int oX = oL + C * kLP * 4;
-    static constexpr int kBytes = oX + C * kLP * 4;
-    static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-byte alignment
+struct Lay {
+    static constexpr int kKQ = 128 * K * 2;
+    static constexpr int kKt = C * K * 2;
+    static constexpr int kV = C * BV * 2;
+    static constexpr int kSlot = kKQ + kKt + kV;
+    static constexpr int oKt = kKQ;                   // within a slot
+    static constexpr int oVv = kKQ + kKt;
+    static constexpr int oL = NS * kSlot;             // fp32 64 x kLP
+    static constexpr int oA = oL + C * kLP * 4;       // bf16 64 x 64, two buffers
+    static constexpr int oKw = oA + 2 * C * C * 2;    // bf16 K rows x 64
+    static constexpr int oXb = oKw + K * 128;         // bf16 64 x 64
+    static constexpr int oS = oXb + C * C * 2;        // bf16 BV x K
+    static constexpr int oU = oS + BV * K * 2;        // bf16 BV x 64 (also O staging)
+    static constexpr int kBytes = oU + BV * C * 2;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+struct Params {
+    int T, V, nchunks;
+    const float *beta, *alpha, *S0;
+    __nv_bfloat16 *o;
+    float *ST;
+    int *status;
+};
+
+struct Bars {
+    uint64_t full[NS], empty[NS];
+    uint64_t g_full, x1, x2, kw_full, x3, u_full, u_sm, s_full, s_ready;
+    uint64_t a_free[2], o_free[2];
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -75,14 +96,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Store n (multiple of 8) consecutive bf16 values of row r, columns
-// [c0, c0+n) inside one 64-column block, into a 128B-swizzled K-major tile
-// whose blocks hold `rows` rows.
+// n (multiple of 8) consecutive bf16 of row r, columns [c0, c0+n) within one
+// 64-column block, into a 128B-swizzled tile whose blocks hold `rows` rows.
 __device__ __forceinline__ void st_row_sw128(uint8_t *tile, int rows, int r, int c0,
                                              const float *vals, int n) {
     uint8_t *rowp = tile + (c0 >> 6) * rows * 128 + r * 128;
     const int cb = (c0 & 63) >> 3;
-#pragma unroll 4
+#pragma unroll
     for (int i = 0; i < n; i += 8) {
         uint4 pk;
         pk.x = pack_bf16x2(vals[i + 0], vals[i + 1]);
@@ -106,150 +126,215 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     }
 }
 
-// K-major operand, 128B swizzle: k-slice ks (16 elements) of a tile whose
-// 64-column blocks hold `rows` rows.
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int rows, int ks) {
     return ptx::sdesc(base + (ks >> 2) * rows * 128 + (ks & 3) * 32, 16, 1024, 2);
 }
-// MN-major operand, 128B swizzle: k-slice ks (16 rows of the stored tile);
-// consecutive 64-element MN blocks are `block_bytes` apart.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t base, int block_bytes, int ks) {
     return ptx::sdesc(base + ks * 2048, block_bytes, 1024, 2);
 }
 
-struct Params {
-    int T, V, nchunks;
-    const float *beta, *alpha, *S0;
-    __nv_bfloat16 *o;
-    float *ST;
-    int *status;
-};
+// Barrier over `count` threads of barrier `id` that also ANDs a predicate:
+// every participant gets the same answer, so a role leaves its loop together.
+__device__ __forceinline__ bool vote_all(bool v, int id, int count) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
+// Bounded wait that also gives up as soon as another thread has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         int *status) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort_flag) return false;
+    }
+    report_status(status, OSDN_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
+// --------------------------------------------------------------- mma.sync
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc (16x8 tile) += A[16 x k] * B[k x 8], fp32 row-major tiles of pitch kLP.
+__device__ __forceinline__ void warp_mm(float (&acc)[4], const float *A, const float *B, int k,
+                                        int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+    for (int k0 = 0; k0 < k; k0 += 8) {
+        uint32_t a[4];
+        a[0] = tf32(A[g * kLP + k0 + tq]);
+        a[1] = tf32(A[(g + 8) * kLP + k0 + tq]);
+        a[2] = tf32(A[g * kLP + k0 + tq + 4]);
+        a[3] = tf32(A[(g + 8) * kLP + k0 + tq + 4]);
+        mma_tf32(acc, a, tf32(B[(k0 + tq) * kLP + g]), tf32(B[(k0 + tq + 4) * kLP + g]));
+    }
+}
+__device__ __forceinline__ void warp_store(float *D, const float (&acc)[4], float scale, int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+    D[g * kLP + 2 * tq] = scale * acc[0];
+    D[g * kLP + 2 * tq + 1] = scale * acc[1];
+    D[(g + 8) * kLP + 2 * tq] = scale * acc[2];
+    D[(g + 8) * kLP + 2 * tq + 1] = scale * acc[3];
+}
+
+// X = (I + L)^-1 in place in sL (strictly lower L in, unit lower X out, the
+// diagonal written as 1; the upper quadrant rows 0-31 x cols 32-63 is
+// scratch).  Recursive doubling: 4x4 diagonal blocks in closed form, then
+// X21 = -X22 L21 X11 on 8x8 and 16x16 blocks in fp32 SIMT, and on 32x32 and
+// 64x64 with mma.sync (tf32 inputs, fp32 accumulation).  sP: 256 floats of
+// scratch.  Called by the 256 prep threads.
+__device__ void solve_unit_lower(float *sL, float *sP, int pt) {
+    const int pw = pt >> 5, lane = pt & 31;
+    if (pt < 64) {  // 16x16 diagonal blocks: lane (blk, c) forms column c
+        const int blk = pt >> 4, c = pt & 15;
+        float *b = sL + 16 * blk * kLP + 16 * blk;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            // x_i = delta_ic - sum_{k<i} L_ik x_k, summed as a tree of 4 partials
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < i; ++k) part[k & 3] = fmaf(b[i * kLP + k], x[k], part[k & 3]);
+            x[i] = ((i == c) ? 1.0f : 0.0f) - ((part[0] + part[1]) + (part[2] + part[3]));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i * kLP + c] = x[i];
+    }
+    ptx::named_bar(1, kPrepThreads);
+    // X_10 = -D_1 L_10 D_0 and X_32 = -D_3 L_32 D_2 on 16x16 blocks (warps 0 and 1)
+    if (pw < 2) {
+        const int a = 2 * pw + 1;
+        float *Lab = sL + 16 * a * kLP + 16 * (a - 1);
+        float *Db = sL + 16 * (a - 1) * kLP + 16 * (a - 1);
+        float *Da = sL + 16 * a * kLP + 16 * a;
+        float *P = sL + 16 * pw * kLP + 32 + 16 * pw;   // upper quadrant: scratch
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float acc[4] = {0, 0, 0, 0};
+            warp_mm(acc, Lab, Db + 8 * nt, 16, lane);
+            warp_store(P + 8 * nt, acc, 1.0f, lane);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float acc[4] = {0, 0, 0, 0};
+            warp_mm(acc, Da, P + 8 * nt, 16, lane);
+            warp_store(Lab + 8 * nt, acc, -1.0f, lane);
+        }
+    }
+    ptx::named_bar(1, kPrepThreads);
+    // X21 = -X22 (L21 X11) on the 32x32 halves; warp (mt, nt) owns a 16x8 tile
+    {
+        const int mt = pw >> 2, nt = pw & 3;
+        float acc[4] = {0, 0, 0, 0};
+        warp_mm(acc, sL + (32 + 16 * mt) * kLP, sL + 8 * nt, 32, lane);
+        warp_store(sL + 16 * mt * kLP + 32 + 8 * nt, acc, 1.0f, lane);   // P in the upper quadrant
+    }
+    ptx::named_bar(1, kPrepThreads);
+    {
+        const int mt = pw >> 2, nt = pw & 3;
+        float acc[4] = {0, 0, 0, 0};
+        warp_mm(acc, sL + (32 + 16 * mt) * kLP + 32, sL + 32 + 8 * nt, 32, lane);
+        warp_store(sL + (32 + 16 * mt) * kLP + 8 * nt, acc, -1.0f, lane);
+    }
+    ptx::named_bar(1, kPrepThreads);
+}
+
+// Scale rows of a 64-row bf16 tile (K/64 blocks of 8 KB) in place: row t by f[t].
+template <int K>
+__device__ __forceinline__ void scale_rows(uint8_t *tile, const float *f, int pt) {
+    constexpr int PIECES = C * K * 2 / 16;   // 16-byte pieces
+    for (int i = pt; i < PIECES; i += kPrepThreads) {
+        const int row = (i >> 3) & 63;        // 8 pieces per 128-byte row
+        uint4 *p = reinterpret_cast<uint4 *>(tile + i * 16);
+        uint4 u = *p;
+        const float s = f[row];
+        uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
+            w[e] = pack_bf16x2(x.x * s, x.y * s);
+        }
+        *p = u;
+    }
+}
 
 template <int K, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_v,
                 Params p) {
-    using SM = Smem<K>;
+    using LY = Lay<K>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_full[2], bar_mma;
+    // 1024-byte aligned start, by pointer arithmetic so accesses stay in the
+    // shared state space (an integer round trip would make them generic)
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float sBeta[C], sLg[C];
-    __shared__ int s_abort;
+    __shared__ float sBeta[NS][C], sLg[NS][C];
+    __shared__ float sScale[2][C];        // prep: g_t, g_C / g_t of the chunk being scaled
+    __shared__ float sP[256];             // solver scratch
+    __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, half = warp >> 2;      // TMEM lane quarter, column half
+    const int q4 = warp & 3;
     const int seq = blockIdx.y, v0 = blockIdx.x * BV;
-    const int T = p.T;
-
-    uint8_t *sXh = smem + SM::oXh, *sXb = smem + SM::oXb, *sA = smem + SM::oA;
-    uint8_t *sKw = smem + SM::oKw, *sS = smem + SM::oS, *sU = smem + SM::oU;
-    uint8_t *sUh = GATED ? smem + SM::oUh : sU;
-    float *sL = reinterpret_cast<float *>(smem + SM::oL);
-    float *sX = reinterpret_cast<float *>(smem + SM::oX);
+    const int T = p.T, nch = p.nchunks;
+    float *sL = reinterpret_cast<float *>(smem + LY::oL);
+    uint8_t *sKw = smem + LY::oKw, *sXb = smem + LY::oXb;
+    uint8_t *sS = smem + LY::oS, *sU = smem + LY::oU;
+    auto slot = [&](int j) { return smem + (j % NS) * LY::kSlot; };
+    auto tA = [&](int j) { return smem + LY::oA + (j & 1) * C * C * 2; };
 
     if (tid == 0) {
-        ptx::mbar_init(&bar_full[0], 1);
-        ptx::mbar_init(&bar_full[1], 1);
-        ptx::mbar_init(&bar_mma, 1);
+        for (int i = 0; i < NS; ++i) {
+            ptx::mbar_init(&bars.full[i], 1);
+            ptx::mbar_init(&bars.empty[i], 1);
+        }
+        uint64_t *one[] = {&bars.g_full, &bars.x1, &bars.x2, &bars.kw_full, &bars.x3,
+                           &bars.u_full, &bars.u_sm, &bars.s_full, &bars.s_ready,
+                           &bars.a_free[0], &bars.a_free[1], &bars.o_free[0], &bars.o_free[1]};
+        for (uint64_t *b : one) ptx::mbar_init(b, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
-        ptx::prefetch_tmap(&tm_q);
-        ptx::prefetch_tmap(&tm_k);
-        ptx::prefetch_tmap(&tm_kt);
-        ptx::prefetch_tmap(&tm_v);
     }
-    if (warp == 0) {
+    if (warp == 1) {
         ptx::tmem_alloc(&tmem_base_sh, kTmemCols);
         ptx::tmem_relinquish();
     }
-
-    // state slice: thread (q4, half, lane < 16) owns row v = 16 q4 + lane,
-    // key columns [half K/2, (half+1) K/2)
-    constexpr int KH = K / 2;
-    const bool srow = lane < 16;
-    const int vrow = 16 * q4 + lane;
-    float S[KH];
-#pragma unroll
-    for (int j = 0; j < KH; ++j)
-        S[j] = (srow && p.S0) ? p.S0[((size_t)seq * p.V + v0 + vrow) * K + half * KH + j] : 0.0f;
-    if (srow) {
-#pragma unroll
-        for (int j = 0; j < KH; j += 32) st_row_sw128(sS, BV, vrow, half * KH + j, S + j, 32);
-    }
-    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+    int *st = p.status;
 
-    auto stage_ptr = [&](int b) { return smem + (b ? SM::oStage1 : SM::oStage0); };
-    auto issue_loads = [&](int chunk, int b) {
-        uint8_t *st = stage_ptr(b);
-        uint8_t *kq = st, *kt = st + SM::kKQ, *vv = st + SM::kKQ + SM::kKt;
-        const int t0 = chunk * C;
-        ptx::mbar_arrive_expect_tx(&bar_full[b], SM::kStage);
-#pragma unroll
-        for (int cb = 0; cb < K / 64; ++cb) {
-            ptx::tma_load_3d(kq + cb * 16384, &tm_k, &bar_full[b], cb * 64, t0, seq);
-            ptx::tma_load_3d(kq + cb * 16384 + 8192, &tm_q, &bar_full[b], cb * 64, t0, seq);
-            ptx::tma_load_3d(kt + cb * 8192, &tm_kt, &bar_full[b], cb * 64, t0, seq);
-        }
-        ptx::tma_load_3d(vv, &tm_v, &bar_full[b], v0, t0, seq);
-    };
-    int issued = 0, consumed = -1;  // chunk indices of the loads issued / waited for
-    if (tid == 0) issue_loads(0, 0);
-
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    auto wait_mma = [&]() {
-        if (!ptx::mbar_wait(&bar_mma, mma_phase, kWaitLimit)) {
-            report_status(p.status, OSDN_ERR_TIMEOUT);
-            s_abort = 1;
-        }
-        mma_phase ^= 1u;
-        ptx::tc_fence_after();
-    };
-
-    for (int chunk = 0; chunk < p.nchunks && ok; ++chunk) {
-        const int b = chunk & 1;
-        const int t0 = chunk * C;
-        uint8_t *st = stage_ptr(b);
-        uint8_t *sKQ = st, *sKt = st + SM::kKQ, *sV = st + SM::kKQ + SM::kKt;
-        const uint32_t aKQ = ptx::smem_u32(sKQ), aKt = ptx::smem_u32(sKt), aV = ptx::smem_u32(sV);
-
-        // ---- 1. inputs of this chunk; prefetch the next chunk -------------------
-        if (!ptx::mbar_wait(&bar_full[b], (chunk >> 1) & 1, kWaitLimit)) {
-            report_status(p.status, OSDN_ERR_TIMEOUT);
-            s_abort = 1;
-        }
-        consumed = chunk;
-        if (tid == 0 && chunk + 1 < p.nchunks) {
-            issue_loads(chunk + 1, b ^ 1);
-            issued = chunk + 1;
-        }
-
-        // ---- 2. Gram + scores, and S Q^T (state of the previous chunk) ---------
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t id_g = ptx::idesc_bf16(128, 64, 0, 0);
-            const uint32_t id_o = ptx::idesc_bf16(64, 64, 0, 0);
-            const uint32_t aS = ptx::smem_u32(sS);
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks)
-                ptx::umma_bf16(tmem + kColG, desc_k(aKQ, 128, ks), desc_k(aKt, 64, ks), id_g, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks)
-                ptx::umma_bf16(tmem + kColO1, desc_k(aS, BV, ks), desc_k(aKQ + 8192, 128, ks), id_o,
-                               ks > 0);
-            ptx::umma_commit(&bar_mma);
-        }
-        // gates of this chunk: beta (0 past the end) and the inclusive cumulative
-        // log of alpha (alpha = 1 past the end)
-        if (warp == 7) {
+    if (warp == 0) {
+        // ======================================================== producer
+        int last = -1;
+        for (int j = 0; j < nch; ++j) {
+            const int sl = j % NS, t0 = j * C;
+            // gates: beta (0 past T) and the inclusive cumulative log alpha,
+            // fetched before waiting for the slot so the load latency overlaps
             float bb[2], lg[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -258,240 +343,316 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 bb[e] = valid ? p.beta[(size_t)seq * T + t] : 0.0f;
                 lg[e] = (GATED && valid) ? logf(p.alpha[(size_t)seq * T + t]) : 0.0f;
             }
-            float s = lg[0] + lg[1];
+            if (j >= NS &&
+                !__all_sync(kFullMask, wait_bar(&bars.empty[sl], ((j / NS) - 1) & 1, &s_abort, st)))
+                break;
+            float sc = lg[0] + lg[1];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(kFullMask, s, off);
-                if (lane >= off) s += y;
+                const float y = __shfl_up_sync(kFullMask, sc, off);
+                if (lane >= off) sc += y;
             }
-            const float excl = s - (lg[0] + lg[1]);
-            sBeta[2 * lane] = bb[0];
-            sBeta[2 * lane + 1] = bb[1];
-            sLg[2 * lane] = excl + lg[0];
-            sLg[2 * lane + 1] = excl + lg[0] + lg[1];
+            const float excl = sc - (lg[0] + lg[1]);
+            sBeta[sl][2 * lane] = bb[0];
+            sBeta[sl][2 * lane + 1] = bb[1];
+            sLg[sl][2 * lane] = excl + lg[0];
+            sLg[sl][2 * lane + 1] = excl + lg[0] + lg[1];
+            __syncwarp();
+            if (lane == 0) {
+                uint8_t *sb = slot(j);
+                ptx::mbar_arrive_expect_tx(&bars.full[sl], LY::kSlot);
+#pragma unroll
+                for (int cb = 0; cb < K / 64; ++cb) {
+                    ptx::tma_load_3d(sb + cb * 16384, &tm_k, &bars.full[sl], cb * 64, t0, seq);
+                    ptx::tma_load_3d(sb + cb * 16384 + 8192, &tm_q, &bars.full[sl], cb * 64, t0, seq);
+                    ptx::tma_load_3d(sb + LY::oKt + cb * 8192, &tm_kt, &bars.full[sl], cb * 64, t0, seq);
+                }
+                ptx::tma_load_3d(sb + LY::oVv, &tm_v, &bars.full[sl], v0, t0, seq);
+            }
+            last = j;
         }
-        __syncthreads();
-        wait_mma();
-
-        // ---- 3. L (fp32, for the solve) and the masked scores A (bf16) ---------
-        {
+        // bulk copies still in flight (only after an abort) must land before exit
+        if (lane == 0 && s_abort) {
+            for (int j = (last > NS - 1 ? last - NS + 1 : 0); j <= last; ++j)
+                for (uint32_t i = 0; i < kWaitLimit; ++i)
+                    if (ptx::mbar_try_wait_sleep(&bars.full[j % NS], (j / NS) & 1, kSleepNs)) break;
+        }
+    } else if (warp == 1) {
+        // ======================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t aXb = ptx::smem_u32(sXb), aKw = ptx::smem_u32(sKw);
+            const uint32_t aS = ptx::smem_u32(sS), aU = ptx::smem_u32(sU);
+            auto gram = [&](int j) {  // [K;Q] Kt^T of chunk j into G
+                const uint32_t aKQ = ptx::smem_u32(slot(j)), aKt = aKQ + LY::oKt;
+                const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    ptx::umma_bf16(tmem + kColG, desc_k(aKQ, 128, ks), desc_k(aKt, C, ks), id, ks > 0);
+                ptx::umma_commit(&bars.g_full);
+            };
+            bool ok = wait_bar(&bars.full[0], 0, &s_abort, st);
+            if (ok) {
+                ptx::tc_fence_after();
+                gram(0);
+            }
+            for (int j = 0; ok && j <= nch; ++j) {
+                // Order per iteration: chain of chunk j-1 (frees the slot chunk j+1
+                // is loaded into), Kw/V' of chunk j, then Gram of chunk j+1.
+                if (j >= 1) {  // chain of chunk c = j - 1
+                    const int c = j - 1;
+                    if (!wait_bar(&bars.x3, c & 1, &s_abort, st)) break;
+                    if (!wait_bar(&bars.s_ready, c & 1, &s_abort, st)) break;
+                    if (c >= 2 && !wait_bar(&bars.o_free[c & 1], ((c >> 1) + 1) & 1, &s_abort, st)) break;
+                    ptx::tc_fence_after();
+                    const uint32_t aKQ = ptx::smem_u32(slot(c)), aKt = aKQ + LY::oKt;
+                    const uint32_t aA = ptx::smem_u32(tA(c));
+                    const uint32_t dU = tmem + kColU + 64 * (c & 1), dO = tmem + kColO + 64 * (c & 1);
+                    const uint32_t idu = ptx::idesc_bf16(64, 64, 0, 1, 1), ido = ptx::idesc_bf16(64, 64, 0, 0);
+#pragma unroll
+                    for (int ks = 0; ks < K / 16; ++ks) {  // U^T -= S Kw^T, O^T = S Q^T
+                        ptx::umma_bf16(dU, desc_k(aS, BV, ks), desc_mn(aKw, 8192, ks), idu, 1);
+                        ptx::umma_bf16(dO, desc_k(aS, BV, ks), desc_k(aKQ + 8192, 128, ks), ido, ks > 0);
+                    }
+                    ptx::umma_commit(&bars.u_full);
+                    if (!wait_bar(&bars.u_sm, c & 1, &s_abort, st)) break;
+                    ptx::tc_fence_after();
+                    const uint32_t ids = ptx::idesc_bf16(64, K, 0, 1), ida = ptx::idesc_bf16(64, 64, 0, 0);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks) {  // S += U^T Kt, O^T += U^T A^T
+                        ptx::umma_bf16(tmem + kColS, desc_k(aU, BV, ks), desc_mn(aKt, 8192, ks), ids, 1);
+                        ptx::umma_bf16(dO, desc_k(aU, BV, ks), desc_k(aA, C, ks), ida, 1);
+                    }
+                    ptx::umma_commit(&bars.s_full);
+                    ptx::umma_commit(&bars.a_free[c & 1]);
+                    ptx::umma_commit(&bars.empty[c % NS]);
+                }
+                if (j < nch) {  // Kw^T = K^T Xb^T (K scaled by g) and U^T = V^T Xb^T of chunk j
+                    if (!wait_bar(&bars.x2, j & 1, &s_abort, st)) break;
+                    ptx::tc_fence_after();
+                    const uint32_t aKQ = ptx::smem_u32(slot(j)), aV = aKQ + LY::oVv;
+                    const uint32_t idk = ptx::idesc_bf16(K, 64, 1, 0), idv = ptx::idesc_bf16(64, 64, 1, 0);
+                    const uint32_t dU = tmem + kColU + 64 * (j & 1);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks) {
+                        ptx::umma_bf16(tmem + kColKw, desc_mn(aKQ, 16384, ks), desc_k(aXb, C, ks), idk, ks > 0);
+                        ptx::umma_bf16(dU, desc_mn(aV, 8192, ks), desc_k(aXb, C, ks), idv, ks > 0);
+                    }
+                    ptx::umma_commit(&bars.kw_full);
+                }
+                if (j + 1 < nch) {  // Gram of the next chunk: slot loaded, G read by prep
+                    if (!wait_bar(&bars.full[(j + 1) % NS], ((j + 1) / NS) & 1, &s_abort, st)) break;
+                    if (!wait_bar(&bars.x1, j & 1, &s_abort, st)) break;
+                    ptx::tc_fence_after();
+                    gram(j + 1);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 10) {
+        // ======================================================== prep
+        const int pt = tid - 64, pw = warp - 2, half = pw >> 2;
+        const int grow = 32 * q4 + lane;       // row of the M=128 Gram/score accumulator
+        // G epilogue of chunk j: L (fp32) into sL, masked scores A into tA(j),
+        // the gate scalings of chunk j into sScale; ends by releasing G.
+        auto g_epilogue = [&](int j) -> bool {
+            const int sl = j % NS;
+            bool ok = wait_bar(&bars.full[sl], (j / NS) & 1, &s_abort, st) &&
+                      wait_bar(&bars.g_full, j & 1, &s_abort, st) &&
+                      (j < 2 || wait_bar(&bars.a_free[j & 1], ((j >> 1) + 1) & 1, &s_abort, st));
+            if (!vote_all(ok, 1, kPrepThreads)) return false;
+            ptx::tc_fence_after();
             float g[32];
             tmem_ld32(tmem + lane_off + kColG + 32 * half, g);
-            const int row = 32 * q4 + lane;
-            if (row < C) {
-                const int i = row;
-                const float bi = sBeta[i];
-                const float lgi = sLg[i];
+            if (grow < C) {  // L = tril(diag(beta) (G . K Kt^T), -1)
+                const int i = grow;
+                const float bi = sBeta[sl][i], lgi = sLg[sl][i];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
+                    const int col = 32 * half + jj;
                     float val = 0.0f;
-                    if (j < i) val = bi * (GATED ? __expf(lgi - sLg[j]) : 1.0f) * g[jj];
-                    sL[i * kLP + j] = val;
+                    if (col < i) val = bi * (GATED ? __expf(lgi - sLg[sl][col]) : 1.0f) * g[jj];
+                    sL[i * kLP + col] = val;
                 }
-            } else {
-                const int t = row - C;
-                const float lgt = sLg[t];
-                float a[32];
+            } else {  // A = tril(G . Q Kt^T)
+                const int t = grow - C;
+                const float lgt = sLg[sl][t];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
-                    const int s = 32 * half + jj;
-                    a[jj] = (s <= t) ? (GATED ? __expf(lgt - sLg[s]) : 1.0f) * g[jj] : 0.0f;
+                    const int col = 32 * half + jj;
+                    g[jj] = (col <= t) ? (GATED ? __expf(lgt - sLg[sl][col]) : 1.0f) * g[jj] : 0.0f;
                 }
-                st_row_sw128(sA, C, t, 32 * half, a, 32);
+                st_row_sw128(tA(j), C, t, 32 * half, g, 32);
             }
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- 4. X = (I + L)^-1 by 16x16 blocks (fp32) ---------------------------
-        if (tid < 64) {  // diagonal blocks: thread (a, c) forms column c of block a
-            const int a = tid >> 4, c = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float s = (i == c) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int k = 0; k < i; ++k) s = fmaf(-sL[(16 * a + i) * kLP + 16 * a + k], x[k], s);
-                x[i] = s;
+            if (GATED && pt < C) {
+                const float lgC = sLg[sl][C - 1], lgt = sLg[sl][pt];
+                sScale[0][pt] = __expf(lgt);
+                sScale[1][pt] = __expf(lgC - lgt);
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sX[(16 * a + i) * kLP + 16 * a + c] = x[i];
-        }
-        __syncthreads();
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int items = (4 - d) * 256;
-            // P_ab = sum_{b <= cc < a} L_a,cc X_cc,b, kept in the (unused) upper block (b, a) of L
-            for (int it = tid; it < items; it += kThreads) {
-                const int b = it >> 8, a = b + d, r = (it >> 4) & 15, c = it & 15;
-                float s = 0.0f;
-                for (int cc = b; cc < a; ++cc)
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        s = fmaf(sL[(16 * a + r) * kLP + 16 * cc + k], sX[(16 * cc + k) * kLP + 16 * b + c], s);
-                sL[(16 * b + r) * kLP + 16 * a + c] = s;
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_bar(1, kPrepThreads);
+            if (pt == 0) ptx::mbar_arrive(&bars.x1);
+            return true;
+        };
+        bool ok = true;
+        for (int j = 0; ok && j < nch; ++j) {
+            const int sl = j % NS;
+            if (!g_epilogue(j)) break;
+            if (GATED) {  // [K;Q] <- diag(g) [K;Q], Kt <- diag(g_C / g) Kt (in place)
+                scale_rows<2 * K>(slot(j), sScale[0], pt);
+                scale_rows<K>(slot(j) + LY::oKt, sScale[1], pt);
             }
-            __syncthreads();
-            // X_ab = -X_aa P_ab
-            for (int it = tid; it < items; it += kThreads) {
-                const int b = it >> 8, a = b + d, r = (it >> 4) & 15, c = it & 15;
-                float s = 0.0f;
+            solve_unit_lower(sL, sP, pt);
+            {  // Xb = X diag(beta): row t, columns s <= t (bf16 B operand)
+                const int t = pt >> 2, s0 = 16 * (pt & 3);
+                float xb[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    s = fmaf(sX[(16 * a + r) * kLP + 16 * a + k], sL[(16 * b + k) * kLP + 16 * a + c], s);
-                sX[(16 * a + r) * kLP + 16 * b + c] = -s;
+                for (int e = 0; e < 16; ++e) {
+                    const int s = s0 + e;
+                    xb[e] = (s <= t) ? sL[t * kLP + s] * sBeta[sl][s] : 0.0f;
+                }
+                st_row_sw128(sXb, C, t, s0, xb, 16);
             }
-            __syncthreads();
-        }
-        // Xh = X diag(beta g), Xb = X diag(beta): B operands, row t, column s
-        {
-            const int t = tid >> 2, s0 = 16 * (tid & 3);
-            float xh[16], xb[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int s = s0 + e;
-                const float x = (s <= t) ? sX[t * kLP + s] : 0.0f;
-                xb[e] = x * sBeta[s];
-                xh[e] = GATED ? xb[e] * __expf(sLg[s]) : xb[e];
-            }
-            st_row_sw128(sXb, C, t, s0, xb, 16);
-            if (GATED) st_row_sw128(sXh, C, t, s0, xh, 16);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- 5. Kw^T = K^T Xh^T and U^T <- V^T Xb^T ---------------------------
-        if (tid == 0) {
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, kPrepThreads);
+            if (pt == 0) ptx::mbar_arrive(&bars.x2);
+            // Kw^T out of TMEM into the MN-major B operand of the chain
+            ok = wait_bar(&bars.kw_full, j & 1, &s_abort, st) &&
+                 (j < 1 || wait_bar(&bars.u_full, (j - 1) & 1, &s_abort, st));
+            if (!vote_all(ok, 1, kPrepThreads)) break;
             ptx::tc_fence_after();
-            const uint32_t aXh = ptx::smem_u32(GATED ? sXh : sXb), aXb = ptx::smem_u32(sXb);
-            const uint32_t id_kw = ptx::idesc_bf16(K, 64, 1, 0);
-            const uint32_t id_v = ptx::idesc_bf16(64, 64, 1, 0);
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                ptx::umma_bf16(tmem + kColKw, desc_mn(aKQ, 16384, ks), desc_k(aXh, C, ks), id_kw, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                ptx::umma_bf16(tmem + kColU, desc_mn(aV, 8192, ks), desc_k(aXb, C, ks), id_v, ks > 0);
-            ptx::umma_commit(&bar_mma);
+            {
+                float kw[32];
+                tmem_ld32(tmem + lane_off + kColKw + 32 * half, kw);
+                const int krow = (K == 128) ? 32 * q4 + lane : 16 * q4 + lane;
+                if (K == 128 || lane < 16) st_row_sw128(sKw, K, krow, 32 * half, kw, 32);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_bar(1, kPrepThreads);
+            if (pt == 0) ptx::mbar_arrive(&bars.x3);
         }
-        __syncwarp();
-        wait_mma();
-
-        // ---- 6. Kw^T to shared memory (bf16, MN-major B operand) --------------
+    } else {
+        // ======================================================== chain
+        const int ct = tid - 320;
+        const bool act = lane < 16;
+        const int vrow = 16 * q4 + lane;
+        // initial state: TMEM S = g_C(0) S0, bf16 copy = S0
         {
-            float kw[32];
-            tmem_ld32(tmem + lane_off + kColKw + 32 * half, kw);
-            const int krow = (K == 128) ? 32 * q4 + lane : 16 * q4 + lane;
-            if (K == 128 || lane < 16) st_row_sw128(sKw, K, krow, 32 * half, kw, 32);
+            float gC = 1.0f;
+            const bool ok0 = !GATED || wait_bar(&bars.full[0], 0, &s_abort, st);
+            if (vote_all(ok0, 2, kChainThreads) && GATED) gC = __expf(sLg[0][C - 1]);
+#pragma unroll
+            for (int c0 = 0; c0 < K; c0 += 32) {
+                float sv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    sv[e] = (act && p.S0) ? p.S0[((size_t)seq * p.V + v0 + vrow) * K + c0 + e] : 0.0f;
+                if (act) st_row_sw128(sS, BV, vrow, c0, sv, 32);
+                float lo[16], hi[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    lo[e] = gC * sv[e];
+                    hi[e] = gC * sv[16 + e];
+                }
+                ptx::tmem_st16(tmem + lane_off + kColS + c0, lo);
+                ptx::tmem_st16(tmem + lane_off + kColS + c0 + 16, hi);
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_bar(2, kChainThreads);
+            if (ct == 0) ptx::mbar_arrive(&bars.s_ready);
         }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- 7. U^T += -S Kw^T ---------------------------------------------------
-        if (tid == 0) {
+        for (int c = 0; c < nch; ++c) {
+            // ---- U^T to shared memory (A operand of the state and output MMAs)
+            if (!vote_all(wait_bar(&bars.u_full, c & 1, &s_abort, st), 2, kChainThreads)) break;
             ptx::tc_fence_after();
-            const uint32_t aS = ptx::smem_u32(sS), aKw = ptx::smem_u32(sKw);
-            const uint32_t id_u = ptx::idesc_bf16(64, 64, 0, 1, 1);
+            {
+                float u[32], u2[32];
+                tmem_ld32(tmem + lane_off + kColU + 64 * (c & 1), u);
+                tmem_ld32(tmem + lane_off + kColU + 64 * (c & 1) + 32, u2);
+                if (act) {
+                    st_row_sw128(sU, BV, vrow, 0, u, 32);
+                    st_row_sw128(sU, BV, vrow, 32, u2, 32);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_bar(2, kChainThreads);
+            if (ct == 0) ptx::mbar_arrive(&bars.u_sm);
+            // ---- state: bf16 copy for the next chunk, g_C(next) folded into TMEM
+            bool okc = wait_bar(&bars.s_full, c & 1, &s_abort, st) &&
+                       (!GATED || c + 1 >= nch ||
+                        wait_bar(&bars.full[(c + 1) % NS], ((c + 1) / NS) & 1, &s_abort, st));
+            if (!vote_all(okc, 2, kChainThreads)) break;
+            ptx::tc_fence_after();
+            const float gN = (GATED && c + 1 < nch) ? __expf(sLg[(c + 1) % NS][C - 1]) : 1.0f;
 #pragma unroll
-            for (int ks = 0; ks < K / 16; ++ks)
-                ptx::umma_bf16(tmem + kColU, desc_k(aS, BV, ks), desc_mn(aKw, 8192, ks), id_u, 1);
-            ptx::umma_commit(&bar_mma);
-        }
-        __syncwarp();
-        wait_mma();
-
-        // ---- 8. U^T (and Uh^T = U^T diag(g_C / g)) to shared memory -----------
-        {
-            float u[32];
-            tmem_ld32(tmem + lane_off + kColU + 32 * half, u);
-            if (srow) {
-                st_row_sw128(sU, BV, vrow, 32 * half, u, 32);
+            for (int c0 = 0; c0 < K; c0 += 32) {
+                float sv[32];
+                tmem_ld32(tmem + lane_off + kColS + c0, sv);
+                if (act) {
+                    st_row_sw128(sS, BV, vrow, c0, sv, 32);
+                    if (c == nch - 1 && p.ST) {
+                        float *dst = p.ST + ((size_t)seq * p.V + v0 + vrow) * K + c0;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(dst + e) = make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
+                    }
+                }
                 if (GATED) {
-                    const float lgC = sLg[C - 1];
+                    float lo[16], hi[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) u[e] *= __expf(lgC - sLg[32 * half + e]);
-                    st_row_sw128(sUh, BV, vrow, 32 * half, u, 32);
+                    for (int e = 0; e < 16; ++e) {
+                        lo[e] = gN * sv[e];
+                        hi[e] = gN * sv[16 + e];
+                    }
+                    ptx::tmem_st16(tmem + lane_off + kColS + c0, lo);
+                    ptx::tmem_st16(tmem + lane_off + kColS + c0 + 16, hi);
                 }
             }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- 9. dS = Uh^T Kt and O2 = U^T A^T ----------------------------------
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t aU = ptx::smem_u32(sU), aUh = ptx::smem_u32(sUh), aA = ptx::smem_u32(sA);
-            const uint32_t id_ds = ptx::idesc_bf16(64, K, 0, 1);
-            const uint32_t id_o2 = ptx::idesc_bf16(64, 64, 0, 0);
+            if (GATED) ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_bar(2, kChainThreads);
+            if (ct == 0) ptx::mbar_arrive(&bars.s_ready);
+            // ---- output: O^T out of TMEM, staged [t][v] in the free U tile
+            {
+                float o1[32], o2[32];
+                tmem_ld32(tmem + lane_off + kColO + 64 * (c & 1), o1);
+                tmem_ld32(tmem + lane_off + kColO + 64 * (c & 1) + 32, o2);
+                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(sU);
+                if (act) {
 #pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                ptx::umma_bf16(tmem + kColDS, desc_k(aUh, BV, ks), desc_mn(aKt, 8192, ks), id_ds, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                ptx::umma_bf16(tmem + kColO2, desc_k(aU, BV, ks), desc_k(aA, C, ks), id_o2, ks > 0);
-            ptx::umma_commit(&bar_mma);
-        }
-        __syncwarp();
-        wait_mma();
-
-        // ---- 10. state carry and output -----------------------------------------
-        {
-            const float gC = GATED ? __expf(sLg[C - 1]) : 1.0f;
-#pragma unroll
-            for (int j = 0; j < KH; j += 32) {
-                float ds[32];
-                tmem_ld32(tmem + lane_off + kColDS + half * KH + j, ds);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) S[j + e] = fmaf(gC, S[j + e], ds[e]);
-                if (srow) st_row_sw128(sS, BV, vrow, half * KH + j, S + j, 32);
-            }
-            float o1[32], o2[32];
-            tmem_ld32(tmem + lane_off + kColO1 + 32 * half, o1);
-            tmem_ld32(tmem + lane_off + kColO2 + 32 * half, o2);
-            // stage O (t rows, v columns, bf16) in the free L tile
-            __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(sL);
-            if (srow) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int t = 32 * half + e;
-                    const float gt = GATED ? __expf(sLg[t]) : 1.0f;
-                    sO[t * BV + vrow] = __float2bfloat16_rn(fmaf(gt, o1[e], o2[e]));
+                    for (int e = 0; e < 32; ++e) {
+                        sO[e * BV + vrow] = __float2bfloat16_rn(o1[e]);
+                        sO[(32 + e) * BV + vrow] = __float2bfloat16_rn(o2[e]);
+                    }
                 }
             }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        ok = !__syncthreads_or(s_abort);
-        {
-            const __nv_bfloat16 *sO = reinterpret_cast<const __nv_bfloat16 *>(sL);
-            // 64 rows x 128 bytes: 8 threads per row, 16 bytes each
-            const int r = tid >> 3, part = tid & 7;
+            ptx::tc_fence_before();
+            ptx::named_bar(2, kChainThreads);
+            if (ct == 0) ptx::mbar_arrive(&bars.o_free[c & 1]);
+            {
+                const __nv_bfloat16 *sO = reinterpret_cast<const __nv_bfloat16 *>(sU);
+                const int r = ct >> 3, part = ct & 7;   // 16 rows x 8 pieces per pass
 #pragma unroll
-            for (int rr = 0; rr < C; rr += kThreads / 8) {
-                const int t = t0 + r + rr;
-                if (t < T)
-                    *reinterpret_cast<uint4 *>(p.o + ((size_t)seq * T + t) * p.V + v0 + part * 8) =
-                        *reinterpret_cast<const uint4 *>(sO + (r + rr) * BV + part * 8);
+                for (int rr = 0; rr < C; rr += 16) {
+                    const int t = c * C + r + rr;
+                    if (t < T)
+                        *reinterpret_cast<uint4 *>(p.o + ((size_t)seq * T + t) * p.V + v0 + part * 8) =
+                            *reinterpret_cast<const uint4 *>(sO + (r + rr) * BV + part * 8);
+                }
             }
+            // the next chunk's U epilogue overwrites this staging tile
+            ptx::named_bar(2, kChainThreads);
         }
-        __syncthreads();
     }
 
-    // ---- final state ------------------------------------------------------------
-    if (p.ST && srow && ok) {
-        float *dst = p.ST + ((size_t)seq * p.V + v0 + vrow) * K + half * KH;
-#pragma unroll
-        for (int j = 0; j < KH; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
-    // Bulk copies still in flight (only after an abort) must land before exit.
-    if (tid == 0 && !ok && issued > consumed)
-        ptx::mbar_wait(&bar_full[issued & 1], (issued >> 1) & 1, kWaitLimit);
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ----------------------------------------------------------------------- host
@@ -529,7 +690,7 @@ static cudaError_t launch(int BH, int T, int V, const void *q, const void *k, co
     if (!make_map(&mq, q, BH, T, K) || !make_map(&mk, k, BH, T, K) ||
         !make_map(&mkt, kt, BH, T, K) || !make_map(&mv, v, BH, T, V))
         return cudaErrorInvalidValue;
-    constexpr int smem = Smem<K>::kAlloc;
+    constexpr int smem = Lay<K>::kAlloc;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(delta_tc_kernel<K, GATED>,
