@@ -373,17 +373,38 @@ def run_ours(args, w, x, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def sources_digest(paths):
+    """sha256 over the named source files (paths relative to the repo root)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if one exists."""
+    """DRAM bytes per launch from the committed ncu summary, if one exists.
+
+    The summary names the sources of the kernel it was captured from and their
+    sha256; when those sources have changed since, the counters describe another
+    kernel and the traffic is reported as unknown (None)."""
     path = os.path.join(ROOT, "profiles", "traffic_%s_%s.txt" % (kernel, workload))
+    fields = {}
     try:
         with open(path) as f:
             for line in f:
-                if line.startswith("dram_bytes_per_launch"):
-                    return float(line.split("=", 1)[1].split()[0])
+                if "=" in line and not line.startswith("#"):
+                    key, val = line.split("=", 1)
+                    fields[key.strip()] = val.strip()
     except OSError:
-        pass
-    return None
+        return None
+    try:
+        if sources_digest(fields["sources"].split()) != fields["sources_sha256"]:
+            return None
+        return float(fields["dram_bytes_per_launch"].split()[0])
+    except (KeyError, OSError, ValueError):
+        return None
 
 
 def main():

@@ -126,12 +126,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     }
 }
 
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int rows, int ks) {
-    return ptx::sdesc(base + (ks >> 2) * rows * 128 + (ks & 3) * 32, 16, 1024, 2);
+// Descriptors are built once per operand (dk0 / dmn0) and advanced per
+// k-slice by adding the byte offset in 16-byte units to the start-address
+// field (all tiles sit below 256 KB, so the 14-bit field never carries).
+__device__ __forceinline__ uint64_t dk0(uint32_t base) { return ptx::sdesc(base, 16, 1024, 2); }
+__device__ __forceinline__ uint64_t dmn0(uint32_t base, int block_bytes) {
+    return ptx::sdesc(base, block_bytes, 1024, 2);
 }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int block_bytes, int ks) {
-    return ptx::sdesc(base + ks * 2048, block_bytes, 1024, 2);
+// k-slice ks of a K-major tile whose 64-column blocks hold `rows` rows
+__host__ __device__ constexpr uint64_t koff(int rows, int ks) {
+    return static_cast<uint64_t>(((ks >> 2) * rows * 128 + (ks & 3) * 32) >> 4);
 }
+// k-slice ks (16 rows) of an MN-major tile
+__host__ __device__ constexpr uint64_t mnoff(int ks) { return static_cast<uint64_t>((ks * 2048) >> 4); }
 
 // Barrier over `count` threads of barrier `id` that also ANDs a predicate:
 // every participant gets the same answer, so a role leaves its loop together.
@@ -385,9 +392,10 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             auto gram = [&](int j) {  // [K;Q] Kt^T of chunk j into G
                 const uint32_t aKQ = ptx::smem_u32(slot(j)), aKt = aKQ + LY::oKt;
                 const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
+                const uint64_t da = dk0(aKQ), db = dk0(aKt);
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
-                    ptx::umma_bf16(tmem + kColG, desc_k(aKQ, 128, ks), desc_k(aKt, C, ks), id, ks > 0);
+                    ptx::umma_bf16(tmem + kColG, da + koff(128, ks), db + koff(C, ks), id, ks > 0);
                 ptx::umma_commit(&bars.g_full);
             };
             bool ok = wait_bar(&bars.full[0], 0, &s_abort, st);
@@ -408,19 +416,21 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t aA = ptx::smem_u32(tA(c));
                     const uint32_t dU = tmem + kColU + 64 * (c & 1), dO = tmem + kColO + 64 * (c & 1);
                     const uint32_t idu = ptx::idesc_bf16(64, 64, 0, 1, 1), ido = ptx::idesc_bf16(64, 64, 0, 0);
+                    const uint64_t dS = dk0(aS), dKw = dmn0(aKw, 8192), dQ = dk0(aKQ + 8192);
 #pragma unroll
                     for (int ks = 0; ks < K / 16; ++ks) {  // U^T -= S Kw^T, O^T = S Q^T
-                        ptx::umma_bf16(dU, desc_k(aS, BV, ks), desc_mn(aKw, 8192, ks), idu, 1);
-                        ptx::umma_bf16(dO, desc_k(aS, BV, ks), desc_k(aKQ + 8192, 128, ks), ido, ks > 0);
+                        ptx::umma_bf16(dU, dS + koff(BV, ks), dKw + mnoff(ks), idu, 1);
+                        ptx::umma_bf16(dO, dS + koff(BV, ks), dQ + koff(128, ks), ido, ks > 0);
                     }
                     ptx::umma_commit(&bars.u_full);
                     if (!wait_bar(&bars.u_sm, c & 1, &s_abort, st)) break;
                     ptx::tc_fence_after();
                     const uint32_t ids = ptx::idesc_bf16(64, K, 0, 1), ida = ptx::idesc_bf16(64, 64, 0, 0);
+                    const uint64_t dUa = dk0(aU), dKt = dmn0(aKt, 8192), dA = dk0(aA);
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks) {  // S += U^T Kt, O^T += U^T A^T
-                        ptx::umma_bf16(tmem + kColS, desc_k(aU, BV, ks), desc_mn(aKt, 8192, ks), ids, 1);
-                        ptx::umma_bf16(dO, desc_k(aU, BV, ks), desc_k(aA, C, ks), ida, 1);
+                        ptx::umma_bf16(tmem + kColS, dUa + koff(BV, ks), dKt + mnoff(ks), ids, 1);
+                        ptx::umma_bf16(dO, dUa + koff(BV, ks), dA + koff(C, ks), ida, 1);
                     }
                     ptx::umma_commit(&bars.s_full);
                     ptx::umma_commit(&bars.a_free[c & 1]);
@@ -432,10 +442,11 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t aKQ = ptx::smem_u32(slot(j)), aV = aKQ + LY::oVv;
                     const uint32_t idk = ptx::idesc_bf16(K, 64, 1, 0), idv = ptx::idesc_bf16(64, 64, 1, 0);
                     const uint32_t dU = tmem + kColU + 64 * (j & 1);
+                    const uint64_t dK = dmn0(aKQ, 16384), dV = dmn0(aV, 8192), dX = dk0(aXb);
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks) {
-                        ptx::umma_bf16(tmem + kColKw, desc_mn(aKQ, 16384, ks), desc_k(aXb, C, ks), idk, ks > 0);
-                        ptx::umma_bf16(dU, desc_mn(aV, 8192, ks), desc_k(aXb, C, ks), idv, ks > 0);
+                        ptx::umma_bf16(tmem + kColKw, dK + mnoff(ks), dX + koff(C, ks), idk, ks > 0);
+                        ptx::umma_bf16(dU, dV + mnoff(ks), dX + koff(C, ks), idv, ks > 0);
                     }
                     ptx::umma_commit(&bars.kw_full);
                 }
