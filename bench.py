@@ -79,13 +79,14 @@ def phase2_flops(w):
 def launches_per_step(w, x):
     """Kernels one step enqueues: the Phase 1 segment scan (plus its verify
     kernel when a retention gate splits sequences into time segments, the
-    same rule the library applies) and the Phase 2 kernel."""
+    same rule the library applies) and Phase 2 (chunk preparation and the
+    state chain for bf16 I/O, one fp32 kernel otherwise)."""
     BH, T = w.B * w.H, w.T
     nseg = 1
     if x["r"] is not None and T > 256:
         L = 1024 if BH * ((T + 1023) // 1024) >= 4 * 152 else 512
         nseg = (T + L - 1) // L if L < T else 1
-    return (2 if nseg > 1 else 1) + 1
+    return (2 if nseg > 1 else 1) + (2 if w.io == "bf16" else 1)
 
 
 def load_peaks():

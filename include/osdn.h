@@ -63,7 +63,7 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1 } osdn_dtype;
 typedef enum {
     OSDN_OK = 0,
     OSDN_ERR_NULL = -1,      /* a required pointer is NULL                     */
-    OSDN_ERR_DIMS = -2,      /* negative size, or K / V not in {64, 128}       */
+    OSDN_ERR_DIMS = -2,      /* negative size, B*H > 65535, or K / V not in {64, 128} */
     OSDN_ERR_DTYPE = -3,     /* io is not OSDN_F32 / OSDN_BF16                 */
     OSDN_ERR_ALIGN = -4,     /* a pointer is not 16-byte aligned               */
     OSDN_ERR_WORKSPACE = -5, /* workspace NULL or smaller than required        */
@@ -132,7 +132,12 @@ int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
                               const float *beta, const float *r, float eta, const float *d0,
                               void *ktilde, float *dT, void *stream);
 
-/* Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256). */
+/*
+ * Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256).  With
+ * io == OSDN_BF16 the call prepares every chunk's operands before it runs the
+ * state recurrence and keeps them in the workspace: about
+ * B*H*ceil(T/64)*64 * (4K + 260) bytes.
+ */
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V);
 
 /*

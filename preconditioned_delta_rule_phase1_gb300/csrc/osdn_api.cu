@@ -23,9 +23,11 @@ cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q
                               const void *kt, const void *v, const float *beta,
                               const float *alpha, const float *S0, void *o, float *ST,
                               cudaStream_t stream);
+size_t delta_tc_scratch_bytes(int BH, int T, int K);
 cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
                             const void *kt, const void *v, const float *beta, const float *alpha,
-                            const float *S0, void *o, float *ST, int *status, cudaStream_t stream);
+                            const float *S0, void *o, float *ST, void *scratch, int *status,
+                            cudaStream_t stream);
 }  // namespace osdn
 
 namespace {
@@ -34,7 +36,10 @@ constexpr size_t kStatusBytes = 256;
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-bool dims_ok(int B, int H, int T) { return B >= 0 && H >= 0 && T >= 0; }
+// Sequences map to the second grid dimension, so B*H is capped at its limit.
+bool dims_ok(int B, int H, int T) {
+    return B >= 0 && H >= 0 && T >= 0 && (size_t)B * (size_t)H <= 65535;
+}
 bool width_ok(int x) { return x == 64 || x == 128; }
 size_t io_bytes(int io) { return io == OSDN_BF16 ? 2 : 4; }
 
@@ -66,7 +71,7 @@ const char *osdn_status_string(int code) {
     switch (code) {
     case OSDN_OK: return "ok";
     case OSDN_ERR_NULL: return "a required pointer is NULL";
-    case OSDN_ERR_DIMS: return "bad dimensions (negative size, or K/V not 64 or 128)";
+    case OSDN_ERR_DIMS: return "bad dimensions (negative size, B*H over 65535, or K/V not 64 or 128)";
     case OSDN_ERR_DTYPE: return "unsupported io dtype";
     case OSDN_ERR_ALIGN: return "pointer not 16-byte aligned";
     case OSDN_ERR_WORKSPACE: return "workspace NULL or too small";
@@ -86,8 +91,10 @@ size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K) {
 }
 
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V) {
-    (void)io; (void)B; (void)H; (void)T; (void)K; (void)V;
-    return kStatusBytes;
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return kStatusBytes;
+    if (io != OSDN_BF16 || T == 0) return kStatusBytes;
+    // the tensor-core path keeps each chunk's prepared operands in the workspace
+    return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K);
 }
 
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
@@ -191,6 +198,7 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
         e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, (cudaStream_t)stream);
     else if (io == OSDN_BF16)  // tensor cores: bf16 operands, fp32 accumulation
         e = osdn::delta_tc_launch((int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
+                                  static_cast<char *>(workspace) + kStatusBytes,
                                   static_cast<int *>(workspace), (cudaStream_t)stream);
     else  // fp32 I/O: fp32 FFMA (tensor-core operand rounding would not meet fp32 accuracy)
         e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,

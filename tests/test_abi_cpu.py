@@ -59,7 +59,9 @@ def scan(L, io=1, B=1, H=1, T=8, K=64, k=FAKE, beta=FAKE, r=None, d0=None, kt=2 
 
 
 def chunk(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, kt=3 * FAKE, v=4 * FAKE,
-          beta=5 * FAKE, alpha=None, S0=None, o=6 * FAKE, ST=None, ws=7 * FAKE, wsb=256):
+          beta=5 * FAKE, alpha=None, S0=None, o=6 * FAKE, ST=None, ws=7 * FAKE, wsb=None):
+    if wsb is None:   # exactly what the shape needs
+        wsb = L.osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V)
     return L.osdn_chunk_fwd(io, B, H, T, K, V, q, k, kt, v, beta, alpha, S0, o, ST, ws, wsb, None)
 
 
@@ -80,7 +82,23 @@ def test_host_validation_chunk_fwd(L):
     assert chunk(L, v=4 * FAKE + 2) == -4
     assert chunk(L, o=FAKE) == -9          # o aliases q
     assert chunk(L, wsb=0) == -5
+    need = L.osdn_chunk_fwd_workspace_bytes(1, 1, 1, 8, 64, 64)
+    assert chunk(L, wsb=need - 1) == -5
     assert chunk(L, H=0) == 0
+    assert chunk(L, B=256, H=256) == -2    # more sequences than the grid holds
+
+
+def test_chunk_fwd_workspace_size(L):
+    # fp32 I/O and empty sequences need only the status word; bf16 keeps each
+    # chunk's prepared operands (Kwn, Qe: 2K bytes a row each; Xb, Ae: 128;
+    # g_C/g: 4) on the chunk-padded length, plus g_C per chunk
+    assert L.osdn_chunk_fwd_workspace_bytes(0, 2, 3, 100, 128, 64) == 256
+    assert L.osdn_chunk_fwd_workspace_bytes(1, 2, 3, 0, 128, 64) == 256
+    for B, H, T, K in [(1, 1, 1, 64), (2, 3, 100, 128), (1, 16, 65536, 128)]:
+        BH, Tp, nch = B * H, -(-T // 64) * 64, -(-T // 64)
+        r = lambda x: -(-x // 256) * 256
+        want = 256 + 2 * r(BH * Tp * K * 2) + 2 * r(BH * Tp * 64 * 2) + r(BH * Tp * 4) + r(BH * nch * 4)
+        assert L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, 64) == want
 
 
 def test_no_gpu_means_cuda_error_not_crash(L):
