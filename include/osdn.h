@@ -136,7 +136,7 @@ int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
  * Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256).  With
  * io == OSDN_BF16 the call prepares every chunk's operands before it runs the
  * state recurrence and keeps them in the workspace: about
- * B*H*ceil(T/64)*64 * (4K + 260) bytes.
+ * B*H*ceil(T/64) * (2K^2 + 256K + 8196) bytes (72 KB a chunk at K = 128).
  */
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V);
 

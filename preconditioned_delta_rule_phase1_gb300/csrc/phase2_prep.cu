@@ -5,22 +5,25 @@
 // the preconditioned keys Kt in the Gram matrix and in the scores).
 //
 // Per chunk of C = 64 tokens, with g the inclusive within-chunk product of
-// alpha (g = 1 without decay), G_ij = g_i / g_j:
-//   L   = tril(diag(b) (G . K Kt^T), -1)      A  = tril(G . Q Kt^T)
-//   X   = (I + L)^-1                          Xb = X diag(b)
-//   Kwn = -Xb diag(g) K                       Ae = A Xb
-//   Qe  = diag(g) Q + A Kwn
-// so that, for the state S entering the chunk, the chunk's residuals and
-// outputs are the single stacked product
-//   [U; O] = [Xb; Ae] V + [Kwn; Qe] S^T
-// and the state leaves as S' = g_C S + U^T diag(g_C / g) Kt.  The kernel
-// writes Kwn, Qe, Xb, Ae (bf16) and the gate factors g_C / g and g_C (fp32)
-// to the workspace, chunk-padded (rows past T are zero).
+// alpha (g = 1 without decay), G_ij = g_i / g_j and D = diag(g_C / g):
+//   L  = tril(diag(b) (G . K Kt^T), -1)       A  = tril(G . Q Kt^T)
+//   X  = (I + L)^-1,  Xb = X diag(b)          Kw = Xb diag(g) K
+//   W  = (D Kt)^T Xb          (K x C)         M  = -(D Kt)^T Kw     (K x K)
+//   Ae = A Xb                 (C x C)         Qe = diag(g) Q - A Kw (C x K)
+// so that, for the state S entering the chunk (U = Xb V - Kw S^T its scaled
+// residuals), the chunk's outputs and the state it leaves are
+//   O    = Ae V + Qe S^T
+//   S'^T = g_C S^T + W V + M S^T
+// -- one product with the state per chunk instead of two dependent ones.
+// The kernel writes W, M, Qe, Ae (bf16) and g_C (fp32) to the workspace;
+// rows past T are zero.
 //
 // One CTA per (chunk, sequence), 288 threads: warps 0-7 compute (epilogues
 // out of TMEM and the triangular solve), warp 8 issues the TMA loads and the
-// tcgen05 MMAs.  58 KB of shared memory and 128 TMEM columns, so three CTAs
-// share an SM and hide each other's latency.
+// tcgen05 MMAs.  The outputs are staged in shared memory in the tensor maps'
+// box layout, in tiles the kernel no longer needs, and leave by TMA stores.
+// 90 KB of shared memory and 256 TMEM columns: two CTAs share an SM and hide
+// each other's latency.
 #include "tc_common.cuh"
 
 namespace osdn {
@@ -31,31 +34,28 @@ namespace {
 constexpr int kLP = 68;              // fp32 pitch of the solver tile
 constexpr int kPrepThreads = 256;    // compute warps 0-7
 constexpr int kPrepBlock = 288;      // + the control warp
-constexpr uint32_t kPrepCols = 128;  // TMEM columns
+constexpr uint32_t kPrepCols = 256;  // TMEM columns
 
 struct PrepParams {
     int T;
     const float *beta, *alpha;
-    __nv_bfloat16 *kwn, *qe, *xb, *ae;
-    float *gk, *gc;
+    float *gc;
     int *status;
 };
 
 // Shared memory: [K;Q] stacked in 128-row blocks of 64 columns (K rows 0-63,
-// Q rows 64-127); Kt in 64-row blocks, whose space takes the fp32 solver tile
-// L once the Gram product has read Kt, and after the solve Xb and Xb diag(g)
-// (bf16); then the masked scores A (bf16).
+// later overwritten by Kw; Q rows 64-127), Kt in 64-row blocks (scaled to
+// D Kt in place once the Gram product has read it), the fp32 solver tile L,
+// then the bf16 tiles A, Xb and Xb diag(g).
 template <int K>
 struct PrepLay {
-    static constexpr int kLBytes = C * kLP * 4;
-    static constexpr int kKtBytes = C * K * 2;
-    static constexpr int kRegion = ((kKtBytes > kLBytes ? kKtBytes : kLBytes) + 1023) / 1024 * 1024;
     static constexpr int oKQ = 0;
     static constexpr int oKt = 128 * K * 2;
-    static constexpr int oXb = oKt;
-    static constexpr int oXg = oKt + C * C * 2;
-    static constexpr int oA = oKt + kRegion;
-    static constexpr int kBytes = oA + C * C * 2;
+    static constexpr int oL = oKt + C * K * 2;
+    static constexpr int oA = oL + ((C * kLP * 4 + 1023) / 1024) * 1024;
+    static constexpr int oXb = oA + C * C * 2;
+    static constexpr int oXg = oXb + C * C * 2;
+    static constexpr int kBytes = oXg + C * C * 2;
     static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -159,16 +159,20 @@ __device__ void solve_unit_lower(float *sL, int pt) {
 }
 
 template <int K, bool GATED>
-__global__ void __launch_bounds__(kPrepBlock, 3)
+__global__ void __launch_bounds__(kPrepBlock, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_kt, PrepParams p) {
+                  const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_w,
+                  const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_qe,
+                  const __grid_constant__ CUtensorMap tm_ae, PrepParams p) {
     using LY = PrepLay<K>;
-    constexpr int NH = K / 2;   // columns of a K-wide M=64 accumulator per thread
+    constexpr int NH = K / 2;   // columns of a K-wide accumulator per thread
+    // TMEM columns: Gram; then Kw | W | Ae; then M' | Qe'
+    constexpr uint32_t cKw = 0, cW = 128, cAe = 192, cM = 0, cQe = 128;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    __shared__ uint64_t bar_full, bar_g, bar_x2, bar_ae, bar_x3, bar_kw, bar_x4, bar_qe;
+    __shared__ uint64_t bar_full, bar_g, bar_x2, bar_p1, bar_x3, bar_p2;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float sBeta[C], sLg[C];
+    __shared__ float sBeta[C], sLg[C], sD[C];
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -177,12 +181,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int nvalid = min(C, T - t0);
     uint8_t *sKQ = smem + LY::oKQ, *sKt = smem + LY::oKt, *sA = smem + LY::oA;
     uint8_t *sXb = smem + LY::oXb, *sXg = GATED ? smem + LY::oXg : sXb;
-    float *sL = reinterpret_cast<float *>(smem + LY::oKt);
+    float *sL = reinterpret_cast<float *>(smem + LY::oL);
     int *st = p.status;
-    const size_t row0 = (size_t)seq * Tp + t0;   // first padded row of this chunk
+    const int krow0 = j * K;   // this chunk's rows of W and M within the sequence
+    // staging of the outputs: W over L; Ae over Xb; M (64x64 boxes) over Kt
+    // and the Kw rows of [K;Q]; Qe in place of Q
+    uint8_t *sW = smem + LY::oL;
+    auto mbox = [&](int rb, int cb) {
+        const int i = rb * (K / 64) + cb;
+        return i < 2 ? sKt + i * 8192 : sKQ + (i - 2) * 16384;
+    };
 
     if (tid == kPrepThreads) {
-        uint64_t *all[] = {&bar_full, &bar_g, &bar_x2, &bar_ae, &bar_x3, &bar_kw, &bar_x4, &bar_qe};
+        uint64_t *all[] = {&bar_full, &bar_g, &bar_x2, &bar_p1, &bar_x3, &bar_p2};
         for (uint64_t *b : all) ptx::mbar_init(b, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -221,37 +232,35 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 last = &bar_g;
             }
             ok = ok && wait_bar(&bar_x2, 0, &s_abort, st);
-            if (ok) {  // Ae = A Xb
+            if (ok) {  // Kw = Xb diag(g) K;  W = (D Kt)^T Xb;  Ae = A Xb
                 ptx::tc_fence_after();
-                const uint32_t id = ptx::idesc_bf16(64, 64, 0, 1);
-                const uint64_t da = dk0(aA), db = dmn0(aXb, 8192);
+                const uint32_t idk = ptx::idesc_bf16(64, K, 0, 1);
+                const uint32_t idw = ptx::idesc_bf16(K, 64, 1, 1);
+                const uint32_t ida = ptx::idesc_bf16(64, 64, 0, 1);
+                const uint64_t dXg = dk0(aXg), dK = dmn0(aKQ, 16384), dKt = dmn0(aKt, 8192);
+                const uint64_t dXb = dmn0(aXb, 8192), dA = dk0(aA);
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    ptx::umma_bf16(tmem, da + koff(C, ks), db + mnoff(ks), id, ks > 0);
-                ptx::umma_commit(&bar_ae);
-                last = &bar_ae;
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    ptx::umma_bf16(tmem + cKw, dXg + koff(C, ks), dK + mnoff(ks), idk, ks > 0);
+                    ptx::umma_bf16(tmem + cW, dKt + mnoff(ks), dXb + mnoff(ks), idw, ks > 0);
+                    ptx::umma_bf16(tmem + cAe, dA + koff(C, ks), dXb + mnoff(ks), ida, ks > 0);
+                }
+                ptx::umma_commit(&bar_p1);
+                last = &bar_p1;
             }
             ok = ok && wait_bar(&bar_x3, 0, &s_abort, st);
-            if (ok) {  // Kw = Xb diag(g) K  (K read as an MN-major operand)
+            if (ok) {  // M' = (D Kt)^T Kw;  Qe' = A Kw  (Kw written over the K rows)
                 ptx::tc_fence_after();
-                const uint32_t id = ptx::idesc_bf16(64, K, 0, 1);
-                const uint64_t da = dk0(aXg), db = dmn0(aKQ, 16384);
+                const uint32_t idm = ptx::idesc_bf16(K, K, 1, 1);
+                const uint32_t idq = ptx::idesc_bf16(64, K, 0, 1);
+                const uint64_t dKt = dmn0(aKt, 8192), dKw = dmn0(aKQ, 16384), dA = dk0(aA);
 #pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    ptx::umma_bf16(tmem, da + koff(C, ks), db + mnoff(ks), id, ks > 0);
-                ptx::umma_commit(&bar_kw);
-                last = &bar_kw;
-            }
-            ok = ok && wait_bar(&bar_x4, 0, &s_abort, st);
-            if (ok) {  // A Kwn  (Kwn written over the K rows)
-                ptx::tc_fence_after();
-                const uint32_t id = ptx::idesc_bf16(64, K, 0, 1);
-                const uint64_t da = dk0(aA), db = dmn0(aKQ, 16384);
-#pragma unroll
-                for (int ks = 0; ks < C / 16; ++ks)
-                    ptx::umma_bf16(tmem, da + koff(C, ks), db + mnoff(ks), id, ks > 0);
-                ptx::umma_commit(&bar_qe);
-                last = &bar_qe;
+                for (int ks = 0; ks < C / 16; ++ks) {
+                    ptx::umma_bf16(tmem + cM, dKt + mnoff(ks), dKw + mnoff(ks), idm, ks > 0);
+                    ptx::umma_bf16(tmem + cQe, dA + koff(C, ks), dKw + mnoff(ks), idq, ks > 0);
+                }
+                ptx::umma_commit(&bar_p2);
+                last = &bar_p2;
             }
             // the copies and products this CTA started land before it exits
             drain_bar(&bar_full, 0);
@@ -288,11 +297,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (GATED && pt < C) {
             // tokens past T add nothing to the log, so sLg[C-1] is the chunk's total
             const float lgC = sLg[C - 1];
-            p.gk[row0 + pt] = (pt < nvalid) ? __expf(lgC - sLg[pt]) : 0.0f;
+            sD[pt] = (pt < nvalid) ? __expf(lgC - sLg[pt]) : 0.0f;
             if (pt == 0) p.gc[(size_t)seq * nch + j] = __expf(lgC);
         }
 
-        // ---- Gram / scores: L (fp32) over Kt's space, A (bf16) for the MMAs
+        // ---- Gram / scores: L (fp32) and A (bf16); then Kt <- D Kt
         bool ok = vote_all(wait_bar(&bar_g, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
@@ -319,11 +328,26 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 st_row_sw128(sA, C, t, 32 * half, g, 32);
             }
-            ptx::fence_proxy_async_smem();
+            if (GATED) {  // Kt rows scaled by g_C / g_t (the Gram product has read Kt)
+                constexpr int PIECES = C * K * 2 / 16;
+                for (int i = pt; i < PIECES; i += kPrepThreads) {
+                    const int row = (i >> 3) & 63;   // 8 pieces per 128-byte row
+                    uint4 *q = reinterpret_cast<uint4 *>(sKt + i * 16);
+                    uint4 u = *q;
+                    const float f = sD[row];
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&wv[e]));
+                        wv[e] = pack_bf16x2(x.x * f, x.y * f);
+                    }
+                    *q = u;
+                }
+            }
             ptx::tc_fence_before();
             ptx::named_bar(1, kPrepThreads);
             solve_unit_lower(sL, pt);
-            // ---- Xb = X diag(beta) (global and shared), Xb diag(g) (shared)
+            // ---- Xb = X diag(beta) and Xb diag(g), bf16 for the MMAs
             const int t = pt >> 2, s0 = 16 * (pt & 3);
             float xb[16];
 #pragma unroll
@@ -331,8 +355,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int s = s0 + e;
                 xb[e] = (s <= t) ? sL[t * kLP + s] * sBeta[s] : 0.0f;
             }
-            ptx::named_bar(1, kPrepThreads);   // L fully read before Xb overwrites it
-            st_global_bf16(p.xb + (row0 + t) * C + s0, xb, 16);
             st_row_sw128(sXb, C, t, s0, xb, 16);
             if (GATED) {
 #pragma unroll
@@ -343,59 +365,84 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             ptx::named_bar(1, kPrepThreads);
             if (pt == 0) ptx::mbar_arrive(&bar_x2);
         }
-        // M=64 accumulators: row 16*q4 + lane (lanes 0-15 of each quarter)
+        // M=64 accumulators: row 16*q4 + lane (lanes 0-15 of each quarter);
+        // an M=K accumulator: row 32*q4 + lane (K = 128) or as M=64 (K = 64)
         const int mrow = 16 * q4 + lane;
         const bool act = lane < 16;
-        // ---- Ae out of TMEM
-        if (ok) ok = vote_all(wait_bar(&bar_ae, 0, &s_abort, st), 1, kPrepThreads);
-        if (ok) {
-            ptx::tc_fence_after();
-            float a[32];
-            tmem_ld32(tmem + lane_off + 32 * half, a);
-            if (act) st_global_bf16(p.ae + (row0 + mrow) * C + 32 * half, a, 32);
-            ptx::tc_fence_before();
-            ptx::named_bar(1, kPrepThreads);
-            if (pt == 0) ptx::mbar_arrive(&bar_x3);
-        }
-        // ---- Kwn = -Kw: to the workspace and over the K rows (B operand of A Kwn)
-        if (ok) ok = vote_all(wait_bar(&bar_kw, 0, &s_abort, st), 1, kPrepThreads);
+        const int krow = (K == 128) ? 32 * q4 + lane : mrow;
+        const bool kact = (K == 128) || act;
+        // ---- Kw (bf16 over the K rows), W and Ae (to the workspace)
+        if (ok) ok = vote_all(wait_bar(&bar_p1, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
 #pragma unroll
             for (int c = 0; c < NH; c += 16) {
-                float w[16];
-                ptx::tmem_ld16(tmem + lane_off + half * NH + c, w);
+                float v[16];
+                ptx::tmem_ld16(tmem + lane_off + cKw + half * NH + c, v);
                 ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = -w[e];
-                if (act) {
-                    st_global_bf16(p.kwn + (row0 + mrow) * K + half * NH + c, w, 16);
-                    st_row_sw128(sKQ, 128, mrow, half * NH + c, w, 16);
-                }
+                if (act) st_row_sw128(sKQ, 128, mrow, half * NH + c, v, 16);
+            }
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + cW + 32 * half, v);
+                if (kact) st_row_sw128(sW + (krow >> 6) * 8192, 64, krow & 63, 32 * half, v, 32);
+                tmem_ld32(tmem + lane_off + cAe + 32 * half, v);
+                if (act) st_row_sw128(sXb, 64, mrow, 32 * half, v, 32);
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::named_bar(1, kPrepThreads);
-            if (pt == 0) ptx::mbar_arrive(&bar_x4);
+            if (pt == 0) {
+                ptx::mbar_arrive(&bar_x3);
+#pragma unroll
+                for (int rb = 0; rb < K / 64; ++rb) ptx::tma_store_3d(&tm_w, sW + rb * 8192, 0, krow0 + rb * 64, seq);
+                ptx::tma_store_3d(&tm_ae, sXb, 0, t0, seq);
+                ptx::bulk_commit_group();
+            }
         }
-        // ---- Qe = diag(g) Q + A Kwn
-        if (ok) ok = vote_all(wait_bar(&bar_qe, 0, &s_abort, st), 1, kPrepThreads);
+        // ---- M = -M' and Qe = diag(g) Q - Qe'
+        if (ok) ok = vote_all(wait_bar(&bar_p2, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
-            const float gt = GATED ? __expf(sLg[mrow]) : 1.0f;
+#pragma unroll
+            for (int c = 0; c < NH; c += 16) {
+                float v[16];
+                ptx::tmem_ld16(tmem + lane_off + cM + half * NH + c, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = -v[e];
+                const int col = half * NH + c;
+                if (kact) st_row_sw128(mbox(krow >> 6, col >> 6), 64, krow & 63, col & 63, v, 16);
+            }
+            const float gt = GATED ? __expf(sLg[mrow & 63]) : 1.0f;
 #pragma unroll
             for (int c = 0; c < NH; c += 16) {
                 float d[16], qv[16];
-                ptx::tmem_ld16(tmem + lane_off + half * NH + c, d);
+                ptx::tmem_ld16(tmem + lane_off + cQe + half * NH + c, d);
                 ptx::tmem_wait_ld();
                 if (act) {
                     ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) d[e] = fmaf(gt, qv[e], d[e]);
-                    st_global_bf16(p.qe + (row0 + mrow) * K + half * NH + c, d, 16);
+                    for (int e = 0; e < 16; ++e) d[e] = fmaf(gt, qv[e], -d[e]);
+                    st_row_sw128(sKQ, 128, C + mrow, half * NH + c, d, 16);
                 }
             }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, kPrepThreads);
+            if (pt == 0) {
+#pragma unroll
+                for (int rb = 0; rb < K / 64; ++rb)
+#pragma unroll
+                    for (int cb = 0; cb < K / 64; ++cb)
+                        ptx::tma_store_3d(&tm_m, mbox(rb, cb), cb * 64, krow0 + rb * 64, seq);
+#pragma unroll
+                for (int cb = 0; cb < K / 64; ++cb)
+                    ptx::tma_store_3d(&tm_qe, sKQ + cb * 16384 + 8192, cb * 64, t0, seq);
+                ptx::bulk_commit_group();
+            }
         }
+        // the stores have read their shared-memory tiles before the CTA exits
+        if (pt == 0) ptx::bulk_wait_read_all();
     }
 
     ptx::tc_fence_before();
@@ -405,11 +452,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
 template <int K, bool GATED>
 cudaError_t prep_launch_t(int BH, int T, const void *q, const void *k, const void *kt,
-                          const float *beta, const float *alpha, __nv_bfloat16 *kwn,
-                          __nv_bfloat16 *qe, __nv_bfloat16 *xb, __nv_bfloat16 *ae, float *gk,
-                          float *gc, int *status, cudaStream_t stream) {
-    CUtensorMap mk, mq, mkt;
-    if (!make_map(&mk, k, BH, T, K) || !make_map(&mq, q, BH, T, K) || !make_map(&mkt, kt, BH, T, K))
+                          const float *beta, const float *alpha, __nv_bfloat16 *w,
+                          __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
+                          int *status, cudaStream_t stream) {
+    const int nch = (T + C - 1) / C, Tp = nch * C;
+    CUtensorMap mk, mq, mkt, mw, mm, mqe, mae;
+    if (!make_map(&mk, k, BH, T, K) || !make_map(&mq, q, BH, T, K) || !make_map(&mkt, kt, BH, T, K) ||
+        !make_map(&mw, w, BH, nch * K, C) || !make_map(&mm, m, BH, nch * K, K) ||
+        !make_map(&mqe, qe, BH, Tp, K) || !make_map(&mae, ae, BH, Tp, C))
         return cudaErrorInvalidValue;
     constexpr int smem = PrepLay<K>::kAlloc;
     static bool attr_set = false;
@@ -423,32 +473,27 @@ cudaError_t prep_launch_t(int BH, int T, const void *q, const void *k, const voi
     p.T = T;
     p.beta = beta;
     p.alpha = alpha;
-    p.kwn = kwn;
-    p.qe = qe;
-    p.xb = xb;
-    p.ae = ae;
-    p.gk = gk;
     p.gc = gc;
     p.status = status;
-    dim3 grid((T + C - 1) / C, BH);
-    chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, p);
+    dim3 grid(nch, BH);
+    chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t chunk_prep_launch(int BH, int T, int K, const void *q, const void *k, const void *kt,
-                              const float *beta, const float *alpha, __nv_bfloat16 *kwn,
-                              __nv_bfloat16 *qe, __nv_bfloat16 *xb, __nv_bfloat16 *ae, float *gk,
-                              float *gc, int *status, cudaStream_t stream) {
+                              const float *beta, const float *alpha, __nv_bfloat16 *w,
+                              __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
+                              int *status, cudaStream_t stream) {
     if (K == 128) {
         if (alpha)
-            return prep_launch_t<128, true>(BH, T, q, k, kt, beta, alpha, kwn, qe, xb, ae, gk, gc, status, stream);
-        return prep_launch_t<128, false>(BH, T, q, k, kt, beta, alpha, kwn, qe, xb, ae, gk, gc, status, stream);
+            return prep_launch_t<128, true>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<128, false>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
     }
     if (alpha)
-        return prep_launch_t<64, true>(BH, T, q, k, kt, beta, alpha, kwn, qe, xb, ae, gk, gc, status, stream);
-    return prep_launch_t<64, false>(BH, T, q, k, kt, beta, alpha, kwn, qe, xb, ae, gk, gc, status, stream);
+        return prep_launch_t<64, true>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+    return prep_launch_t<64, false>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
 }
 
 }  // namespace tc

@@ -9,90 +9,98 @@
 // Two kernels.  chunk_prep_kernel (phase2_prep.cu) does, for every chunk of
 // every sequence in parallel, all the work that does not involve the state:
 // the Gram matrix, the unit-lower triangular inverse and the products that
-// fold it into the operands Kwn, Qe, Xb, Ae.  The chain kernel here then runs
-// the state recurrence, one chunk of C = 64 tokens after the other:
-//   [U; O] = [Xb; Ae] V + [Kwn; Qe] S^T          (one M=128 accumulator)
-//   S'^T   = g_C S^T + Kt^T (diag(g_C / g) U)
+// fold it into the per-chunk operands W, M, Qe, Ae.  The chain kernel here
+// then runs the state recurrence, one chunk of C = 64 tokens after another:
+//   S'^T = g_C S^T + [W | M] [V; S^T]           (the only product on the chain)
+//   O    = [Ae | Qe] [V; S^T]                   (off the chain)
 // with S^T kept as an fp32 accumulator in TMEM and as a bf16 copy in shared
-// memory (the B operand of the next chunk's product).
+// memory (the B operand of both products).  The output product of a chunk is
+// issued after the next chunk's state product, so the chain never queues
+// behind it; three bf16 copies of the state rotate to allow that.
 //
-// One CTA per (sequence, 64 columns of V), 320 threads in five roles:
-//   warp 0      TMA producer: V and [Xb; Ae] (2-deep ring), [Kwn; Qe] and Kt
-//               (3- or 4-deep ring);
-//   warp 1      MMA issuer (one thread): every tcgen05.mma and commit;
-//   warps 2-3   O out of TMEM (rows 64-127) to global memory as bf16;
-//   warps 4-7   the state: S^T out of TMEM, its bf16 copy, the decay g_C,
-//               and the final state;
-//   warps 8-9   U out of TMEM (rows 0-63), scaled by g_C / g, as the bf16 B
-//               operand of the state update.
-// The chain per chunk is: product into [U; O] -> U to shared memory -> state
-// update -> S^T to shared memory; the product of the next chunk's V term and
-// the O readout overlap it.  Every wait is bounded: a wait that runs out
-// records OSDN_ERR_TIMEOUT in the status word and all roles leave their loops.
+// One CTA per (sequence, 64 columns of V), 320 threads in four roles:
+//   warp 0      TMA producer: [W | M] and V (2-deep ring), [Ae | Qe] and V
+//               (2-deep ring; V is loaded twice so that each ring stage is
+//               released by one product);
+//   warp 1      MMA issuer (one thread): every tcgen05.mma and commit; it
+//               polls its barriers without sleeping;
+//   warps 2-5   O out of TMEM to global memory as bf16;
+//   warps 6-9   the state: S^T out of TMEM, its bf16 copy, the decay g_C of
+//               the next chunk, and the final state.
+// Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
+// status word and all roles leave their loops.
 #include "tc_common.cuh"
 
 namespace osdn {
 namespace tc {
 
 cudaError_t chunk_prep_launch(int BH, int T, int K, const void *q, const void *k, const void *kt,
-                              const float *beta, const float *alpha, __nv_bfloat16 *kwn,
-                              __nv_bfloat16 *qe, __nv_bfloat16 *xb, __nv_bfloat16 *ae, float *gk,
-                              float *gc, int *status, cudaStream_t stream);
+                              const float *beta, const float *alpha, __nv_bfloat16 *w,
+                              __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
+                              int *status, cudaStream_t stream);
 
 namespace {
 
 constexpr int BV = 64;          // columns of V (rows of S) per CTA
-constexpr int NA = 2;           // depth of the V / [Xb; Ae] ring
+constexpr int NS = 2;           // depth of both input rings
+constexpr int NSB = 3;          // bf16 copies of the state
 constexpr int kThreads = 320;
-constexpr uint32_t kColUO = 0;  // [U; O] (M=128), two buffers of 64 columns
-constexpr uint32_t kColS = 128; // S^T (M=K), 64 columns
+constexpr uint32_t kColS = 0;   // S^T (M=K), 64 columns
+constexpr uint32_t kColO = 64;  // O (M=64), two buffers of 64 columns
 constexpr uint32_t kTmemCols = 256;
 
-// Shared memory: ring A stages ([Xb; Ae] as one 128-row K-major block, then
-// V), ring B stages ([Kwn; Qe] as 128-row blocks of 64 columns, then Kt in
-// 64-row blocks), the bf16 copy of S^T (K rows of 64 values) and the scaled
-// U (64 rows of 64 values).
+// Shared memory: ring X stages ([W | M] as K-row blocks of 64 columns, then
+// V), ring Y stages ([Ae | Qe] as 64-row blocks of 64 columns, then V), and
+// the bf16 copies of S^T (K rows of 64 values each).
 template <int K>
 struct Lay {
-    static constexpr int NB = (K == 128) ? 3 : 4;
-    static constexpr int kA = 3 * C * 128;
-    static constexpr int kB = 128 * K * 2 + C * K * 2;
-    static constexpr int oKt = 128 * K * 2;    // within a ring B stage
-    static constexpr int oV = 2 * C * 128;     // within a ring A stage
-    static constexpr int oA = 0;
-    static constexpr int oB = NA * kA;
-    static constexpr int oS = oB + NB * kB;
-    static constexpr int oU = oS + K * 128;
-    static constexpr int kBytes = oU + C * 128;
+    static constexpr int oVx = (1 + K / 64) * K * 128;   // within a ring X stage
+    static constexpr int oVy = (1 + K / 64) * C * 128;   // within a ring Y stage
+    static constexpr int kX = oVx + C * 128;
+    static constexpr int kY = oVy + C * 128;
+    static constexpr int oX = 0;
+    static constexpr int oY = NS * kX;
+    static constexpr int oS = oY + NS * kY;
+    static constexpr int kBytes = oS + NSB * K * 128;
     static constexpr int kAlloc = kBytes + 1024;
 };
 
+// Bounded poll without a suspend hint, for the MMA issuer: its waits sit on
+// the chain's critical path, where a sleeping thread wakes too late.
+__device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status) {
+    for (uint32_t i = 0; i < (kWaitLimit << 11); ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort_flag) return false;
+    }
+    report_status(status, OSDN_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
 struct Params {
-    int T, V, nch, Tp;
-    const float *S0, *gk, *gc;
+    int T, V, nch;
+    const float *S0, *gc;
     __nv_bfloat16 *o;
     float *ST;
     int *status;
 };
 
-template <int NB>
 struct Bars {
-    uint64_t fullA[NA], emptyA[NA], fullB[NB], emptyB[NB];
-    uint64_t u_full, u_sm, s_full, s_ready, done;
-    uint64_t o_full[2], acc_free[2];
+    uint64_t fullX[NS], emptyX[NS], fullY[NS], emptyY[NS];
+    uint64_t s_full, s_ready, done;
+    uint64_t o_full[2], o_free[2];
 };
 
 template <int K, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_constant__ CUtensorMap tm_ae,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kwn,
-                   const __grid_constant__ CUtensorMap tm_qe, const __grid_constant__ CUtensorMap tm_kt,
-                   Params p) {
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_m,
+                   const __grid_constant__ CUtensorMap tm_ae, const __grid_constant__ CUtensorMap tm_qe,
+                   const __grid_constant__ CUtensorMap tm_v, Params p) {
     using LY = Lay<K>;
-    constexpr int NB = LY::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    __shared__ Bars<NB> bars;
+    __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int s_abort;
 
@@ -100,22 +108,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
     const int q4 = warp & 3;
     const int seq = blockIdx.y, v0 = blockIdx.x * BV;
     const int T = p.T, nch = p.nch;
-    uint8_t *sS = smem + LY::oS, *sU = smem + LY::oU;
-    auto stA = [&](int j) { return smem + LY::oA + (j % NA) * LY::kA; };
-    auto stB = [&](int j) { return smem + LY::oB + (j % NB) * LY::kB; };
+    auto stX = [&](int j) { return smem + LY::oX + (j % NS) * LY::kX; };
+    auto stY = [&](int j) { return smem + LY::oY + (j % NS) * LY::kY; };
+    // the bf16 copy of the state leaving chunk j (j = -1: the initial state)
+    auto sS = [&](int j) { return smem + LY::oS + ((j + NSB) % NSB) * K * 128; };
     int *st = p.status;
 
     if (tid == 0) {
-        for (int i = 0; i < NA; ++i) {
-            ptx::mbar_init(&bars.fullA[i], 1);
-            ptx::mbar_init(&bars.emptyA[i], 1);
+        for (int i = 0; i < NS; ++i) {
+            ptx::mbar_init(&bars.fullX[i], 1);
+            ptx::mbar_init(&bars.emptyX[i], 1);
+            ptx::mbar_init(&bars.fullY[i], 1);
+            ptx::mbar_init(&bars.emptyY[i], 1);
         }
-        for (int i = 0; i < NB; ++i) {
-            ptx::mbar_init(&bars.fullB[i], 1);
-            ptx::mbar_init(&bars.emptyB[i], 1);
-        }
-        uint64_t *one[] = {&bars.u_full, &bars.u_sm, &bars.s_full, &bars.s_ready, &bars.done,
-                           &bars.o_full[0], &bars.o_full[1], &bars.acc_free[0], &bars.acc_free[1]};
+        uint64_t *one[] = {&bars.s_full, &bars.s_ready, &bars.done,
+                           &bars.o_full[0], &bars.o_full[1], &bars.o_free[0], &bars.o_free[1]};
         for (uint64_t *b : one) ptx::mbar_init(b, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -133,121 +140,124 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
     if (warp == 0) {
         // ======================================================== producer
         if (lane == 0) {
-            ptx::prefetch_tmap(&tm_xb);
+            ptx::prefetch_tmap(&tm_w);
+            ptx::prefetch_tmap(&tm_m);
             ptx::prefetch_tmap(&tm_ae);
-            ptx::prefetch_tmap(&tm_v);
-            ptx::prefetch_tmap(&tm_kwn);
             ptx::prefetch_tmap(&tm_qe);
-            ptx::prefetch_tmap(&tm_kt);
-            int lastA = -1, lastB = -1;
+            ptx::prefetch_tmap(&tm_v);
+            int lastX = -1, lastY = -1;
             for (int j = 0; j < nch; ++j) {
-                const int t0 = j * C;
-                if (j >= NA && !wait_bar(&bars.emptyA[j % NA], ((j / NA) - 1) & 1, &s_abort, st)) break;
-                uint8_t *a = stA(j);
-                ptx::mbar_arrive_expect_tx(&bars.fullA[j % NA], LY::kA);
-                ptx::tma_load_3d(a, &tm_xb, &bars.fullA[j % NA], 0, t0, seq);
-                ptx::tma_load_3d(a + C * 128, &tm_ae, &bars.fullA[j % NA], 0, t0, seq);
-                ptx::tma_load_3d(a + LY::oV, &tm_v, &bars.fullA[j % NA], v0, t0, seq);
-                lastA = j;
-                if (j >= NB && !wait_bar(&bars.emptyB[j % NB], ((j / NB) - 1) & 1, &s_abort, st)) break;
-                uint8_t *b = stB(j);
-                ptx::mbar_arrive_expect_tx(&bars.fullB[j % NB], LY::kB);
+                const int t0 = j * C, r0 = j * K;   // rows of this chunk in (Qe, Ae, V) and (W, M)
+                if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st)) break;
+                uint8_t *x = stX(j);
+                ptx::mbar_arrive_expect_tx(&bars.fullX[j % NS], LY::kX);
 #pragma unroll
-                for (int cb = 0; cb < K / 64; ++cb) {
-                    ptx::tma_load_3d(b + cb * 16384, &tm_kwn, &bars.fullB[j % NB], cb * 64, t0, seq);
-                    ptx::tma_load_3d(b + cb * 16384 + 8192, &tm_qe, &bars.fullB[j % NB], cb * 64, t0, seq);
-                    ptx::tma_load_3d(b + LY::oKt + cb * 8192, &tm_kt, &bars.fullB[j % NB], cb * 64, t0, seq);
+                for (int rb = 0; rb < K / 64; ++rb) {
+                    ptx::tma_load_3d(x + rb * 8192, &tm_w, &bars.fullX[j % NS], 0, r0 + rb * 64, seq);
+#pragma unroll
+                    for (int cb = 0; cb < K / 64; ++cb)
+                        ptx::tma_load_3d(x + (1 + cb) * K * 128 + rb * 8192, &tm_m, &bars.fullX[j % NS],
+                                         cb * 64, r0 + rb * 64, seq);
                 }
-                lastB = j;
+                ptx::tma_load_3d(x + LY::oVx, &tm_v, &bars.fullX[j % NS], v0, t0, seq);
+                lastX = j;
+                if (j >= NS && !wait_bar(&bars.emptyY[j % NS], ((j / NS) - 1) & 1, &s_abort, st)) break;
+                uint8_t *y = stY(j);
+                ptx::mbar_arrive_expect_tx(&bars.fullY[j % NS], LY::kY);
+                ptx::tma_load_3d(y, &tm_ae, &bars.fullY[j % NS], 0, t0, seq);
+#pragma unroll
+                for (int cb = 0; cb < K / 64; ++cb)
+                    ptx::tma_load_3d(y + (1 + cb) * 8192, &tm_qe, &bars.fullY[j % NS], cb * 64, t0, seq);
+                ptx::tma_load_3d(y + LY::oVy, &tm_v, &bars.fullY[j % NS], v0, t0, seq);
+                lastY = j;
             }
             // bulk copies still in flight (only after an abort) land before exit
             if (s_abort) {
-                for (int j = (lastA >= NA ? lastA - NA + 1 : 0); j <= lastA; ++j)
-                    drain_bar(&bars.fullA[j % NA], (j / NA) & 1);
-                for (int j = (lastB >= NB ? lastB - NB + 1 : 0); j <= lastB; ++j)
-                    drain_bar(&bars.fullB[j % NB], (j / NB) & 1);
+                for (int j = (lastX >= NS ? lastX - NS + 1 : 0); j <= lastX; ++j)
+                    drain_bar(&bars.fullX[j % NS], (j / NS) & 1);
+                for (int j = (lastY >= NS ? lastY - NS + 1 : 0); j <= lastY; ++j)
+                    drain_bar(&bars.fullY[j % NS], (j / NS) & 1);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ======================================================== MMA issuer
         if (lane == 0) {
-            const uint32_t aS = ptx::smem_u32(sS), aU = ptx::smem_u32(sU);
-            const uint32_t id_uo = ptx::idesc_bf16(128, BV, 0, 1);   // K-major A, MN-major B
-            const uint32_t id_s = ptx::idesc_bf16(K, BV, 1, 1);      // Kt^T (MN-major) x U
-            const uint64_t dS = dmn0(aS, 8192), dU = dmn0(aU, 8192);
-            auto vterm = [&](int j) {  // [U; O] of chunk j = [Xb; Ae] V
-                const uint32_t a = ptx::smem_u32(stA(j));
-                const uint64_t da = dk0(a), dv = dmn0(a + LY::oV, 8192);
-                const uint32_t d = tmem + kColUO + 64 * (j & 1);
+            const uint32_t id_s = ptx::idesc_bf16(K, BV, 0, 1);    // K-major A, MN-major B
+            const uint32_t id_o = ptx::idesc_bf16(64, BV, 0, 1);
+            // O = [Ae | Qe] [V; S^T] of chunk c (S^T entering c); releases ring Y
+            auto out_product = [&](int c) -> bool {
+                if (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st)) return false;
+                ptx::tc_fence_after();
+                const uint32_t y = ptx::smem_u32(stY(c));
+                const uint64_t da = dk0(y), dV = dmn0(y + LY::oVy, 8192);
+                const uint64_t dSp = dmn0(ptx::smem_u32(sS(c - 1)), 8192);
+                const uint32_t d = tmem + kColO + 64 * (c & 1);
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
-                    ptx::umma_bf16(d, da + koff(128, ks), dv + mnoff(ks), id_uo, ks > 0);
-                ptx::umma_commit(&bars.emptyA[j % NA]);
-            };
-            bool ok = wait_bar(&bars.fullA[0], 0, &s_abort, st);
-            if (ok) {
-                ptx::tc_fence_after();
-                vterm(0);
-            }
-            for (int j = 0; ok && j < nch; ++j) {
-                if (!wait_bar(&bars.fullB[j % NB], (j / NB) & 1, &s_abort, st)) break;
-                if (!wait_bar(&bars.s_ready, j & 1, &s_abort, st)) break;
-                ptx::tc_fence_after();
-                const uint32_t b = ptx::smem_u32(stB(j));
-                {  // [U; O] += [Kwn; Qe] S^T
-                    const uint64_t da = dk0(b);
-                    const uint32_t d = tmem + kColUO + 64 * (j & 1);
+                    ptx::umma_bf16(d, da + koff(C, ks), dV + mnoff(ks), id_o, ks > 0);
 #pragma unroll
-                    for (int ks = 0; ks < K / 16; ++ks)
-                        ptx::umma_bf16(d, da + koff(128, ks), dS + mnoff(ks), id_uo, 1);
-                    ptx::umma_commit(&bars.u_full);
-                    ptx::umma_commit(&bars.o_full[j & 1]);
-                }
-                if (!wait_bar(&bars.u_sm, j & 1, &s_abort, st)) break;
+                for (int ks = 0; ks < K / 16; ++ks)
+                    ptx::umma_bf16(d, da + koff(C, 4 + ks), dSp + mnoff(ks), id_o, 1);
+                ptx::umma_commit(&bars.o_full[c & 1]);
+                ptx::umma_commit(&bars.emptyY[c % NS]);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < nch; ++j) {
+                ok = wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) &&
+                     wait_poll(&bars.s_ready, j & 1, &s_abort, st);
+                if (!ok) break;
                 ptx::tc_fence_after();
-                {  // S^T += Kt^T Uh
-                    const uint64_t da = dmn0(b + LY::oKt, 8192);
+                {  // S^T += [W | M] [V; S^T]; releases ring X
+                    const uint32_t x = ptx::smem_u32(stX(j));
+                    const uint64_t da = dk0(x), dV = dmn0(x + LY::oVx, 8192);
+                    const uint64_t dSp = dmn0(ptx::smem_u32(sS(j - 1)), 8192);
 #pragma unroll
                     for (int ks = 0; ks < C / 16; ++ks)
-                        ptx::umma_bf16(tmem + kColS, da + mnoff(ks), dU + mnoff(ks), id_s, 1);
+                        ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
+#pragma unroll
+                    for (int ks = 0; ks < K / 16; ++ks)
+                        ptx::umma_bf16(tmem + kColS, da + koff(K, 4 + ks), dSp + mnoff(ks), id_s, 1);
                     ptx::umma_commit(&bars.s_full);
-                    ptx::umma_commit(&bars.emptyB[j % NB]);
+                    ptx::umma_commit(&bars.emptyX[j % NS]);
                 }
-                if (j + 1 < nch) {  // V term of the next chunk, once its buffer is read out
-                    const int n = j + 1;
-                    if (!wait_bar(&bars.fullA[n % NA], (n / NA) & 1, &s_abort, st)) break;
-                    if (n >= 2 && !wait_bar(&bars.acc_free[n & 1], ((n >> 1) - 1) & 1, &s_abort, st)) break;
-                    ptx::tc_fence_after();
-                    vterm(n);
+                // the previous chunk's output, behind this chunk's state product
+                if (j >= 1) {
+                    ok = wait_poll(&bars.fullY[(j - 1) % NS], ((j - 1) / NS) & 1, &s_abort, st) &&
+                         out_product(j - 1);
+                    if (!ok) break;
                 }
             }
+            if (ok && nch > 0 && wait_poll(&bars.fullY[(nch - 1) % NS], ((nch - 1) / NS) & 1, &s_abort, st))
+                out_product(nch - 1);
             // every product issued has completed before TMEM is released
             ptx::umma_commit(&bars.done);
             drain_bar(&bars.done, 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < 6) {
         // ======================================================== O readout
-        const int ot = tid - 64;   // row t of the chunk (TMEM lane 64 + t)
+        const int ot = tid - 64;
+        const int trow = 16 * q4 + lane;   // M=64 accumulator: lanes 0-15 of each quarter
         for (int j = 0; j < nch; ++j) {
-            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st), 3, 64)) break;
+            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st), 3, 128)) break;
             ptx::tc_fence_after();
             float o[64];
-            tmem_ld64(tmem + lane_off + kColUO + 64 * (j & 1), o);
+            tmem_ld64(tmem + lane_off + kColO + 64 * (j & 1), o);
             ptx::tc_fence_before();
-            ptx::named_bar(3, 64);
-            if (ot == 0) ptx::mbar_arrive(&bars.acc_free[j & 1]);
-            const int t = j * C + ot;
-            if (t < T) st_global_bf16(p.o + ((size_t)seq * T + t) * p.V + v0, o, 64);
+            ptx::named_bar(3, 128);
+            if (ot == 0) ptx::mbar_arrive(&bars.o_free[j & 1]);
+            const int t = j * C + trow;
+            if (lane < 16 && t < T) st_global_bf16(p.o + ((size_t)seq * T + t) * p.V + v0, o, 64);
         }
-    } else if (warp < 8) {
+    } else {
         // ======================================================== state
-        const int sti = tid - 128;
+        const int sti = tid - 192;
         // S^T row k: TMEM lane k (M=128) or 32*(k/16) + k%16 (M=64)
         const int krow = (K == 128) ? 32 * q4 + lane : 16 * q4 + lane;
         const bool act = (K == 128) || lane < 16;
-        {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T
+        {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T (buffer of chunk -1)
             const float g0 = GATED ? p.gc[(size_t)seq * nch] : 1.0f;
 #pragma unroll
             for (int c0 = 0; c0 < BV; c0 += 32) {
@@ -255,7 +265,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     sv[e] = (act && p.S0) ? p.S0[((size_t)seq * p.V + v0 + c0 + e) * K + krow] : 0.0f;
-                if (act) st_row_sw128(sS, K, krow, c0, sv, 32);
+                if (act) st_row_sw128(sS(-1), K, krow, c0, sv, 32);
                 float lo[16], hi[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -287,7 +297,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
                             p.ST[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
                     }
                 } else {
-                    if (act) st_row_sw128(sS, K, krow, c0, sv, 32);
+                    if (act) st_row_sw128(sS(j), K, krow, c0, sv, 32);
                     if (GATED) {  // the next chunk's decay, applied before its update
                         float lo[16], hi[16];
 #pragma unroll
@@ -307,28 +317,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
             ptx::named_bar(1, 128);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
-    } else {
-        // ======================================================== U readout
-        const int ut = tid - 256;   // row t of the chunk (TMEM lane t)
-        for (int j = 0; j < nch; ++j) {
-            const float gk = GATED ? p.gk[(size_t)seq * p.Tp + j * C + ut] : 1.0f;
-            if (!vote_all(wait_bar(&bars.u_full, j & 1, &s_abort, st), 2, 64)) break;
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int c0 = 0; c0 < BV; c0 += 32) {
-                float u[32];
-                tmem_ld32(tmem + lane_off + kColUO + 64 * (j & 1) + c0, u);
-                if (GATED) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) u[e] *= gk;
-                }
-                st_row_sw128(sU, C, ut, c0, u, 32);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::named_bar(2, 64);
-            if (ut == 0) ptx::mbar_arrive(&bars.u_sm);
-        }
     }
 
     ptx::tc_fence_before();
@@ -337,16 +325,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_xb, const __grid_const
 }
 
 template <int K, bool GATED>
-cudaError_t chain_launch_t(int BH, int T, int V, const void *kt, const void *v,
-                           const __nv_bfloat16 *kwn, const __nv_bfloat16 *qe,
-                           const __nv_bfloat16 *xb, const __nv_bfloat16 *ae, const float *gk,
-                           const float *gc, const float *S0, void *o, float *ST, int *status,
-                           cudaStream_t stream) {
+cudaError_t chain_launch_t(int BH, int T, int V, const void *v, const __nv_bfloat16 *w,
+                           const __nv_bfloat16 *m, const __nv_bfloat16 *qe,
+                           const __nv_bfloat16 *ae, const float *gc, const float *S0, void *o,
+                           float *ST, int *status, cudaStream_t stream) {
     const int nch = (T + C - 1) / C, Tp = nch * C;
-    CUtensorMap mxb, mae, mv, mkwn, mqe, mkt;
-    if (!make_map(&mxb, xb, BH, Tp, C) || !make_map(&mae, ae, BH, Tp, C) ||
-        !make_map(&mv, v, BH, T, V) || !make_map(&mkwn, kwn, BH, Tp, K) ||
-        !make_map(&mqe, qe, BH, Tp, K) || !make_map(&mkt, kt, BH, T, K))
+    CUtensorMap mw, mm, mae, mqe, mv;
+    if (!make_map(&mw, w, BH, nch * K, C) || !make_map(&mm, m, BH, nch * K, K) ||
+        !make_map(&mae, ae, BH, Tp, C) || !make_map(&mqe, qe, BH, Tp, K) ||
+        !make_map(&mv, v, BH, T, V))
         return cudaErrorInvalidValue;
     constexpr int smem = Lay<K>::kAlloc;
     static bool attr_set = false;
@@ -360,44 +347,42 @@ cudaError_t chain_launch_t(int BH, int T, int V, const void *kt, const void *v,
     p.T = T;
     p.V = V;
     p.nch = nch;
-    p.Tp = Tp;
     p.S0 = S0;
-    p.gk = gk;
     p.gc = gc;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.ST = ST;
     p.status = status;
     dim3 grid(V / BV, BH);
-    chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mxb, mae, mv, mkwn, mqe, mkt, p);
+    chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
     return cudaGetLastError();
 }
 
-// Workspace carve-up of the prepared operands, chunk-padded to Tp rows.
+// Workspace carve-up of the prepared operands: W and M per chunk (K rows
+// each), Qe and Ae per token (chunk-padded), g_C per chunk.
 struct Carve {
-    __nv_bfloat16 *kwn, *qe, *xb, *ae;
-    float *gk, *gc;
+    __nv_bfloat16 *w, *m, *qe, *ae;
+    float *gc;
     size_t bytes;
 };
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 Carve carve(void *base, int BH, int T, int K) {
     const size_t nch = (size_t)(T + C - 1) / C, Tp = nch * C;
-    const size_t sz[6] = {round256((size_t)BH * Tp * K * 2), round256((size_t)BH * Tp * K * 2),
-                          round256((size_t)BH * Tp * C * 2), round256((size_t)BH * Tp * C * 2),
-                          round256((size_t)BH * Tp * 4), round256((size_t)BH * nch * 4)};
+    const size_t sz[5] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
+                          round256((size_t)BH * Tp * K * 2), round256((size_t)BH * Tp * C * 2),
+                          round256((size_t)BH * nch * 4)};
     char *b = static_cast<char *>(base);
-    Carve c;
+    char *ptrs[5];
     size_t off = 0;
-    char *ptrs[6];
-    for (int i = 0; i < 6; ++i) {
+    for (int i = 0; i < 5; ++i) {
         ptrs[i] = b ? b + off : nullptr;
         off += sz[i];
     }
-    c.kwn = reinterpret_cast<__nv_bfloat16 *>(ptrs[0]);
-    c.qe = reinterpret_cast<__nv_bfloat16 *>(ptrs[1]);
-    c.xb = reinterpret_cast<__nv_bfloat16 *>(ptrs[2]);
+    Carve c;
+    c.w = reinterpret_cast<__nv_bfloat16 *>(ptrs[0]);
+    c.m = reinterpret_cast<__nv_bfloat16 *>(ptrs[1]);
+    c.qe = reinterpret_cast<__nv_bfloat16 *>(ptrs[2]);
     c.ae = reinterpret_cast<__nv_bfloat16 *>(ptrs[3]);
-    c.gk = reinterpret_cast<float *>(ptrs[4]);
-    c.gc = reinterpret_cast<float *>(ptrs[5]);
+    c.gc = reinterpret_cast<float *>(ptrs[4]);
     c.bytes = off;
     return c;
 }
@@ -440,17 +425,17 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
                             cudaStream_t stream) {
     if (!tc::tensor_map_encoder_ready()) return cudaErrorNotSupported;
     const tc::Carve w = tc::carve(scratch, BH, T, K);
-    cudaError_t e = tc::chunk_prep_launch(BH, T, K, q, k, kt, beta, alpha, w.kwn, w.qe, w.xb, w.ae,
-                                          w.gk, w.gc, status, stream);
+    cudaError_t e = tc::chunk_prep_launch(BH, T, K, q, k, kt, beta, alpha, w.w, w.m, w.qe, w.ae,
+                                          w.gc, status, stream);
     if (e != cudaSuccess) return e;
     if (K == 128) {
         if (alpha)
-            return tc::chain_launch_t<128, true>(BH, T, V, kt, v, w.kwn, w.qe, w.xb, w.ae, w.gk, w.gc, S0, o, ST, status, stream);
-        return tc::chain_launch_t<128, false>(BH, T, V, kt, v, w.kwn, w.qe, w.xb, w.ae, w.gk, w.gc, S0, o, ST, status, stream);
+            return tc::chain_launch_t<128, true>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+        return tc::chain_launch_t<128, false>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
     }
     if (alpha)
-        return tc::chain_launch_t<64, true>(BH, T, V, kt, v, w.kwn, w.qe, w.xb, w.ae, w.gk, w.gc, S0, o, ST, status, stream);
-    return tc::chain_launch_t<64, false>(BH, T, V, kt, v, w.kwn, w.qe, w.xb, w.ae, w.gk, w.gc, S0, o, ST, status, stream);
+        return tc::chain_launch_t<64, true>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+    return tc::chain_launch_t<64, false>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
 }
 
 }  // namespace osdn

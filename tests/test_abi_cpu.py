@@ -90,14 +90,16 @@ def test_host_validation_chunk_fwd(L):
 
 def test_chunk_fwd_workspace_size(L):
     # fp32 I/O and empty sequences need only the status word; bf16 keeps each
-    # chunk's prepared operands (Kwn, Qe: 2K bytes a row each; Xb, Ae: 128;
-    # g_C/g: 4) on the chunk-padded length, plus g_C per chunk
+    # chunk's prepared operands: W (K x 64) and M (K x K) per chunk, Qe (2K
+    # bytes a row) and Ae (128 bytes a row) on the chunk-padded length, g_C
+    # per chunk
     assert L.osdn_chunk_fwd_workspace_bytes(0, 2, 3, 100, 128, 64) == 256
     assert L.osdn_chunk_fwd_workspace_bytes(1, 2, 3, 0, 128, 64) == 256
     for B, H, T, K in [(1, 1, 1, 64), (2, 3, 100, 128), (1, 16, 65536, 128)]:
         BH, Tp, nch = B * H, -(-T // 64) * 64, -(-T // 64)
         r = lambda x: -(-x // 256) * 256
-        want = 256 + 2 * r(BH * Tp * K * 2) + 2 * r(BH * Tp * 64 * 2) + r(BH * Tp * 4) + r(BH * nch * 4)
+        want = (256 + r(BH * nch * K * 64 * 2) + r(BH * nch * K * K * 2) + r(BH * Tp * K * 2)
+                + r(BH * Tp * 64 * 2) + r(BH * nch * 4))
         assert L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, 64) == want
 
 
