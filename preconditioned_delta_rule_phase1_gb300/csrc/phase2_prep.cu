@@ -177,7 +177,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j = blockIdx.x, seq = blockIdx.y, nch = gridDim.x;
-    const int T = p.T, t0 = j * C, Tp = nch * C;
+    const int T = p.T, t0 = j * C;
     const int nvalid = min(C, T - t0);
     uint8_t *sKQ = smem + LY::oKQ, *sKt = smem + LY::oKt, *sA = smem + LY::oA;
     uint8_t *sXb = smem + LY::oXb, *sXg = GATED ? smem + LY::oXg : sXb;

@@ -14,19 +14,22 @@
 //   S'^T = g_C S^T + [W | M] [V; S^T]           (the only product on the chain)
 //   O    = [Ae | Qe] [V; S^T]                   (off the chain)
 // with S^T kept as an fp32 accumulator in TMEM and as a bf16 copy in shared
-// memory (the B operand of both products).  The output product of a chunk is
-// issued after the next chunk's state product, so the chain never queues
-// behind it; three bf16 copies of the state rotate to allow that.
+// memory (the B operand of both products; three copies rotate, so the
+// output product may still read one while the next is written).
 //
-// One CTA per (sequence, 64 columns of V), 320 threads in four roles:
+// One CTA per (sequence, 64 columns of V), 480 threads in five roles:
 //   warp 0      TMA producer: [W | M] and V (2-deep ring), [Ae | Qe] and V
 //               (2-deep ring; V is loaded twice so that each ring stage is
 //               released by one product);
-//   warp 1      MMA issuer (one thread): every tcgen05.mma and commit; it
-//               polls its barriers without sleeping;
-//   warps 2-5   O out of TMEM to global memory as bf16;
-//   warps 6-9   the state: S^T out of TMEM, its bf16 copy, the decay g_C of
+//   warp 1      state MMA issuer (one thread): the chain's product only;
+//   warp 2      output MMA issuer (one thread): a chunk's output product,
+//               issued right behind its state product so that it never
+//               delays the chain;
+//   warps 3-6   O out of TMEM to global memory as bf16;
+//   warps 7-14  the state: S^T out of TMEM, its bf16 copy, the decay g_C of
 //               the next chunk, and the final state.
+// Both issuers poll their barriers without sleeping: their waits sit on the
+// chain's critical path.
 // Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
 // status word and all roles leave their loops.
 #include "tc_common.cuh"
@@ -44,7 +47,7 @@ namespace {
 constexpr int BV = 64;          // columns of V (rows of S) per CTA
 constexpr int NS = 2;           // depth of both input rings
 constexpr int NSB = 3;          // bf16 copies of the state
-constexpr int kThreads = 320;
+constexpr int kThreads = 480;
 constexpr uint32_t kColS = 0;   // S^T (M=K), 64 columns
 constexpr uint32_t kColO = 64;  // O (M=64), two buffers of 64 columns
 constexpr uint32_t kTmemCols = 256;
@@ -86,9 +89,14 @@ struct Params {
     int *status;
 };
 
+// Barriers.  The bf16 state copy entering chunk c sits in buffer c % NSB:
+// s_issued[b] completes when the state product reading it has been issued
+// (so the copy is complete), o_read[b] when the output product reading it
+// has completed (the buffer may then be overwritten).
 struct Bars {
     uint64_t fullX[NS], emptyX[NS], fullY[NS], emptyY[NS];
-    uint64_t s_full, s_ready, done;
+    uint64_t s_full, s_ready, done_s, done_o;
+    uint64_t s_issued[NSB], o_read[NSB];
     uint64_t o_full[2], o_free[2];
 };
 
@@ -110,8 +118,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     const int T = p.T, nch = p.nch;
     auto stX = [&](int j) { return smem + LY::oX + (j % NS) * LY::kX; };
     auto stY = [&](int j) { return smem + LY::oY + (j % NS) * LY::kY; };
-    // the bf16 copy of the state leaving chunk j (j = -1: the initial state)
-    auto sS = [&](int j) { return smem + LY::oS + ((j + NSB) % NSB) * K * 128; };
+    // the bf16 copy of the state entering chunk c
+    auto sS = [&](int c) { return smem + LY::oS + (c % NSB) * K * 128; };
     int *st = p.status;
 
     if (tid == 0) {
@@ -121,9 +129,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::mbar_init(&bars.fullY[i], 1);
             ptx::mbar_init(&bars.emptyY[i], 1);
         }
-        uint64_t *one[] = {&bars.s_full, &bars.s_ready, &bars.done,
+        uint64_t *one[] = {&bars.s_full, &bars.s_ready, &bars.done_s, &bars.done_o,
                            &bars.o_full[0], &bars.o_full[1], &bars.o_free[0], &bars.o_free[1]};
         for (uint64_t *b : one) ptx::mbar_init(b, 1);
+        for (int i = 0; i < NSB; ++i) {
+            ptx::mbar_init(&bars.s_issued[i], 1);
+            ptx::mbar_init(&bars.o_read[i], 1);
+        }
         ptx::fence_mbar_init();
         s_abort = 0;
     }
@@ -181,17 +193,47 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ======================================================== MMA issuer
+        // ======================================================== state MMA issuer
         if (lane == 0) {
             const uint32_t id_s = ptx::idesc_bf16(K, BV, 0, 1);    // K-major A, MN-major B
+            for (int j = 0; j < nch; ++j) {
+                if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) ||
+                    !wait_poll(&bars.s_ready, j & 1, &s_abort, st))
+                    break;
+                ptx::tc_fence_after();
+                // S^T += [W | M] [V; S^T]; releases ring X
+                const uint32_t x = ptx::smem_u32(stX(j));
+                const uint64_t da = dk0(x), dV = dmn0(x + LY::oVx, 8192);
+                const uint64_t dSp = dmn0(ptx::smem_u32(sS(j)), 8192);
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    ptx::umma_bf16(tmem + kColS, da + koff(K, 4 + ks), dSp + mnoff(ks), id_s, 1);
+                ptx::umma_commit(&bars.s_full);
+                ptx::umma_commit(&bars.emptyX[j % NS]);
+                ptx::mbar_arrive(&bars.s_issued[j % NSB]);
+            }
+            // every product issued has completed before TMEM is released
+            ptx::umma_commit(&bars.done_s);
+            drain_bar(&bars.done_s, 0);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ======================================================== output MMA issuer
+        if (lane == 0) {
             const uint32_t id_o = ptx::idesc_bf16(64, BV, 0, 1);
-            // O = [Ae | Qe] [V; S^T] of chunk c (S^T entering c); releases ring Y
-            auto out_product = [&](int c) -> bool {
-                if (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st)) return false;
+            for (int c = 0; c < nch; ++c) {
+                // O = [Ae | Qe] [V; S^T] of chunk c, behind chunk c's state product
+                if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st) ||
+                    !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st) ||
+                    (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st)))
+                    break;
                 ptx::tc_fence_after();
                 const uint32_t y = ptx::smem_u32(stY(c));
                 const uint64_t da = dk0(y), dV = dmn0(y + LY::oVy, 8192);
-                const uint64_t dSp = dmn0(ptx::smem_u32(sS(c - 1)), 8192);
+                const uint64_t dSp = dmn0(ptx::smem_u32(sS(c)), 8192);
                 const uint32_t d = tmem + kColO + 64 * (c & 1);
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
@@ -201,44 +243,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                     ptx::umma_bf16(d, da + koff(C, 4 + ks), dSp + mnoff(ks), id_o, 1);
                 ptx::umma_commit(&bars.o_full[c & 1]);
                 ptx::umma_commit(&bars.emptyY[c % NS]);
-                return true;
-            };
-            bool ok = true;
-            for (int j = 0; j < nch; ++j) {
-                ok = wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) &&
-                     wait_poll(&bars.s_ready, j & 1, &s_abort, st);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                {  // S^T += [W | M] [V; S^T]; releases ring X
-                    const uint32_t x = ptx::smem_u32(stX(j));
-                    const uint64_t da = dk0(x), dV = dmn0(x + LY::oVx, 8192);
-                    const uint64_t dSp = dmn0(ptx::smem_u32(sS(j - 1)), 8192);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
-#pragma unroll
-                    for (int ks = 0; ks < K / 16; ++ks)
-                        ptx::umma_bf16(tmem + kColS, da + koff(K, 4 + ks), dSp + mnoff(ks), id_s, 1);
-                    ptx::umma_commit(&bars.s_full);
-                    ptx::umma_commit(&bars.emptyX[j % NS]);
-                }
-                // the previous chunk's output, behind this chunk's state product
-                if (j >= 1) {
-                    ok = wait_poll(&bars.fullY[(j - 1) % NS], ((j - 1) / NS) & 1, &s_abort, st) &&
-                         out_product(j - 1);
-                    if (!ok) break;
-                }
+                ptx::umma_commit(&bars.o_read[c % NSB]);
             }
-            if (ok && nch > 0 && wait_poll(&bars.fullY[(nch - 1) % NS], ((nch - 1) / NS) & 1, &s_abort, st))
-                out_product(nch - 1);
-            // every product issued has completed before TMEM is released
-            ptx::umma_commit(&bars.done);
-            drain_bar(&bars.done, 0);
+            ptx::umma_commit(&bars.done_o);
+            drain_bar(&bars.done_o, 0);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 7) {
         // ======================================================== O readout
-        const int ot = tid - 64;
+        const int ot = tid - 96;
         const int trow = 16 * q4 + lane;   // M=64 accumulator: lanes 0-15 of each quarter
         for (int j = 0; j < nch; ++j) {
             if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st), 3, 128)) break;
@@ -253,68 +266,66 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         }
     } else {
         // ======================================================== state
-        const int sti = tid - 192;
-        // S^T row k: TMEM lane k (M=128) or 32*(k/16) + k%16 (M=64)
+        const int sti = tid - 224, half = (warp - 7) >> 2, c0 = 32 * half;
+        // S^T row k: TMEM lane k (M=128) or 32*(k/16) + k%16 (M=64); columns c0..c0+31
         const int krow = (K == 128) ? 32 * q4 + lane : 16 * q4 + lane;
         const bool act = (K == 128) || lane < 16;
-        {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T (buffer of chunk -1)
+        const uint32_t tS = tmem + lane_off + kColS + c0;
+        {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T
             const float g0 = GATED ? p.gc[(size_t)seq * nch] : 1.0f;
+            float sv[32];
 #pragma unroll
-            for (int c0 = 0; c0 < BV; c0 += 32) {
-                float sv[32];
+            for (int e = 0; e < 32; ++e)
+                sv[e] = (act && p.S0) ? p.S0[((size_t)seq * p.V + v0 + c0 + e) * K + krow] : 0.0f;
+            if (act) st_row_sw128(sS(0), K, krow, c0, sv, 32);
+            float lo[16], hi[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    sv[e] = (act && p.S0) ? p.S0[((size_t)seq * p.V + v0 + c0 + e) * K + krow] : 0.0f;
-                if (act) st_row_sw128(sS(-1), K, krow, c0, sv, 32);
-                float lo[16], hi[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    lo[e] = g0 * sv[e];
-                    hi[e] = g0 * sv[16 + e];
-                }
-                ptx::tmem_st16(tmem + lane_off + kColS + c0, lo);
-                ptx::tmem_st16(tmem + lane_off + kColS + c0 + 16, hi);
+            for (int e = 0; e < 16; ++e) {
+                lo[e] = g0 * sv[e];
+                hi[e] = g0 * sv[16 + e];
             }
+            ptx::tmem_st16(tS, lo);
+            ptx::tmem_st16(tS + 16, hi);
             ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::named_bar(1, 128);
+            ptx::named_bar(1, 256);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
         for (int j = 0; j < nch; ++j) {
             const bool last = (j == nch - 1);
             const float gN = (GATED && !last) ? p.gc[(size_t)seq * nch + j + 1] : 1.0f;
-            if (!vote_all(wait_bar(&bars.s_full, j & 1, &s_abort, st), 1, 128)) break;
+            if (!vote_all(wait_bar(&bars.s_full, j & 1, &s_abort, st), 1, 256)) break;
             ptx::tc_fence_after();
+            float sv[32];
+            tmem_ld32(tS, sv);
+            if (last) {
+                if (act && p.ST) {
 #pragma unroll
-            for (int c0 = 0; c0 < BV; c0 += 32) {
-                float sv[32];
-                tmem_ld32(tmem + lane_off + kColS + c0, sv);
-                if (last) {
-                    if (act && p.ST) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            p.ST[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
-                    }
-                } else {
-                    if (act) st_row_sw128(sS(j), K, krow, c0, sv, 32);
-                    if (GATED) {  // the next chunk's decay, applied before its update
-                        float lo[16], hi[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            lo[e] = gN * sv[e];
-                            hi[e] = gN * sv[16 + e];
-                        }
-                        ptx::tmem_st16(tmem + lane_off + kColS + c0, lo);
-                        ptx::tmem_st16(tmem + lane_off + kColS + c0 + 16, hi);
-                    }
+                    for (int e = 0; e < 32; ++e) p.ST[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
                 }
+                break;
             }
-            if (last) break;
+            if (GATED) {  // the next chunk's decay, applied before its update
+                float lo[16], hi[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    lo[e] = gN * sv[e];
+                    hi[e] = gN * sv[16 + e];
+                }
+                ptx::tmem_st16(tS, lo);
+                ptx::tmem_st16(tS + 16, hi);
+            }
+            // the copy entering chunk j+1 overwrites the one chunk j-2's output read
+            const int n = j + 1;
+            if (n >= NSB &&
+                !vote_all(wait_bar(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st), 1, 256))
+                break;
+            if (act) st_row_sw128(sS(n), K, krow, c0, sv, 32);
             if (GATED) ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::named_bar(1, 128);
+            ptx::named_bar(1, 256);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
     }
