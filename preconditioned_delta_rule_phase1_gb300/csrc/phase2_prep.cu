@@ -375,12 +375,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (ok) ok = vote_all(wait_bar(&bar_p1, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < NH; c += 16) {
-                float v[16];
-                ptx::tmem_ld16(tmem + lane_off + cKw + half * NH + c, v);
-                ptx::tmem_wait_ld();
-                if (act) st_row_sw128(sKQ, 128, mrow, half * NH + c, v, 16);
+            {
+                float v[NH];
+                tmem_ldn<NH>(tmem + lane_off + cKw + half * NH, v);
+                if (act) st_row_sw128(sKQ, 128, mrow, half * NH, v, NH);
             }
             {
                 float v[32];
@@ -404,27 +402,27 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (ok) ok = vote_all(wait_bar(&bar_p2, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
+            {
+                float v[NH];
+                tmem_ldn<NH>(tmem + lane_off + cM + half * NH, v);
 #pragma unroll
-            for (int c = 0; c < NH; c += 16) {
-                float v[16];
-                ptx::tmem_ld16(tmem + lane_off + cM + half * NH + c, v);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = -v[e];
-                const int col = half * NH + c;
-                if (kact) st_row_sw128(mbox(krow >> 6, col >> 6), 64, krow & 63, col & 63, v, 16);
+                for (int e = 0; e < NH; ++e) v[e] = -v[e];
+                const int col = half * NH;
+                if (kact) st_row_sw128(mbox(krow >> 6, col >> 6), 64, krow & 63, col & 63, v, NH);
             }
             const float gt = GATED ? __expf(sLg[mrow & 63]) : 1.0f;
-#pragma unroll
-            for (int c = 0; c < NH; c += 16) {
-                float d[16], qv[16];
-                ptx::tmem_ld16(tmem + lane_off + cQe + half * NH + c, d);
-                ptx::tmem_wait_ld();
+            {
+                float d[NH];
+                tmem_ldn<NH>(tmem + lane_off + cQe + half * NH, d);
                 if (act) {
-                    ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) d[e] = fmaf(gt, qv[e], -d[e]);
-                    st_row_sw128(sKQ, 128, C + mrow, half * NH + c, d, 16);
+                    for (int c = 0; c < NH; c += 16) {
+                        float qv[16];
+                        ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) qv[e] = fmaf(gt, qv[e], -d[c + e]);
+                        st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
+                    }
                 }
             }
             ptx::fence_proxy_async_smem();

@@ -28,8 +28,8 @@
 //   warps 3-6   O out of TMEM to global memory as bf16;
 //   warps 7-14  the state: S^T out of TMEM, its bf16 copy, the decay g_C of
 //               the next chunk, and the final state.
-// Both issuers poll their barriers without sleeping: their waits sit on the
-// chain's critical path.
+// The issuers and the state readout poll their barriers without sleeping:
+// their waits sit on the chain's critical path.
 // Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
 // status word and all roles leave their loops.
 #include "tc_common.cuh"
@@ -67,19 +67,6 @@ struct Lay {
     static constexpr int kBytes = oS + NSB * K * 128;
     static constexpr int kAlloc = kBytes + 1024;
 };
-
-// Bounded poll without a suspend hint, for the MMA issuer: its waits sit on
-// the chain's critical path, where a sleeping thread wakes too late.
-__device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int *status) {
-    for (uint32_t i = 0; i < (kWaitLimit << 11); ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
-    }
-    report_status(status, OSDN_ERR_TIMEOUT);
-    *abort_flag = 1;
-    return false;
-}
 
 struct Params {
     int T, V, nch;
@@ -212,8 +199,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 for (int ks = 0; ks < K / 16; ++ks)
                     ptx::umma_bf16(tmem + kColS, da + koff(K, 4 + ks), dSp + mnoff(ks), id_s, 1);
                 ptx::umma_commit(&bars.s_full);
-                ptx::umma_commit(&bars.emptyX[j % NS]);
                 ptx::mbar_arrive(&bars.s_issued[j % NSB]);
+                ptx::umma_commit(&bars.emptyX[j % NS]);
             }
             // every product issued has completed before TMEM is released
             ptx::umma_commit(&bars.done_s);
@@ -295,7 +282,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         for (int j = 0; j < nch; ++j) {
             const bool last = (j == nch - 1);
             const float gN = (GATED && !last) ? p.gc[(size_t)seq * nch + j + 1] : 1.0f;
-            if (!vote_all(wait_bar(&bars.s_full, j & 1, &s_abort, st), 1, 256)) break;
+            // the copy entering chunk j+1 overwrites the one chunk j-2's output read
+            const int n = j + 1;
+            const bool okw = (last || n < NSB ||
+                              wait_poll(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st)) &&
+                             wait_poll(&bars.s_full, j & 1, &s_abort, st);
+            if (!vote_all(okw, 1, 256)) break;
             ptx::tc_fence_after();
             float sv[32];
             tmem_ld32(tS, sv);
@@ -316,11 +308,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 ptx::tmem_st16(tS, lo);
                 ptx::tmem_st16(tS + 16, hi);
             }
-            // the copy entering chunk j+1 overwrites the one chunk j-2's output read
-            const int n = j + 1;
-            if (n >= NSB &&
-                !vote_all(wait_bar(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st), 1, 256))
-                break;
             if (act) st_row_sw128(sS(n), K, krow, c0, sv, 32);
             if (GATED) ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();

@@ -86,6 +86,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         v[16 + i] = b[i];
     }
 }
+// N (16, 32 or 64) consecutive TMEM columns, all loads in flight before one wait.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&v)[N]) {
+    static_assert(N == 16 || N == 32 || N == 64, "16, 32 or 64 columns");
+    float a[4][16];
+#pragma unroll
+    for (int q = 0; q < N / 16; ++q) ptx::tmem_ld16(taddr + 16 * q, a[q]);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < N / 16; ++q)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * q + i] = a[q][i];
+}
 // 64 consecutive TMEM columns, four loads in flight before one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     float a[16], b[16], c[16], d[16];
@@ -147,6 +160,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
         if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
         if (*abort_flag) return false;
+    }
+    report_status(status, OSDN_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+// Bounded poll without a suspend hint, for waits on a critical path, where a
+// sleeping thread wakes too late.
+__device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status) {
+    for (uint32_t i = 0; i < (kWaitLimit << 11); ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort_flag) return false;
     }
     report_status(status, OSDN_ERR_TIMEOUT);
     *abort_flag = 1;
