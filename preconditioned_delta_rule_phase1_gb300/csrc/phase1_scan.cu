@@ -297,24 +297,63 @@ __global__ void __launch_bounds__(K) precond_segment_kernel(Params p) {
 
 // Grid (BH): verify every speculative segment start against its predecessor's
 // end; recompute (exactly) the segments that do not match; write d_T.
+// Without a repair every boundary check is independent (the predecessor's
+// end is then exact), so all boundaries are checked at once first; the
+// sequential check-and-repair walk starts at the first boundary that fails.
 template <typename io_t, int K>
 __global__ void __launch_bounds__(K) precond_verify_kernel(Params p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem<io_t, K> &sm = *reinterpret_cast<Smem<io_t, K> *>(smem_raw);
     constexpr int NW = K / 32;
+    constexpr int kBatch = 64;   // boundaries checked per pass
     const int seq = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t base = (size_t)seq * p.nseg;
-    __shared__ int any_flag;
+    __shared__ int any_flag, first_bad;
+    __shared__ float sDiff[NW][kBatch], sMag[NW][kBatch];
     if (tid == 0) {
         int f = 0;
         for (int i = 0; i < p.nseg; ++i) f |= p.ws_flag[base + i];
         any_flag = f;
+        first_bad = f ? 1 : p.nseg;
         sm.flag = 0;
     }
     __syncthreads();
+    // ---- all boundaries in parallel: segment i starts where i-1 ended?
+    for (int b0 = 1; b0 < p.nseg && !any_flag; b0 += kBatch) {
+        const int nb = min(kBatch, p.nseg - b0);
+#pragma unroll 4
+        for (int q = 0; q < nb; ++q) {
+            const int i = b0 + q;
+            const float st = p.ws_start[(base + i) * K + tid];
+            float diff = fabsf(p.ws_end[(base + i - 1) * K + tid] - st), mag = fabsf(st);
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) {
+                diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
+                mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
+            }
+            if (lane == 0) {
+                sDiff[warp][q] = diff;
+                sMag[warp][q] = mag;
+            }
+        }
+        __syncthreads();
+        if (tid < nb) {
+            float dmax = 0.f, mmax = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                dmax = fmaxf(dmax, sDiff[ww][tid]);
+                mmax = fmaxf(mmax, sMag[ww][tid]);
+            }
+            if (!(dmax <= kRelTol * mmax)) atomicMin(&first_bad, b0 + tid);
+        }
+        __syncthreads();
+        if (first_bad < p.nseg) break;
+    }
     const bool all_suspect = any_flag != 0;
-    float prev_end = p.ws_end[base * K + tid];
-    for (int i = 1; i < p.nseg; ++i) {
+    const int start = first_bad;
+    // ---- sequential walk from the first failing boundary (rare)
+    float prev_end = p.ws_end[(base + start - 1) * K + tid];
+    for (int i = start; i < p.nseg; ++i) {
         const float st = p.ws_start[(base + i) * K + tid];
         float diff = fabsf(prev_end - st), mag = fabsf(st);
 #pragma unroll
