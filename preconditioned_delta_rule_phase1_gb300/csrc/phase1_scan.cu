@@ -46,11 +46,13 @@ template <typename io_t, int K>
 struct Smem {
     static constexpr int NW = K / 32;
     io_t keys[NSTAGE][C][K];
-    float gb[NSTAGE][C], gr[NSTAGE][C];   // beta, r of the staged chunk
+    alignas(16) float gb[NSTAGE][C];      // beta of the staged chunk
+    alignas(16) float gr[NSTAGE][C];      // r of the staged chunk
     float wS[C][K + 4];                   // w = k^2 for the Gram fragments
-    float gpart[NW][C][C + 1];            // per-warp partial Gram
+    float gpart[NW][C][C + 4];            // per-warp partial Gram (16-byte aligned rows)
     float part[NW][2 * C];                // per-warp partial p (0..15) and n (16..31)
-    float sE[C], sR[C];
+    alignas(16) float sE[C];
+    alignas(16) float sR[C];
     float red[NW][2];
     int flag;
 };
@@ -212,26 +214,45 @@ __device__ void scan_range(const Params &p, Smem<io_t, K> &sm, int seq, int tb, 
                 pt += sm.part[ww][t];
                 nt_ += sm.part[ww][C + t];
             }
+            // row t of the Gram and the chunk's r, all loaded before the chains below
+            float g[C], rr[C];
+#pragma unroll
+            for (int u = 0; u < C; u += 4) {
+                float4 acc4 = *reinterpret_cast<const float4 *>(&sm.gpart[0][t][u]);
+#pragma unroll
+                for (int ww = 1; ww < NW; ++ww) {
+                    const float4 x = *reinterpret_cast<const float4 *>(&sm.gpart[ww][t][u]);
+                    acc4.x += x.x; acc4.y += x.y; acc4.z += x.z; acc4.w += x.w;
+                }
+                g[u] = acc4.x; g[u + 1] = acc4.y; g[u + 2] = acc4.z; g[u + 3] = acc4.w;
+                if (rseq) {
+                    const float4 r4 = *reinterpret_cast<const float4 *>(&sm.gr[s][u]);
+                    rr[u] = r4.x; rr[u + 1] = r4.y; rr[u + 2] = r4.z; rr[u + 3] = r4.w;
+                } else {
+                    rr[u] = rr[u + 1] = rr[u + 2] = rr[u + 3] = 1.0f;
+                }
+            }
             const float bt = sm.gb[s][t];
-            const float rt = rseq ? sm.gr[s][t] : 1.0f;
+            float rt = 1.0f, gtt = 0.0f;
+#pragma unroll
+            for (int u = 0; u < C; ++u) {
+                if (u == t) {
+                    rt = rr[u];
+                    gtt = g[u];
+                }
+            }
             const float ct = nt_ > 0.0f ? p.eta * bt / nt_ : 0.0f;
             // coupling row t: coef_u = c_t beta_t pi_ut G_tu (u < t); rho_t
             float coef[C];
             float pi = 1.0f;
 #pragma unroll
             for (int u = C - 1; u >= 0; --u) {
-                float gtu = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < NW; ++ww) gtu += sm.gpart[ww][t][u];
-                coef[u] = (u < t) ? ct * bt * pi * gtu : 0.0f;
-                if (u < t) pi *= (rseq ? sm.gr[s][u] : 1.0f);
+                coef[u] = (u < t) ? ct * bt * pi * g[u] : 0.0f;
+                if (u < t) pi *= rr[u];
             }
             const float rho = pi;  // prod_{v < t} r_v
             // can this token's one-step map expand?  ||A_t|| = max(|r|, |r - lambda|)
             {
-                float gtt = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < NW; ++ww) gtt += sm.gpart[ww][t][t];
                 const float lam = nt_ > 0.0f ? p.eta * bt * bt * gtt / nt_ : 0.0f;
                 const float nrm = fmaxf(fabsf(rt), fabsf(rt - lam));
                 if (lane < C && t < nv && nrm > 1.0f + 1e-6f) sm.flag = 1;
@@ -251,11 +272,21 @@ __device__ void scan_range(const Params &p, Smem<io_t, K> &sm, int seq, int tb, 
 
         // ---- 4. this column through the chunk; emit ktilde ----------------------
         const bool emit = t0 >= tseg;
+        // the chunk's e and r in registers first: the ktilde stores below go
+        // through a generic pointer and would otherwise order every later load
+        float eR[C], rR[C];
+#pragma unroll
+        for (int t = 0; t < C; t += 4) {
+            const float4 e4 = *reinterpret_cast<const float4 *>(&sm.sE[t]);
+            const float4 r4 = *reinterpret_cast<const float4 *>(&sm.sR[t]);
+            eR[t] = e4.x; eR[t + 1] = e4.y; eR[t + 2] = e4.z; eR[t + 3] = e4.w;
+            rR[t] = r4.x; rR[t + 1] = r4.y; rR[t + 2] = r4.z; rR[t + 3] = r4.w;
+        }
 #pragma unroll
         for (int t = 0; t < C; ++t) {
             if (t < nv) {
                 if (emit) from_f32(ktseq[(size_t)(t0 + t) * K + tid], d * kv[t]);
-                d = fmaf(sm.sR[t], d, sm.sE[t] * w[t]);
+                d = fmaf(rR[t], d, eR[t] * w[t]);
             }
         }
     }
