@@ -220,7 +220,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             uint64_t *last = &bar_full;   // completes once everything issued so far has
             const uint32_t aKQ = ptx::smem_u32(sKQ), aKt = ptx::smem_u32(sKt);
             const uint32_t aA = ptx::smem_u32(sA), aXb = ptx::smem_u32(sXb), aXg = ptx::smem_u32(sXg);
-            bool ok = wait_bar(&bar_full, 0, &s_abort, st);
+            bool ok = wait_poll(&bar_full, 0, &s_abort, st);
             if (ok) {  // [K;Q] Kt^T (M=128): Gram rows 0-63, scores rows 64-127
                 ptx::tc_fence_after();
                 const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
@@ -231,7 +231,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ptx::umma_commit(&bar_g);
                 last = &bar_g;
             }
-            ok = ok && wait_bar(&bar_x2, 0, &s_abort, st);
+            ok = ok && wait_poll(&bar_x2, 0, &s_abort, st);
             if (ok) {  // Kw = Xb diag(g) K;  W = (D Kt)^T Xb;  Ae = A Xb
                 ptx::tc_fence_after();
                 const uint32_t idk = ptx::idesc_bf16(64, K, 0, 1);
@@ -248,7 +248,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ptx::umma_commit(&bar_p1);
                 last = &bar_p1;
             }
-            ok = ok && wait_bar(&bar_x3, 0, &s_abort, st);
+            ok = ok && wait_poll(&bar_x3, 0, &s_abort, st);
             if (ok) {  // M' = (D Kt)^T Kw;  Qe' = A Kw  (Kw written over the K rows)
                 ptx::tc_fence_after();
                 const uint32_t idm = ptx::idesc_bf16(K, K, 1, 1);
@@ -302,7 +302,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
 
         // ---- Gram / scores: L (fp32) and A (bf16); then Kt <- D Kt
-        bool ok = vote_all(wait_bar(&bar_g, 0, &s_abort, st), 1, kPrepThreads);
+        bool ok = vote_all(wait_poll(&bar_g, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
             float g[32];
@@ -372,7 +372,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int krow = (K == 128) ? 32 * q4 + lane : mrow;
         const bool kact = (K == 128) || act;
         // ---- Kw (bf16 over the K rows), W and Ae (to the workspace)
-        if (ok) ok = vote_all(wait_bar(&bar_p1, 0, &s_abort, st), 1, kPrepThreads);
+        if (ok) ok = vote_all(wait_poll(&bar_p1, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
             {
@@ -398,8 +398,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ptx::bulk_commit_group();
             }
         }
-        // ---- M = -M' and Qe = diag(g) Q - Qe'
-        if (ok) ok = vote_all(wait_bar(&bar_p2, 0, &s_abort, st), 1, kPrepThreads);
+        // ---- M = -M' (stored as soon as it is staged), then Qe = diag(g) Q - Qe'
+        if (ok) ok = vote_all(wait_poll(&bar_p2, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
             {
@@ -410,21 +410,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int col = half * NH;
                 if (kact) st_row_sw128(mbox(krow >> 6, col >> 6), 64, krow & 63, col & 63, v, NH);
             }
-            const float gt = GATED ? __expf(sLg[mrow & 63]) : 1.0f;
-            {
-                float d[NH];
-                tmem_ldn<NH>(tmem + lane_off + cQe + half * NH, d);
-                if (act) {
-#pragma unroll
-                    for (int c = 0; c < NH; c += 16) {
-                        float qv[16];
-                        ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) qv[e] = fmaf(gt, qv[e], -d[c + e]);
-                        st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
-                    }
-                }
-            }
+            float d[NH];
+            tmem_ldn<NH>(tmem + lane_off + cQe + half * NH, d);
             ptx::fence_proxy_async_smem();
             ptx::named_bar(1, kPrepThreads);
             if (pt == 0) {
@@ -433,6 +420,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int cb = 0; cb < K / 64; ++cb)
                         ptx::tma_store_3d(&tm_m, mbox(rb, cb), cb * 64, krow0 + rb * 64, seq);
+                ptx::bulk_commit_group();
+            }
+            const float gt = GATED ? __expf(sLg[mrow & 63]) : 1.0f;
+            if (act) {
+#pragma unroll
+                for (int c = 0; c < NH; c += 16) {
+                    float qv[16];
+                    ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) qv[e] = fmaf(gt, qv[e], -d[c + e]);
+                    st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar(1, kPrepThreads);
+            if (pt == 0) {
 #pragma unroll
                 for (int cb = 0; cb < K / 64; ++cb)
                     ptx::tma_store_3d(&tm_qe, sKQ + cb * 16384 + 8192, cb * 64, t0, seq);
