@@ -136,7 +136,8 @@ int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
  * Bytes of workspace osdn_chunk_fwd needs for this shape (>= 256).  With
  * io == OSDN_BF16 the call prepares every chunk's operands before it runs the
  * state recurrence and keeps them in the workspace: about
- * B*H*ceil(T/64) * (2K^2 + 256K + 8196) bytes (72 KB a chunk at K = 128).
+ * B*H*ceil(T/64) * (2K^2 + 256K + 8196) bytes (72 KB a chunk at K = 128),
+ * plus 8*B*H*V*K bytes for the state carried between slabs of chunks.
  */
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V);
 
@@ -173,6 +174,11 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
  *   ST           out [B][H][V][K] fp32, or NULL (not written)
  * io == OSDN_BF16 runs on the tensor cores (bf16 operands, fp32
  * accumulation, state carried in fp32); io == OSDN_F32 runs in fp32 FFMA.
+ * For sequences longer than 16 chunks of 64 tokens the bf16 path overlaps
+ * the preparation of later chunks with the state recurrence of earlier ones
+ * on two library-owned streams per device (created on first use, forked from
+ * and joined back to `stream` with events); the library serialises the
+ * enqueue of such calls.
  * With T == 0 the call writes ST = S0 and nothing else.
  */
 int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, const void *k,

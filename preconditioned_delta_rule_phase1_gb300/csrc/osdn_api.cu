@@ -23,7 +23,7 @@ cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q
                               const void *kt, const void *v, const float *beta,
                               const float *alpha, const float *S0, void *o, float *ST,
                               cudaStream_t stream);
-size_t delta_tc_scratch_bytes(int BH, int T, int K);
+size_t delta_tc_scratch_bytes(int BH, int T, int K, int V);
 cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
@@ -94,7 +94,7 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return kStatusBytes;
     if (io != OSDN_BF16 || T == 0) return kStatusBytes;
     // the tensor-core path keeps each chunk's prepared operands in the workspace
-    return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K);
+    return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K, V);
 }
 
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {

@@ -37,7 +37,7 @@ constexpr int kPrepBlock = 288;      // + the control warp
 constexpr uint32_t kPrepCols = 256;  // TMEM columns
 
 struct PrepParams {
-    int T;
+    int T, nch, c0;   // sequence length, its chunks, first chunk of this launch
     const float *beta, *alpha;
     float *gc;
     int *status;
@@ -176,7 +176,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = blockIdx.x, seq = blockIdx.y, nch = gridDim.x;
+    const int j = p.c0 + blockIdx.x, seq = blockIdx.y, nch = p.nch;
     const int T = p.T, t0 = j * C;
     const int nvalid = min(C, T - t0);
     uint8_t *sKQ = smem + LY::oKQ, *sKt = smem + LY::oKt, *sA = smem + LY::oA;
@@ -452,8 +452,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 }
 
 template <int K, bool GATED>
-cudaError_t prep_launch_t(int BH, int T, const void *q, const void *k, const void *kt,
-                          const float *beta, const float *alpha, __nv_bfloat16 *w,
+cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const void *k,
+                          const void *kt, const float *beta, const float *alpha, __nv_bfloat16 *w,
                           __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
                           int *status, cudaStream_t stream) {
     const int nch = (T + C - 1) / C, Tp = nch * C;
@@ -472,29 +472,32 @@ cudaError_t prep_launch_t(int BH, int T, const void *q, const void *k, const voi
     }
     PrepParams p;
     p.T = T;
+    p.nch = nch;
+    p.c0 = c0;
     p.beta = beta;
     p.alpha = alpha;
     p.gc = gc;
     p.status = status;
-    dim3 grid(nch, BH);
+    dim3 grid(c1 - c0, BH);
     chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t chunk_prep_launch(int BH, int T, int K, const void *q, const void *k, const void *kt,
-                              const float *beta, const float *alpha, __nv_bfloat16 *w,
-                              __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
-                              int *status, cudaStream_t stream) {
+// Chunks [c0, c1) of every sequence.
+cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
+                              const void *kt, const float *beta, const float *alpha,
+                              __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe,
+                              __nv_bfloat16 *ae, float *gc, int *status, cudaStream_t stream) {
     if (K == 128) {
         if (alpha)
-            return prep_launch_t<128, true>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
-        return prep_launch_t<128, false>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+            return prep_launch_t<128, true>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<128, false>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
     }
     if (alpha)
-        return prep_launch_t<64, true>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
-    return prep_launch_t<64, false>(BH, T, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<64, true>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+    return prep_launch_t<64, false>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
 }
 
 }  // namespace tc

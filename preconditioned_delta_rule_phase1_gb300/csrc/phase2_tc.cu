@@ -32,15 +32,18 @@
 // their waits sit on the chain's critical path.
 // Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
 // status word and all roles leave their loops.
+#include <algorithm>
+#include <mutex>
+
 #include "tc_common.cuh"
 
 namespace osdn {
 namespace tc {
 
-cudaError_t chunk_prep_launch(int BH, int T, int K, const void *q, const void *k, const void *kt,
-                              const float *beta, const float *alpha, __nv_bfloat16 *w,
-                              __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
-                              int *status, cudaStream_t stream);
+cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
+                              const void *kt, const float *beta, const float *alpha,
+                              __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe,
+                              __nv_bfloat16 *ae, float *gc, int *status, cudaStream_t stream);
 
 namespace {
 
@@ -69,7 +72,7 @@ struct Lay {
 };
 
 struct Params {
-    int T, V, nch;
+    int T, V, nch, c0, ncs;   // sequence length, V, its chunks; this launch: chunks [c0, c0 + ncs)
     const float *S0, *gc;
     __nv_bfloat16 *o;
     float *ST;
@@ -102,7 +105,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;
     const int seq = blockIdx.y, v0 = blockIdx.x * BV;
-    const int T = p.T, nch = p.nch;
+    const int T = p.T, nch = p.nch, cbase = p.c0, ncs = p.ncs;
     auto stX = [&](int j) { return smem + LY::oX + (j % NS) * LY::kX; };
     auto stY = [&](int j) { return smem + LY::oY + (j % NS) * LY::kY; };
     // the bf16 copy of the state entering chunk c
@@ -145,8 +148,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::prefetch_tmap(&tm_qe);
             ptx::prefetch_tmap(&tm_v);
             int lastX = -1, lastY = -1;
-            for (int j = 0; j < nch; ++j) {
-                const int t0 = j * C, r0 = j * K;   // rows of this chunk in (Qe, Ae, V) and (W, M)
+            for (int j = 0; j < ncs; ++j) {
+                // rows of global chunk cbase + j in (Qe, Ae, V) and (W, M)
+                const int t0 = (cbase + j) * C, r0 = (cbase + j) * K;
                 if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st)) break;
                 uint8_t *x = stX(j);
                 ptx::mbar_arrive_expect_tx(&bars.fullX[j % NS], LY::kX);
@@ -183,7 +187,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         // ======================================================== state MMA issuer
         if (lane == 0) {
             const uint32_t id_s = ptx::idesc_bf16(K, BV, 0, 1);    // K-major A, MN-major B
-            for (int j = 0; j < nch; ++j) {
+            for (int j = 0; j < ncs; ++j) {
                 if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) ||
                     !wait_poll(&bars.s_ready, j & 1, &s_abort, st))
                     break;
@@ -211,7 +215,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         // ======================================================== output MMA issuer
         if (lane == 0) {
             const uint32_t id_o = ptx::idesc_bf16(64, BV, 0, 1);
-            for (int c = 0; c < nch; ++c) {
+            for (int c = 0; c < ncs; ++c) {
                 // O = [Ae | Qe] [V; S^T] of chunk c, behind chunk c's state product
                 if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st) ||
                     !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st) ||
@@ -240,7 +244,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         // ======================================================== O readout
         const int ot = tid - 96;
         const int trow = 16 * q4 + lane;   // M=64 accumulator: lanes 0-15 of each quarter
-        for (int j = 0; j < nch; ++j) {
+        for (int j = 0; j < ncs; ++j) {
             if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st), 3, 128)) break;
             ptx::tc_fence_after();
             float o[64];
@@ -248,7 +252,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::tc_fence_before();
             ptx::named_bar(3, 128);
             if (ot == 0) ptx::mbar_arrive(&bars.o_free[j & 1]);
-            const int t = j * C + trow;
+            const int t = (cbase + j) * C + trow;
             if (lane < 16 && t < T) st_global_bf16(p.o + ((size_t)seq * T + t) * p.V + v0, o, 64);
         }
     } else {
@@ -259,7 +263,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         const bool act = (K == 128) || lane < 16;
         const uint32_t tS = tmem + lane_off + kColS + c0;
         {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T
-            const float g0 = GATED ? p.gc[(size_t)seq * nch] : 1.0f;
+            const float g0 = GATED ? p.gc[(size_t)seq * nch + cbase] : 1.0f;
             float sv[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -279,9 +283,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::named_bar(1, 256);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
-        for (int j = 0; j < nch; ++j) {
-            const bool last = (j == nch - 1);
-            const float gN = (GATED && !last) ? p.gc[(size_t)seq * nch + j + 1] : 1.0f;
+        for (int j = 0; j < ncs; ++j) {
+            const bool last = (j == ncs - 1);
+            const float gN = (GATED && !last) ? p.gc[(size_t)seq * nch + cbase + j + 1] : 1.0f;
             // the copy entering chunk j+1 overwrites the one chunk j-2's output read
             const int n = j + 1;
             const bool okw = (last || n < NSB ||
@@ -322,11 +326,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Chunks [c0, c1) of every sequence, from the state S0 (NULL: zeros) to ST
+// (NULL: not written).
 template <int K, bool GATED>
-cudaError_t chain_launch_t(int BH, int T, int V, const void *v, const __nv_bfloat16 *w,
-                           const __nv_bfloat16 *m, const __nv_bfloat16 *qe,
-                           const __nv_bfloat16 *ae, const float *gc, const float *S0, void *o,
-                           float *ST, int *status, cudaStream_t stream) {
+cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
+                           const __nv_bfloat16 *w, const __nv_bfloat16 *m,
+                           const __nv_bfloat16 *qe, const __nv_bfloat16 *ae, const float *gc,
+                           const float *S0, void *o, float *ST, int *status, cudaStream_t stream) {
     const int nch = (T + C - 1) / C, Tp = nch * C;
     CUtensorMap mw, mm, mae, mqe, mv;
     if (!make_map(&mw, w, BH, nch * K, C) || !make_map(&mm, m, BH, nch * K, K) ||
@@ -345,6 +351,8 @@ cudaError_t chain_launch_t(int BH, int T, int V, const void *v, const __nv_bfloa
     p.T = T;
     p.V = V;
     p.nch = nch;
+    p.c0 = c0;
+    p.ncs = c1 - c0;
     p.S0 = S0;
     p.gc = gc;
     p.o = static_cast<__nv_bfloat16 *>(o);
@@ -355,23 +363,25 @@ cudaError_t chain_launch_t(int BH, int T, int V, const void *v, const __nv_bfloa
     return cudaGetLastError();
 }
 
-// Workspace carve-up of the prepared operands: W and M per chunk (K rows
-// each), Qe and Ae per token (chunk-padded), g_C per chunk.
+// Workspace carve-up: the prepared operands (W and M per chunk, K rows each;
+// Qe and Ae per token, chunk-padded; g_C per chunk) and two fp32 states
+// [BH][V][K] that carry S from one slab of chunks to the next.
 struct Carve {
     __nv_bfloat16 *w, *m, *qe, *ae;
-    float *gc;
+    float *gc, *state[2];
     size_t bytes;
 };
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-Carve carve(void *base, int BH, int T, int K) {
+Carve carve(void *base, int BH, int T, int K, int V) {
     const size_t nch = (size_t)(T + C - 1) / C, Tp = nch * C;
-    const size_t sz[5] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
+    const size_t sz[7] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
                           round256((size_t)BH * Tp * K * 2), round256((size_t)BH * Tp * C * 2),
-                          round256((size_t)BH * nch * 4)};
+                          round256((size_t)BH * nch * 4), round256((size_t)BH * V * K * 4),
+                          round256((size_t)BH * V * K * 4)};
     char *b = static_cast<char *>(base);
-    char *ptrs[5];
+    char *ptrs[7];
     size_t off = 0;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 7; ++i) {
         ptrs[i] = b ? b + off : nullptr;
         off += sz[i];
     }
@@ -381,8 +391,42 @@ Carve carve(void *base, int BH, int T, int K) {
     c.qe = reinterpret_cast<__nv_bfloat16 *>(ptrs[2]);
     c.ae = reinterpret_cast<__nv_bfloat16 *>(ptrs[3]);
     c.gc = reinterpret_cast<float *>(ptrs[4]);
+    c.state[0] = reinterpret_cast<float *>(ptrs[5]);
+    c.state[1] = reinterpret_cast<float *>(ptrs[6]);
     c.bytes = off;
     return c;
+}
+
+// Slabs of chunks: preparation of slab s+1 runs on the SMs the chain of slab
+// s leaves idle.  Two internal streams per device (the chain at the highest
+// priority, so its CTAs take SMs first) and a pool of events, set up once;
+// the enqueue is serialised so that concurrent calls do not share events.
+constexpr int kSlabChunks = 64;     // chunks per slab (at least)
+constexpr int kMaxSlabs = 64;
+struct Overlap {
+    cudaStream_t chain = nullptr, prep = nullptr;
+    cudaEvent_t ev[kMaxSlabs + 2] = {};
+    bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+Overlap g_overlap[kMaxDevices];
+std::mutex g_overlap_mu;
+
+cudaError_t overlap_for(int dev, Overlap **out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    Overlap &o = g_overlap[dev];
+    if (!o.ready) {
+        int least = 0, greatest = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&o.chain, cudaStreamNonBlocking, greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&o.prep, cudaStreamNonBlocking, least);
+        for (int i = 0; e == cudaSuccess && i < kMaxSlabs + 2; ++i)
+            e = cudaEventCreateWithFlags(&o.ev[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        o.ready = true;
+    }
+    *out = &o;
+    return cudaSuccess;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -413,27 +457,79 @@ bool make_map(CUtensorMap *m, const void *ptr, int BH, int rows, int width) {
 
 }  // namespace tc
 
-size_t delta_tc_scratch_bytes(int BH, int T, int K) {
-    return tc::carve(nullptr, BH, T, K).bytes;
+size_t delta_tc_scratch_bytes(int BH, int T, int K, int V) {
+    return tc::carve(nullptr, BH, T, K, V).bytes;
 }
+
+namespace {
+cudaError_t prep_range(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
+                       const void *kt, const float *beta, const float *alpha, const tc::Carve &w,
+                       int *status, cudaStream_t stream) {
+    return tc::chunk_prep_launch(BH, T, K, c0, c1, q, k, kt, beta, alpha, w.w, w.m, w.qe, w.ae, w.gc,
+                                 status, stream);
+}
+cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void *v, const float *alpha,
+                        const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
+                        cudaStream_t stream) {
+    if (K == 128) {
+        if (alpha)
+            return tc::chain_launch_t<128, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+        return tc::chain_launch_t<128, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+    }
+    if (alpha)
+        return tc::chain_launch_t<64, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+    return tc::chain_launch_t<64, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+}
+}  // namespace
 
 cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
                             cudaStream_t stream) {
     if (!tc::tensor_map_encoder_ready()) return cudaErrorNotSupported;
-    const tc::Carve w = tc::carve(scratch, BH, T, K);
-    cudaError_t e = tc::chunk_prep_launch(BH, T, K, q, k, kt, beta, alpha, w.w, w.m, w.qe, w.ae,
-                                          w.gc, status, stream);
-    if (e != cudaSuccess) return e;
-    if (K == 128) {
-        if (alpha)
-            return tc::chain_launch_t<128, true>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
-        return tc::chain_launch_t<128, false>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+    const tc::Carve w = tc::carve(scratch, BH, T, K, V);
+    const int nch = (T + tc::C - 1) / tc::C;
+    int per = tc::kSlabChunks;
+    while ((nch + per - 1) / per > tc::kMaxSlabs) per *= 2;
+    const int nslab = (nch + per - 1) / per;
+    if (nslab <= 1) {  // one slab: preparation, then the chain, on the caller's stream
+        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);
+        if (e != cudaSuccess) return e;
+        return chain_range(BH, T, K, V, 0, nch, v, alpha, w, S0, o, ST, status, stream);
     }
-    if (alpha)
-        return tc::chain_launch_t<64, true>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
-    return tc::chain_launch_t<64, false>(BH, T, V, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(tc::g_overlap_mu);
+    tc::Overlap *ov = nullptr;
+    if ((e = tc::overlap_for(dev, &ov)) != cudaSuccess) return e;
+    cudaEvent_t *ev = ov->ev;
+    // fork: both internal streams start after the caller's prior work
+    if ((e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ov->chain, ev[0], 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ov->prep, ev[0], 0)) != cudaSuccess) return e;
+    // slab 0 prepared ahead of the chain; slabs 1.. prepared behind it
+    if ((e = prep_range(BH, T, K, 0, per, q, k, kt, beta, alpha, w, status, ov->chain)) != cudaSuccess)
+        return e;
+    for (int s = 1; s < nslab; ++s) {
+        const int c0 = s * per, c1 = std::min(nch, c0 + per);
+        if ((e = prep_range(BH, T, K, c0, c1, q, k, kt, beta, alpha, w, status, ov->prep)) != cudaSuccess)
+            return e;
+        if ((e = cudaEventRecord(ev[1 + s], ov->prep)) != cudaSuccess) return e;
+    }
+    for (int s = 0; s < nslab; ++s) {
+        const int c0 = s * per, c1 = std::min(nch, c0 + per);
+        if (s >= 1 && (e = cudaStreamWaitEvent(ov->chain, ev[1 + s], 0)) != cudaSuccess) return e;
+        const float *sin = s == 0 ? S0 : w.state[(s - 1) & 1];
+        float *sout = s == nslab - 1 ? ST : w.state[s & 1];
+        if ((e = chain_range(BH, T, K, V, c0, c1, v, alpha, w, sin, o, sout, status, ov->chain)) !=
+            cudaSuccess)
+            return e;
+    }
+    // join: the caller's stream continues after the last chain slab (which
+    // itself waited for the last preparation slab)
+    if ((e = cudaEventRecord(ev[1], ov->chain)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(stream, ev[1], 0);
 }
 
 }  // namespace osdn
