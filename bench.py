@@ -408,6 +408,58 @@ def load_traffic(kernel, workload):
         return None
 
 
+def run_decode(args, local_rank):
+    """--decode: the recurrent step (osdn_decode_step) on a serving batch of
+    128 sequences x 16 heads at d_k = d_v = 128, bf16 I/O, fp32 state.  The
+    state (128 MB) exceeds L2, so every step streams it from HBM; one JSON
+    line, with the step's HBM roofline (8 V K bytes of state per head plus
+    the token's vectors)."""
+    from preconditioned_delta_rule_phase1_gb300 import ops
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    B, H, K, V = 128, 16, 128, 128
+    g = torch.Generator().manual_seed(0)
+    q = torch.nn.functional.normalize(torch.randn(B, H, K, generator=g), dim=-1).to(torch.bfloat16).to(dev)
+    k = torch.nn.functional.normalize(torch.randn(B, H, K, generator=g), dim=-1).to(torch.bfloat16).to(dev)
+    v = torch.randn(B, H, V, generator=g).to(torch.bfloat16).to(dev)
+    beta = torch.sigmoid(torch.randn(B, H, generator=g)).to(dev)
+    r = torch.sigmoid(torch.randn(B, H, generator=g) + 2).to(dev)
+    alpha = torch.exp(-0.1 * torch.nn.functional.softplus(torch.randn(B, H, generator=g))).to(dev)
+    d = torch.ones(B, H, K, device=dev)
+    S = (0.01 * torch.randn(B, H, V, K, generator=g)).to(dev)
+    o = torch.empty(B, H, V, dtype=torch.bfloat16, device=dev)
+    kt = torch.empty(B, H, K, dtype=torch.bfloat16, device=dev)
+    ws = ops.Workspace(device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: ops.decode_step(q, k, v, beta, d, S, r, 0.1, alpha, o, kt, ws, stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert ws.status(stream) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    BH = B * H
+    nbytes = BH * (8 * V * K + 8 * K + 2 * (2 * K + 2 * V) + 12)
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "OSDN decode step tokens/s (T=1, 128 sequences x 16 heads, d=128)",
+        "value": B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode_b128_h16_d128", "B": B, "H": H, "d_k": K, "d_v": V,
+                   "state": "fp32, 128 MB (larger than L2)"},
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "algorithmic_bytes": nbytes, "peak_source": peak_src},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,10 +468,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the recurrent decode step instead of the forward pass")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, world, local_rank = env_rank()
+    if args.decode:
+        run_decode(args, local_rank)
+        return
     if world > 1:
         torch.distributed.init_process_group("gloo")
     w = synth.WORKLOADS[args.workload]

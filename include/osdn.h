@@ -186,6 +186,30 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
                    const float *S0, void *o, float *ST, void *workspace, size_t workspace_bytes,
                    void *stream);
 
+/*
+ * One recurrent step (T = 1) of both phases, in place: the inference form of
+ * the method (section 1: constant-memory recurrent inference; section 2.2
+ * for the preconditioner step, section 2.1 for the state update).  For every
+ * sequence (b,h), with w = k (.) k and n = ||k||^2:
+ *     ktilde = d (.) k                               (d before the step)
+ *     d     <- r d + eta beta (1 - beta <d, w>) w / n   (r = 1 if r == NULL;
+ *                                                       the step is 0 if n = 0)
+ *     S     <- alpha S + beta (v - alpha S k) ktilde^T  (alpha = 1 if NULL)
+ *     o      = S q                                   (the updated state)
+ * The same arithmetic as osdn_precond_scan + osdn_chunk_fwd with T = 1.
+ *
+ *   q, k    in [B][H][K] io          v   in [B][H][V] io
+ *   beta    in [B][H] fp32;  r, alpha in [B][H] fp32 or NULL
+ *   d       in/out [B][H][K] fp32    S   in/out [B][H][V][K] fp32
+ *   o       out [B][H][V] io;  ktilde out [B][H][K] io, or NULL
+ * The workspace only carries the status word (>= 256 bytes).  Outputs must
+ * not overlap inputs or each other (OSDN_ERR_ALIAS).
+ */
+int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const void *k,
+                     const void *v, const float *beta, const float *r, float eta,
+                     const float *alpha, float *d, float *S, void *o, void *ktilde,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
 /* Zero the 256-byte status area at the start of a workspace (async). */
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 

@@ -28,6 +28,10 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
                             cudaStream_t stream);
+cudaError_t decode_step_launch(int io, int BH, int K, int V, const void *q, const void *k,
+                               const void *v, const float *beta, const float *r, float eta,
+                               const float *alpha, float *d, float *S, void *o, void *ktilde,
+                               cudaStream_t stream);
 }  // namespace osdn
 
 namespace {
@@ -203,6 +207,38 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
     else  // fp32 I/O: fp32 FFMA (tensor-core operand rounding would not meet fp32 accuracy)
         e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
                                     (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const void *k,
+                     const void *v, const float *beta, const float *r, float eta,
+                     const float *alpha, float *d, float *S, void *o, void *ktilde,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, 0) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (!workspace || workspace_bytes < kStatusBytes) return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (!q || !k || !v || !beta || !d || !S || !o) return OSDN_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(beta) || misaligned(r) ||
+        misaligned(alpha) || misaligned(d) || misaligned(S) || misaligned(o) ||
+        misaligned(ktilde) || misaligned(workspace))
+        return OSDN_ERR_ALIGN;
+    const size_t es = io_bytes(io);
+    const void *ins[6] = {q, k, v, beta, r, alpha};
+    const size_t insz[6] = {BH * K * es, BH * K * es, BH * V * es, BH * 4, BH * 4, BH * 4};
+    const void *outs[4] = {d, S, o, ktilde};
+    const size_t outsz[4] = {BH * K * 4, BH * V * K * 4, BH * V * es, BH * K * es};
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 6; ++i)
+            if (overlap(outs[a], outsz[a], ins[i], insz[i])) return OSDN_ERR_ALIAS;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], outsz[a], outs[b], outsz[b])) return OSDN_ERR_ALIAS;
+    }
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaError_t e = osdn::decode_step_launch(io, (int)BH, K, V, q, k, v, beta, r, eta, alpha, d, S,
+                                             o, ktilde, (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

@@ -34,6 +34,9 @@ _SIGS = {
                        [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_precond_scan_noalloc": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
                                   [ctypes.c_float] + [ctypes.c_void_p] * 4),
+    "osdn_decode_step": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5 +
+                         [ctypes.c_float] + [ctypes.c_void_p] * 6 +
+                         [ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 
@@ -195,3 +198,23 @@ def forward(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, worksp
     ktilde, dT = precond_scan(k, beta, r, eta, d0, workspace=ws, stream=stream)
     o, ST = chunk_fwd(q, k, ktilde, v, beta, alpha, S0, workspace=ws, stream=stream)
     return ktilde, dT, o, ST
+
+
+def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde=None,
+                workspace=None, stream=None):
+    """One recurrent step (osdn_decode_step): updates d [B,H,K] and S [B,H,V,K]
+    (fp32) in place for the token q, k [B,H,K], v [B,H,V] (io); returns
+    (o, ktilde)."""
+    B, H, K = k.shape
+    V = v.shape[-1]
+    io = _io(k)
+    if o is None:
+        o = torch.empty(B, H, V, dtype=k.dtype, device=k.device)
+    if ktilde is None:
+        ktilde = torch.empty(B, H, K, dtype=k.dtype, device=k.device)
+    ws = workspace or Workspace(device=k.device)
+    code = lib().osdn_decode_step(io, B, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(r),
+                                  float(eta), _ptr(alpha), _ptr(d), _ptr(S), _ptr(o),
+                                  _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream))
+    _check(code, "osdn_decode_step")
+    return o, ktilde

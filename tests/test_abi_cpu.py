@@ -110,3 +110,20 @@ def test_no_gpu_means_cuda_error_not_crash(L):
         pytest.skip("a GPU is present")
     assert scan(L) in (-6, -10)
     assert chunk(L) in (-6, -10)
+
+
+def decode(L, io=1, B=1, H=1, K=64, V=64, q=FAKE, k=2 * FAKE, v=3 * FAKE, beta=4 * FAKE, r=None,
+           alpha=None, d=5 * FAKE, S=6 * FAKE, o=7 * FAKE, kt=None, ws=8 * FAKE, wsb=256):
+    return L.osdn_decode_step(io, B, H, K, V, q, k, v, beta, r, 0.1, alpha, d, S, o, kt, ws, wsb,
+                              None)
+
+
+def test_host_validation_decode_step(L):
+    assert decode(L, io=3) == -3
+    assert decode(L, K=32) == -2 and decode(L, V=96) == -2 and decode(L, B=-1) == -2
+    assert decode(L, q=None) == -1 and decode(L, d=None) == -1 and decode(L, S=None) == -1
+    assert decode(L, ws=None) == -5 and decode(L, wsb=16) == -5
+    assert decode(L, k=2 * FAKE + 4) == -4
+    assert decode(L, o=FAKE) == -9          # o aliases q
+    assert decode(L, S=5 * FAKE) == -9      # S overlaps d
+    assert decode(L, H=0) == 0
