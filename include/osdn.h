@@ -121,7 +121,7 @@ int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const f
  * first call should be made before any stream capture.  The call allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  * Shapes whose speculative segments need more than 2 MiB of scratch (about
- * B*H*ceil(T/L)*8*K bytes, L the segment length of 512 or 1024 tokens, and
+ * B*H*ceil(T/L)*8*K bytes, L the segment length of 256 to 1024 tokens, and
  * none without a retention gate) return OSDN_ERR_SCRATCH before anything is
  * enqueued.  All calls share the array and it keeps the last call's
  * contents: calls whose kernels may overlap on the GPU (unordered streams)

@@ -15,11 +15,18 @@
 // so the 16 scalars e_t follow from one lower-triangular substitution,
 //     e_t = c_t (1 - beta_t rho_t p_t) - c_t beta_t sum_{u<t} pi_ut G_tu e_u,
 // after which every column of d steps through the chunk independently
-// (ktilde_t = d (.) k_t, d <- r_t d + e_t w_t).  The chain from one chunk to
-// the next is one K-wide reduction (p), the 16-step substitution and the
-// column updates.  G only enters through the small coupling c beta G, so it
-// is formed on the tensor cores (mma.sync, tf32 inputs, fp32 accumulation);
-// p and n, which enter e directly, are reduced in fp32.
+// (ktilde_t = d (.) k_t, d <- r_t d + e_t w_t).  G only enters through the
+// small coupling c beta G, so it is formed on the tensor cores (mma.sync,
+// tf32 inputs, fp32 accumulation); p and n, which enter e directly, are
+// reduced in fp32.
+//
+// One warp scans one stretch of one sequence: lane l owns the K/32
+// consecutive columns from l K/32 (its part of d stays in registers), so a
+// chunk needs no block barrier.  Per chunk the warp stages the keys in its
+// own shared-memory ring (cp.async, four chunks in flight), reduces p and n
+// by one transpose-reduce of 32 partial sums, forms G from the staged keys,
+// runs the substitution on lanes 0..15 and steps its columns with packed
+// fp32x2 arithmetic.
 //
 // Time segments.  With a retention gate the map d -> d_{t+1} contracts, so a
 // segment can start from a state estimated by running the scan over the W
@@ -38,23 +45,22 @@ namespace osdn {
 namespace p1 {
 
 constexpr int C = 16;          // tokens per chunk
-constexpr int NSTAGE = 4;      // key chunks in flight
+constexpr int NST = 4;         // key chunks in flight per warp
 constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment
+constexpr int kMaxWarps = 4;   // warps (segments) per CTA
+constexpr int kSmCount = 152;  // SMs the segment count is sized for (GB300)
 constexpr float kRelTol = 4.76837158203125e-07f;  // 2^-21
 
+// One warp's staging area.  Key rows are padded by 8 elements so that the
+// Gram fragment loads (rows g and g+8, two columns per lane) hit 32 banks.
 template <typename io_t, int K>
-struct Smem {
-    static constexpr int NW = K / 32;
-    io_t keys[NSTAGE][C][K];
-    alignas(16) float gb[NSTAGE][C];      // beta of the staged chunk
-    alignas(16) float gr[NSTAGE][C];      // r of the staged chunk
-    float wS[C][K + 4];                   // w = k^2 for the Gram fragments
-    float gpart[NW][C][C + 4];            // per-warp partial Gram (16-byte aligned rows)
-    float part[NW][2 * C];                // per-warp partial p (0..15) and n (16..31)
-    alignas(16) float sE[C];
-    alignas(16) float sR[C];
-    float red[NW][2];
-    int flag;
+struct WarpSmem {
+    static constexpr int KP = K + 8;
+    alignas(16) io_t keys[NST][C][KP];
+    alignas(16) float gb[NST][C];   // beta of the staged chunk
+    alignas(16) float gr[NST][C];   // r of the staged chunk
+    alignas(16) float sG[2][C][20]; // Gram (and n_t in column 16) of two chunks
+    alignas(16) float4 sER[C];      // (e_t, e_t, r_t, r_t)
 };
 
 struct Params {
@@ -86,11 +92,11 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// fp32 -> tf32 operand, rounded to nearest (ties away from zero): add half a
+// tf32 unit in the last place; the tensor core ignores the 13 low bits.  One
+// integer add instead of the conversion instruction's NaN handling; operands
+// here are squares of finite keys.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x) + 0x1000u; }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
@@ -100,321 +106,408 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Scan tokens [tb, te) of sequence `seq` starting from the state in `d`
-// (this thread's column); ktilde is written for tokens >= te_emit0.  Returns
-// the state after te in `d`.  Sets sm.flag if some token's one-step map
-// could expand.  All K threads of the CTA call this together.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 x) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 ld_pair(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ float2 ld_pair(const __nv_bfloat16 *p) {
+    return bf2_to_f2(*reinterpret_cast<const uint32_t *>(p));
+}
+
+// EP consecutive element pairs (a lane's columns) as fp32.
+template <int EP>
+__device__ __forceinline__ void ld_pairs(const float *p, float2 (&x)[EP]) {
+    if constexpr (EP == 2) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        x[0] = make_float2(v.x, v.y);
+        x[1] = make_float2(v.z, v.w);
+    } else {
+        x[0] = *reinterpret_cast<const float2 *>(p);
+    }
+}
+template <int EP>
+__device__ __forceinline__ void ld_pairs(const __nv_bfloat16 *p, float2 (&x)[EP]) {
+    if constexpr (EP == 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        x[0] = bf2_to_f2(u.x);
+        x[1] = bf2_to_f2(u.y);
+    } else {
+        x[0] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(p));
+    }
+}
+template <int EP>
+__device__ __forceinline__ void st_pairs(float *p, const float2 (&x)[EP]) {
+    if constexpr (EP == 2)
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+    else
+        *reinterpret_cast<float2 *>(p) = x[0];
+}
+template <int EP>
+__device__ __forceinline__ void st_pairs(__nv_bfloat16 *p, const float2 (&x)[EP]) {
+    if constexpr (EP == 2)
+        *reinterpret_cast<uint2 *>(p) = make_uint2(f2_to_bf2(x[0]), f2_to_bf2(x[1]));
+    else
+        *reinterpret_cast<uint32_t *>(p) = f2_to_bf2(x[0]);
+}
+
+// The half of a chunk's step that does not depend on d, formed while the
+// previous chunk runs its chain.
+//
+// Gram: G_tu = <w_t, w_u> on the tensor cores, and n_t = ||k_t||^2 summed
+// in fp32 from the same fragments.  The reduction index of k-step s8 visits
+// columns 8 s8 .. 8 s8 + 7 in the order that puts a lane's two A elements
+// next to each other (positions q and q + 4 are columns 8 s8 + 2q and
+// 8 s8 + 2q + 1); any order gives the same sum.  B = A^T, so its fragments
+// are A's.  Two accumulators per tile (even and odd k-steps) halve the mma
+// chain.  finish() leaves G in sG and n_t in column 16 of row t.
 template <typename io_t, int K>
-__device__ void scan_range(const Params &p, Smem<io_t, K> &sm, int seq, int tb, int tseg, int te,
-                           float &d) {
-    constexpr int NW = K / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+struct GramPass {
+    float acc[2][2][4];
+    float2 n0, n1;
+    __device__ __forceinline__ void start() {
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[a][b][i] = 0.f;
+        n0 = n1 = make_float2(0.f, 0.f);
+    }
+    __device__ __forceinline__ void step(const io_t (*kr)[K + 8], int g, int q, int s8) {
+        float2 x0 = ld_pair(&kr[g][8 * s8 + 2 * q]);
+        float2 x1 = ld_pair(&kr[g + 8][8 * s8 + 2 * q]);
+        x0 = __fmul2_rn(x0, x0);
+        x1 = __fmul2_rn(x1, x1);
+        n0 = __fadd2_rn(n0, x0);
+        n1 = __fadd2_rn(n1, x1);
+        const uint32_t a[4] = {to_tf32(x0.x), to_tf32(x1.x), to_tf32(x0.y), to_tf32(x1.y)};
+        mma_tf32(acc[s8 & 1][0], a, a[0], a[2]);
+        mma_tf32(acc[s8 & 1][1], a, a[1], a[3]);
+    }
+    __device__ __forceinline__ void finish(float (*sG)[20], int g, int q) {
+        float ng = n0.x + n0.y, ng8 = n1.x + n1.y;   // rows g and g + 8, this lane's columns
+        ng += __shfl_xor_sync(kFullMask, ng, 1);
+        ng8 += __shfl_xor_sync(kFullMask, ng8, 1);
+        ng += __shfl_xor_sync(kFullMask, ng, 2);
+        ng8 += __shfl_xor_sync(kFullMask, ng8, 2);
+        float gs[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gs[nt][i] = acc[0][nt][i] + acc[1][nt][i];
+        *reinterpret_cast<float2 *>(&sG[g][2 * q]) = make_float2(gs[0][0], gs[0][1]);
+        *reinterpret_cast<float2 *>(&sG[g][8 + 2 * q]) = make_float2(gs[1][0], gs[1][1]);
+        *reinterpret_cast<float2 *>(&sG[g + 8][2 * q]) = make_float2(gs[0][2], gs[0][3]);
+        *reinterpret_cast<float2 *>(&sG[g + 8][8 + 2 * q]) = make_float2(gs[1][2], gs[1][3]);
+        if (q == 0) {
+            sG[g][C] = ng;
+            sG[g + 8][C] = ng8;
+        }
+    }
+};
+
+// Coupling row of token t = lane & 15: coef_u = c_t beta_t pi_ut G_tu (u < t),
+// c_t, and c_t beta_t rho_t, so that on the chain
+//     e_t = c_t - c_t beta_t rho_t p_t - sum_u coef_u e_u.
+// Also flags a token whose one-step map could expand
+// (||A_t|| = max(|r_t|, |r_t - lambda_t|), lambda_t = eta beta_t^2 |w_t|^2 / n_t).
+// step(u) runs u = C-1 down to 0.
+template <bool HAS_R>
+struct CoefPass {
+    float coef[C];
+    float ct, cbr, rt;
+    float grow[C], rr[C], cb, pi;
+    __device__ __forceinline__ void start(const float *gb, const float *gr, const float (*sG)[20],
+                                          int t, int nv, float eta, bool &expand) {
+#pragma unroll
+        for (int u = 0; u < C; u += 4) {
+            const float4 g4 = *reinterpret_cast<const float4 *>(&sG[t][u]);
+            grow[u] = g4.x; grow[u + 1] = g4.y; grow[u + 2] = g4.z; grow[u + 3] = g4.w;
+            if (HAS_R) {
+                const float4 r4 = *reinterpret_cast<const float4 *>(&gr[u]);
+                rr[u] = r4.x; rr[u + 1] = r4.y; rr[u + 2] = r4.z; rr[u + 3] = r4.w;
+            }
+        }
+        const float nt = sG[t][C];
+        const float gtt = sG[t][t];
+        const float bt = gb[t];
+        rt = HAS_R ? gr[t] : 1.0f;
+        const float inv_n = nt > 0.0f ? __frcp_rn(nt) : 0.0f;
+        ct = eta * bt * inv_n;
+        cb = ct * bt;
+        pi = 1.0f;
+        const float lam = cb * gtt;
+        const float nrm = fmaxf(fabsf(rt), fabsf(rt - lam));
+        if (t < nv && nrm > 1.0f + 1e-6f) expand = true;
+    }
+    __device__ __forceinline__ void step(int t, int u) {
+        coef[u] = (u < t) ? cb * pi * grow[u] : 0.0f;
+        if (HAS_R && u < t) pi *= rr[u];
+    }
+    __device__ __forceinline__ void finish() { cbr = cb * pi; }
+};
+
+// Scan tokens [tb, te) of sequence `seq` with one warp, starting from this
+// lane's part of the state in `d`; ktilde is written for tokens >= tseg.
+// Returns the state after te in `d`; sets `expand` if some token's one-step
+// map could expand.  All 32 lanes call this together.
+//
+// Software-pipelined: while chunk j runs its chain (p from d, the 16-step
+// substitution, the column steps), the warp forms chunk j+1's Gram, n and
+// coupling rows, which do not depend on d.
+template <typename io_t, int K, bool HAS_R>
+__device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int tb, int tseg,
+                          int te, float2 (&d)[K / 64], bool &expand) {
+    constexpr int EP = K / 64;                      // element pairs per lane
+    constexpr int E = 2 * EP;                       // columns per lane
+    constexpr int EPP = 16 / (int)sizeof(io_t);     // elements per 16-byte piece
+    constexpr int PR = K / EPP;                     // pieces per key row
+    constexpr int KS = K / 8;                       // Gram k-steps
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;   // mma fragment coordinates
+    const int t = lane & (C - 1);            // the token this lane solves for
     const io_t *kseq = static_cast<const io_t *>(p.k) + (size_t)seq * p.T * K;
     io_t *ktseq = static_cast<io_t *>(p.ktilde) + (size_t)seq * p.T * K;
     const float *bseq = p.beta + (size_t)seq * p.T;
-    const float *rseq = p.r ? p.r + (size_t)seq * p.T : nullptr;
+    const float *rseq = HAS_R ? p.r + (size_t)seq * p.T : nullptr;
     const int nc = (te - tb + C - 1) / C;
 
     auto issue = [&](int j) {
         if (j < nc) {
-            const int s = j % NSTAGE, t0 = tb + j * C;
-            constexpr int PER_ROW = K * (int)sizeof(io_t) / 16;   // 16-byte pieces per key row
-            for (int i = tid; i < C * PER_ROW; i += K) {
-                const int t = i / PER_ROW, pc = i % PER_ROW;
-                const bool valid = t0 + t < te;
-                const io_t *src = valid ? kseq + (size_t)(t0 + t) * K + pc * (16 / sizeof(io_t)) : kseq;
-                cp_async16(&sm.keys[s][t][pc * (16 / sizeof(io_t))], src, valid);
+            const int s = j % NST, t0 = tb + j * C;
+#pragma unroll
+            for (int i = lane; i < C * PR; i += 32) {
+                const int tt = i / PR, pc = i % PR;
+                const bool valid = t0 + tt < te;
+                const io_t *src = valid ? kseq + (size_t)(t0 + tt) * K + pc * EPP : kseq;
+                cp_async16(&st.keys[s][tt][pc * EPP], src, valid);
             }
-            if (tid < C) {
-                const bool valid = t0 + tid < te;
-                cp_async4(&sm.gb[s][tid], valid ? bseq + t0 + tid : bseq, valid);
-            } else if (tid < 2 * C && rseq) {
-                const int t = tid - C;
-                const bool valid = t0 + t < te;
-                cp_async4(&sm.gr[s][t], valid ? rseq + t0 + t : rseq, valid);
-            }
+            // lanes 0..15 fetch beta, lanes 16..31 r (when there is one)
+            const bool valid = t0 + t < te && (HAS_R || lane < C);
+            const float *src = lane < C ? bseq : rseq;
+            float *dst = lane < C ? &st.gb[s][t] : &st.gr[s][t];
+            cp_async4(dst, valid ? src + t0 + t : bseq, valid);
         }
         cp_commit();
     };
 #pragma unroll
-    for (int j = 0; j < NSTAGE - 1; ++j) issue(j);
+    for (int j = 0; j < NST - 1; ++j) issue(j);
+
+    GramPass<io_t, K> gp;
+    CoefPass<HAS_R> cf;
+    // chunk 0's input-only half
+    cp_wait<NST - 2>();
+    __syncwarp();
+    gp.start();
+#pragma unroll
+    for (int s8 = 0; s8 < KS; ++s8) gp.step(st.keys[0], g, q, s8);
+    gp.finish(st.sG[0], g, q);
+    __syncwarp();
+    cf.start(st.gb[0], st.gr[0], st.sG[0], t, min(C, te - tb), p.eta, expand);
+#pragma unroll
+    for (int u = C - 1; u >= 0; --u) cf.step(t, u);
+    cf.finish();
 
     for (int j = 0; j < nc; ++j) {
-        issue(j + NSTAGE - 1);
-        cp_wait<NSTAGE - 1>();
-        __syncthreads();
-        const int s = j % NSTAGE, t0 = tb + j * C;
+        issue(j + NST - 1);
+        cp_wait<NST - 2>();   // chunks j and j+1 have landed
+        __syncwarp();
+        const int s = j % NST, s1 = (j + 1) % NST, t0 = tb + j * C;
         const int nv = min(C, te - t0);
+        // chunk j+1's stage may be empty past the end; its results are then unused
+        const io_t(*kr1)[K + 8] = st.keys[s1];
 
-        // ---- 1. this column of the chunk; p and n partials ---------------------
-        float kv[C], w[C];
+        // ---- chain: this lane's columns, w = k^2, partial p --------------------
+        float2 kk[C][EP], w[C][EP];
+        float v[C];
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
-            kv[t] = to_f32(sm.keys[s][t][tid]);
-            w[t] = kv[t] * kv[t];
-            sm.wS[t][tid] = w[t];
-        }
-        {
-            // transpose-reduce 32 partials across the warp: lane l ends with index l
-            float v[2 * C];
+        for (int u = 0; u < C; ++u) {
+            ld_pairs<EP>(&st.keys[s][u][E * lane], kk[u]);
+            float2 pp = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                v[t] = d * w[t];
-                v[C + t] = w[t];
+            for (int e = 0; e < EP; ++e) {
+                w[u][e] = __fmul2_rn(kk[u][e], kk[u][e]);
+                pp = __ffma2_rn(d[e], w[u][e], pp);
             }
-#pragma unroll
-            for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
-                const bool hi = (lane & off) != 0;
-#pragma unroll
-                for (int i = 0; i < n; ++i) {
-                    const float keep = hi ? v[i + n] : v[i];
-                    const float send = hi ? v[i] : v[i + n];
-                    v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
-                }
-            }
-            sm.part[warp][lane] = v[0];
+            v[u] = pp.x + pp.y;
         }
-        __syncthreads();
 
-        // ---- 2. partial Gram of this warp's 32 key columns (tensor cores) -------
-        {
-            const int g = lane >> 2, tq = lane & 3;
-            float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        // ---- off the chain: chunk j+1's Gram and n ------------------------------
+        gp.start();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const int k0 = warp * 32 + ks * 8;
-                uint32_t a[4];
-                a[0] = to_tf32(sm.wS[g][k0 + tq]);
-                a[1] = to_tf32(sm.wS[g + 8][k0 + tq]);
-                a[2] = to_tf32(sm.wS[g][k0 + tq + 4]);
-                a[3] = to_tf32(sm.wS[g + 8][k0 + tq + 4]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b0 = to_tf32(sm.wS[8 * nt + g][k0 + tq]);
-                    const uint32_t b1 = to_tf32(sm.wS[8 * nt + g][k0 + tq + 4]);
-                    mma_tf32(acc[nt], a, b0, b1);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sm.gpart[warp][g][8 * nt + 2 * tq] = acc[nt][0];
-                sm.gpart[warp][g][8 * nt + 2 * tq + 1] = acc[nt][1];
-                sm.gpart[warp][g + 8][8 * nt + 2 * tq] = acc[nt][2];
-                sm.gpart[warp][g + 8][8 * nt + 2 * tq + 1] = acc[nt][3];
-            }
-        }
-        __syncthreads();
+        for (int s8 = 0; s8 < KS; ++s8) gp.step(kr1, g, q, s8);
+        gp.finish(st.sG[(j + 1) & 1], g, q);
 
-        // ---- 3. the 16 coefficients e_t (warp 0, lane t) -------------------------
-        if (warp == 0) {
-            const int t = lane & (C - 1);
-            float pt = 0.f, nt_ = 0.f;
+        // ---- chain: reduce p; lanes 2t and 2t+1 end with p_t --------------------
 #pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
-                pt += sm.part[ww][t];
-                nt_ += sm.part[ww][C + t];
-            }
-            // row t of the Gram and the chunk's r, all loaded before the chains below
-            float g[C], rr[C];
+        for (int off = 16, n = 8; off >= 2; off >>= 1, n >>= 1) {
+            const bool hi = (lane & off) != 0;
 #pragma unroll
-            for (int u = 0; u < C; u += 4) {
-                float4 acc4 = *reinterpret_cast<const float4 *>(&sm.gpart[0][t][u]);
-#pragma unroll
-                for (int ww = 1; ww < NW; ++ww) {
-                    const float4 x = *reinterpret_cast<const float4 *>(&sm.gpart[ww][t][u]);
-                    acc4.x += x.x; acc4.y += x.y; acc4.z += x.z; acc4.w += x.w;
-                }
-                g[u] = acc4.x; g[u + 1] = acc4.y; g[u + 2] = acc4.z; g[u + 3] = acc4.w;
-                if (rseq) {
-                    const float4 r4 = *reinterpret_cast<const float4 *>(&sm.gr[s][u]);
-                    rr[u] = r4.x; rr[u + 1] = r4.y; rr[u + 2] = r4.z; rr[u + 3] = r4.w;
-                } else {
-                    rr[u] = rr[u + 1] = rr[u + 2] = rr[u + 3] = 1.0f;
-                }
-            }
-            const float bt = sm.gb[s][t];
-            float rt = 1.0f, gtt = 0.0f;
-#pragma unroll
-            for (int u = 0; u < C; ++u) {
-                if (u == t) {
-                    rt = rr[u];
-                    gtt = g[u];
-                }
-            }
-            const float ct = nt_ > 0.0f ? p.eta * bt / nt_ : 0.0f;
-            // coupling row t: coef_u = c_t beta_t pi_ut G_tu (u < t); rho_t
-            float coef[C];
-            float pi = 1.0f;
-#pragma unroll
-            for (int u = C - 1; u >= 0; --u) {
-                coef[u] = (u < t) ? ct * bt * pi * g[u] : 0.0f;
-                if (u < t) pi *= rr[u];
-            }
-            const float rho = pi;  // prod_{v < t} r_v
-            // can this token's one-step map expand?  ||A_t|| = max(|r|, |r - lambda|)
-            {
-                const float lam = nt_ > 0.0f ? p.eta * bt * bt * gtt / nt_ : 0.0f;
-                const float nrm = fmaxf(fabsf(rt), fabsf(rt - lam));
-                if (lane < C && t < nv && nrm > 1.0f + 1e-6f) sm.flag = 1;
-            }
-            float acc = ct * (1.0f - bt * rho * pt);
-#pragma unroll
-            for (int u = 0; u < C; ++u) {
-                const float eu = __shfl_sync(kFullMask, acc, u);
-                if (t > u) acc = fmaf(-coef[u], eu, acc);
-            }
-            if (lane < C) {
-                sm.sE[t] = t < nv ? acc : 0.0f;
-                sm.sR[t] = rt;
+            for (int i = 0; i < n; ++i) {
+                const float keep = hi ? v[i + n] : v[i];
+                const float send = hi ? v[i] : v[i + n];
+                v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
             }
         }
-        __syncthreads();
+        v[0] += __shfl_xor_sync(kFullMask, v[0], 1);
+        const float pt = __shfl_sync(kFullMask, v[0], 2 * t);
 
-        // ---- 4. this column through the chunk; emit ktilde ----------------------
-        const bool emit = t0 >= tseg;
-        // the chunk's e and r in registers first: the ktilde stores below go
-        // through a generic pointer and would otherwise order every later load
-        float eR[C], rR[C];
+        // ---- chain: the 16-step substitution for e_t ----------------------------
+        float acc = cf.ct - cf.cbr * pt;
 #pragma unroll
-        for (int t = 0; t < C; t += 4) {
-            const float4 e4 = *reinterpret_cast<const float4 *>(&sm.sE[t]);
-            const float4 r4 = *reinterpret_cast<const float4 *>(&sm.sR[t]);
-            eR[t] = e4.x; eR[t + 1] = e4.y; eR[t + 2] = e4.z; eR[t + 3] = e4.w;
-            rR[t] = r4.x; rR[t + 1] = r4.y; rR[t + 2] = r4.z; rR[t + 3] = r4.w;
+        for (int u = 0; u < C - 1; ++u) acc = fmaf(-cf.coef[u], __shfl_sync(kFullMask, acc, u), acc);
+        if (lane < C) {
+            const float et = t < nv ? acc : 0.0f, rt = t < nv ? cf.rt : 1.0f;
+            st.sER[t] = make_float4(et, et, rt, rt);
         }
+        __syncwarp();
+
+        // ---- chain: this lane's columns through the chunk; emit ktilde ----------
+        const int nst = t0 >= tseg ? nv : 0;   // tokens of this chunk to emit
+        io_t *kst = ktseq + (size_t)t0 * K + E * lane;
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
-            if (t < nv) {
-                if (emit) from_f32(ktseq[(size_t)(t0 + t) * K + tid], d * kv[t]);
-                d = fmaf(rR[t], d, eR[t] * w[t]);
+        for (int u = 0; u < C; ++u) {
+            const float4 er = st.sER[u];
+            float2 kt[EP];
+#pragma unroll
+            for (int e = 0; e < EP; ++e) kt[e] = __fmul2_rn(d[e], kk[u][e]);
+            if (u < nst) st_pairs<EP>(kst + u * K, kt);
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                const float2 rd = HAS_R ? __fmul2_rn(make_float2(er.z, er.w), d[e]) : d[e];
+                d[e] = __ffma2_rn(make_float2(er.x, er.y), w[u][e], rd);
             }
         }
+
+        // ---- off the chain: chunk j+1's coupling rows ---------------------------
+        cf.start(st.gb[s1], st.gr[s1], st.sG[(j + 1) & 1], t, min(C, te - t0 - C), p.eta, expand);
+#pragma unroll
+        for (int u = C - 1; u >= 0; --u) cf.step(t, u);
+        cf.finish();
     }
     cp_wait<0>();
-    __syncthreads();
+    __syncwarp();
 }
 
-// Grid (nseg, BH): segment `seg` of sequence `seq`.
-template <typename io_t, int K>
-__global__ void __launch_bounds__(K) precond_segment_kernel(Params p) {
+// One warp per (segment, sequence): warp id = segment + nseg * sequence.
+template <typename io_t, int K, bool HAS_R>
+__global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Smem<io_t, K> &sm = *reinterpret_cast<Smem<io_t, K> *>(smem_raw);
-    const int seg = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
-    if (tid == 0) sm.flag = 0;
+    constexpr int EP = K / 64, E = 2 * EP;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int id = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (id >= p.BH * p.nseg) return;
+    WarpSmem<io_t, K> &st = reinterpret_cast<WarpSmem<io_t, K> *>(smem_raw)[warp];
+    const int seq = id / p.nseg, seg = id % p.nseg;
     const int tseg = seg * p.L;
     const int te = min(p.T, tseg + p.L);
-    float d;
+    float2 d[EP];
     int tb;
     if (seg == 0) {
-        d = p.d0 ? p.d0[(size_t)seq * K + tid] : 1.0f;
+        if (p.d0) {
+            ld_pairs<EP>(p.d0 + (size_t)seq * K + E * lane, d);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EP; ++e) d[e] = make_float2(1.0f, 1.0f);
+        }
         tb = 0;
     } else {
-        d = 0.0f;  // speculative: the warm-up forgets this guess
+#pragma unroll
+        for (int e = 0; e < EP; ++e) d[e] = make_float2(0.0f, 0.0f);   // the warm-up forgets this
         tb = tseg - kWarm;
     }
-    __syncthreads();
-    if (seg > 0) {
-        scan_range<io_t, K>(p, sm, seq, tb, tseg, tseg, d);  // warm-up, nothing emitted
-    }
-    if (p.nseg > 1) p.ws_start[((size_t)seq * p.nseg + seg) * K + tid] = d;
-    scan_range<io_t, K>(p, sm, seq, tseg, tseg, te, d);
+    bool expand = false;
+    if (seg > 0) warp_scan<io_t, K, HAS_R>(p, st, seq, tb, tseg, tseg, d, expand);
+    const size_t slot = (size_t)seq * p.nseg + seg;
+    if (p.nseg > 1) st_pairs<EP>(p.ws_start + slot * K + E * lane, d);
+    warp_scan<io_t, K, HAS_R>(p, st, seq, tseg, tseg, te, d, expand);
+    expand = __any_sync(kFullMask, expand);
     if (p.nseg > 1) {
-        p.ws_end[((size_t)seq * p.nseg + seg) * K + tid] = d;
-        if (tid == 0) p.ws_flag[(size_t)seq * p.nseg + seg] = sm.flag;
+        st_pairs<EP>(p.ws_end + slot * K + E * lane, d);
+        if (lane == 0) p.ws_flag[slot] = expand ? 1 : 0;
     } else if (p.dT) {
-        p.dT[(size_t)seq * K + tid] = d;
+        st_pairs<EP>(p.dT + (size_t)seq * K + E * lane, d);
     }
 }
 
-// Grid (BH): verify every speculative segment start against its predecessor's
-// end; recompute (exactly) the segments that do not match; write d_T.
-// Without a repair every boundary check is independent (the predecessor's
-// end is then exact), so all boundaries are checked at once first; the
-// sequential check-and-repair walk starts at the first boundary that fails.
-template <typename io_t, int K>
-__global__ void __launch_bounds__(K) precond_verify_kernel(Params p) {
+// Largest |a_i - b_i| and |b_i| over a K-vector held as this lane's pairs.
+template <int EP>
+__device__ __forceinline__ void warp_diff(const float2 (&a)[EP], const float2 (&b)[EP], float &diff,
+                                          float &mag) {
+    diff = 0.f;
+    mag = 0.f;
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+        diff = fmaxf(diff, fmaxf(fabsf(a[e].x - b[e].x), fabsf(a[e].y - b[e].y)));
+        mag = fmaxf(mag, fmaxf(fabsf(b[e].x), fabsf(b[e].y)));
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
+        mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
+    }
+}
+
+// Grid (BH), kMaxWarps warps: verify every speculative segment start against
+// its predecessor's end; recompute (exactly) the segments that do not match;
+// write d_T.  Without a repair every boundary check is independent (the
+// predecessor's end is then exact), so the warps check all boundaries at
+// once; warp 0 then walks sequentially from the first one that fails.
+template <typename io_t, int K, bool HAS_R>
+__global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Smem<io_t, K> &sm = *reinterpret_cast<Smem<io_t, K> *>(smem_raw);
-    constexpr int NW = K / 32;
-    constexpr int kBatch = 64;   // boundaries checked per pass
-    const int seq = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int EP = K / 64, E = 2 * EP;
+    WarpSmem<io_t, K> &st = *reinterpret_cast<WarpSmem<io_t, K> *>(smem_raw);
+    const int seq = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
     const size_t base = (size_t)seq * p.nseg;
-    __shared__ int any_flag, first_bad;
-    __shared__ float sDiff[NW][kBatch], sMag[NW][kBatch];
-    if (tid == 0) {
-        int f = 0;
-        for (int i = 0; i < p.nseg; ++i) f |= p.ws_flag[base + i];
-        any_flag = f;
-        first_bad = f ? 1 : p.nseg;
-        sm.flag = 0;
+    __shared__ int first_bad;
+    int f = 0;
+    for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) f |= p.ws_flag[base + i];
+    const bool all_suspect = __syncthreads_or(f) != 0;
+    if (threadIdx.x == 0) first_bad = all_suspect ? 1 : p.nseg;
+    __syncthreads();
+    if (!all_suspect) {
+        for (int i = 1 + warp; i < p.nseg; i += nw) {
+            float2 prev[EP], cur[EP];
+            ld_pairs<EP>(p.ws_end + (base + i - 1) * K + E * lane, prev);
+            ld_pairs<EP>(p.ws_start + (base + i) * K + E * lane, cur);
+            float diff, mag;
+            warp_diff<EP>(prev, cur, diff, mag);
+            if (lane == 0 && !(diff <= kRelTol * mag)) atomicMin(&first_bad, i);
+        }
     }
     __syncthreads();
-    // ---- all boundaries in parallel: segment i starts where i-1 ended?
-    for (int b0 = 1; b0 < p.nseg && !any_flag; b0 += kBatch) {
-        const int nb = min(kBatch, p.nseg - b0);
-#pragma unroll 4
-        for (int q = 0; q < nb; ++q) {
-            const int i = b0 + q;
-            const float st = p.ws_start[(base + i) * K + tid];
-            float diff = fabsf(p.ws_end[(base + i - 1) * K + tid] - st), mag = fabsf(st);
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) {
-                diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
-                mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
-            }
-            if (lane == 0) {
-                sDiff[warp][q] = diff;
-                sMag[warp][q] = mag;
-            }
-        }
-        __syncthreads();
-        if (tid < nb) {
-            float dmax = 0.f, mmax = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
-                dmax = fmaxf(dmax, sDiff[ww][tid]);
-                mmax = fmaxf(mmax, sMag[ww][tid]);
-            }
-            if (!(dmax <= kRelTol * mmax)) atomicMin(&first_bad, b0 + tid);
-        }
-        __syncthreads();
-        if (first_bad < p.nseg) break;
-    }
-    const bool all_suspect = any_flag != 0;
+    if (warp != 0) return;   // the walk below is warp 0's alone
     const int start = first_bad;
-    // ---- sequential walk from the first failing boundary (rare)
-    float prev_end = p.ws_end[(base + start - 1) * K + tid];
+    float2 prev_end[EP];
+    ld_pairs<EP>(p.ws_end + (base + start - 1) * K + E * lane, prev_end);
     for (int i = start; i < p.nseg; ++i) {
-        const float st = p.ws_start[(base + i) * K + tid];
-        float diff = fabsf(prev_end - st), mag = fabsf(st);
+        float2 cur[EP];
+        ld_pairs<EP>(p.ws_start + (base + i) * K + E * lane, cur);
+        float diff, mag;
+        warp_diff<EP>(prev_end, cur, diff, mag);
+        const bool ok = !all_suspect && diff <= kRelTol * mag;
+        float2 dd[EP];
+        if (ok) {
+            ld_pairs<EP>(p.ws_end + (base + i) * K + E * lane, dd);
+        } else {   // recompute segment i from the exact end of segment i-1
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
-            mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
-        }
-        if (lane == 0) {
-            sm.red[warp][0] = diff;
-            sm.red[warp][1] = mag;
-        }
-        __syncthreads();
-        float dmax = 0.f, mmax = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < NW; ++ww) {
-            dmax = fmaxf(dmax, sm.red[ww][0]);
-            mmax = fmaxf(mmax, sm.red[ww][1]);
-        }
-        __syncthreads();
-        const bool ok = !all_suspect && dmax <= kRelTol * mmax;
-        float d = p.ws_end[(base + i) * K + tid];
-        if (!ok) {  // recompute segment i from the exact end of segment i-1
-            d = prev_end;
+            for (int e = 0; e < EP; ++e) dd[e] = prev_end[e];
             const int tseg = i * p.L, te = min(p.T, tseg + p.L);
-            scan_range<io_t, K>(p, sm, seq, tseg, tseg, te, d);
-            p.ws_end[(base + i) * K + tid] = d;
+            bool unused = false;
+            warp_scan<io_t, K, HAS_R>(p, st, seq, tseg, tseg, te, dd, unused);
+            st_pairs<EP>(p.ws_end + (base + i) * K + E * lane, dd);
         }
-        prev_end = d;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) prev_end[e] = dd[e];
     }
-    if (p.dT) p.dT[(size_t)seq * K + tid] = prev_end;
+    if (p.dT) st_pairs<EP>(p.dT + (size_t)seq * K + E * lane, prev_end);
 }
 
 // T == 0: the final preconditioner is the initial one.
@@ -425,37 +518,51 @@ __global__ void copy_or_fill_kernel(size_t n, const float *__restrict__ src, flo
         dst[i] = src ? src[i] : fill;
 }
 
-template <typename io_t, int K>
-static cudaError_t launch(const Params &p, cudaStream_t stream) {
-    const int smem = (int)sizeof(Smem<io_t, K>);
+template <typename io_t, int K, bool HAS_R>
+static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
+    constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K, HAS_R>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMaxWarps * kStage);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K, HAS_R>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kStage);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    precond_segment_kernel<io_t, K><<<dim3(p.nseg, p.BH), K, smem, stream>>>(p);
+    // few segments: one per CTA, so that they spread over the SMs
+    const long long nwarps = (long long)p.BH * p.nseg;
+    const int wpc = nwarps >= 2LL * kSmCount ? kMaxWarps : 1;
+    const unsigned grid = (unsigned)((nwarps + wpc - 1) / wpc);
+    precond_segment_kernel<io_t, K, HAS_R><<<grid, 32 * wpc, wpc * kStage, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nseg == 1) return e;
-    precond_verify_kernel<io_t, K><<<p.BH, K, smem, stream>>>(p);
+    precond_verify_kernel<io_t, K, HAS_R><<<p.BH, 32 * kMaxWarps, kStage, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <typename io_t, int K>
+static cudaError_t launch(const Params &p, cudaStream_t stream) {
+    return p.r ? launch_t<io_t, K, true>(p, stream) : launch_t<io_t, K, false>(p, stream);
 }
 
 }  // namespace p1
 
-// Segment length: long enough that the warm-up costs little extra reading,
-// short enough to give the GPU a few waves of CTAs.  Only a retention gate
-// (r != NULL) makes the warm-up converge, so without one there is a single
-// segment per sequence.
+// Segment length: each segment is one warp, and about 8 of them are resident
+// per SM (two CTAs of four), so segments are halved from 1024 tokens while
+// all of them still fit in that one wave: more warps hide more latency, a
+// second wave costs a whole segment time, and below 256 tokens the 128-token
+// warm-up would double the work.  Only a retention gate (r != NULL) makes the
+// warm-up converge, so without one there is a single segment per sequence.
 int precond_segments(int BH, int T, bool has_r, int *L_out) {
     int L = T;
     if (has_r && T > 2 * p1::kWarm) {
         L = 1024;
-        if ((long long)BH * ((T + L - 1) / L) < 4LL * 152) L = 512;
+        while (L > 2 * p1::kWarm &&
+               (long long)BH * ((T + L / 2 - 1) / (L / 2)) <= 8LL * p1::kSmCount)
+            L >>= 1;
         if (L >= T) L = T;
     }
     if (L < 1) L = 1;

@@ -135,7 +135,8 @@ def test_alias_rejected_before_launch():
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("case", ["converging", "slow_retention", "expansive_token", "short_tail"])
+@pytest.mark.parametrize("case", ["converging", "slow_retention", "expansive_token", "expansive_step",
+                                  "short_tail"])
 def test_segmented_scan_exact(io, case):
     """The time-segmented scan (used when a retention gate is given) equals the
     token recurrence whether the speculative segment starts verify or must be
@@ -146,6 +147,11 @@ def test_segmented_scan_exact(io, case):
         x["r"] = torch.full_like(x["r"], 0.99995)
     if case == "expansive_token":     # one map with ||A_t|| > 1: all segments recomputed
         x["r"][:, :, 1700] = 1.5
+    if case == "expansive_step":      # |r_t - eta beta_t^2 |w_t|^2 / n_t| > 1 at one token
+        x["eta"] = 2.5
+        x["k"][:, :, 1700] = 0.0
+        x["k"][:, :, 1700, 5] = 1.0
+        x["beta"][:, :, 1700] = 1.0
     g = to_cuda(x)
     ws = ops.Workspace()
     kt, dT = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], workspace=ws)
