@@ -12,7 +12,8 @@ and marshals numpy arrays in and out.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts the
 pages and the mathematics fix (DeltaNet special case, definitional
-hypergradient surrogate, residual-ratio identity, dense unrolled product,
+hypergradient surrogate, residual-ratio identity and its per-sequence log sum,
+dense unrolled product,
 gated Newton condition, one-hot closed form, eta = 0 decay, state chaining).
 """
 from __future__ import annotations
@@ -55,7 +56,7 @@ def _load():
         lib = ctypes.CDLL(path)
         lib.oracle_precond_scan.restype = ctypes.c_int
         lib.oracle_precond_scan.argtypes = [ctypes.c_int] * 4 + [_dp, _dp, _dp, ctypes.c_double,
-                                                                 _dp, _dp, _dp, ctypes.c_int]
+                                                                 _dp, _dp, _dp, _dp, ctypes.c_int]
         lib.oracle_delta_fwd.restype = ctypes.c_int
         lib.oracle_delta_fwd.argtypes = [ctypes.c_int] * 5 + [_dp] * 9 + [ctypes.c_int]
         _lib = lib
@@ -81,10 +82,13 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_dp)
 
 
-def precond_scan(k, beta, r=None, eta=0.1, d0=None, nthreads=None):
+def precond_scan(k, beta, r=None, eta=0.1, d0=None, nthreads=None, log_ratio=False):
     """Phase 1: ktilde [B,H,T,K] and d_T [B,H,K] from k [B,H,T,K], beta [B,H,T].
 
     r [B,H,T] (None: r = 1) and d0 [B,H,K] (None: d0 = 1) are optional.
+    With log_ratio=True also returns [B,H]: sum_t log((1 - beta_t <d_t, k_t^2>)^2),
+    the log of the product of the token residual ratios f_t(S_t)/f_t(S_{t-1})
+    (theorem 5.2; exp of it over T is the geometric-mean ratio q_geo).
     """
     k = _f64(k)
     B, H, T, K = k.shape
@@ -94,12 +98,13 @@ def precond_scan(k, beta, r=None, eta=0.1, d0=None, nthreads=None):
     assert d0 is None or d0.shape == (B, H, K)
     kt = np.empty_like(k)
     dT = np.empty((B, H, K))
+    lr = np.empty((B, H)) if log_ratio else None
     rc = _load().oracle_precond_scan(B, H, T, K, _ptr(k), _ptr(beta), _ptr(r), float(eta),
-                                     _ptr(d0), _ptr(kt), _ptr(dT),
+                                     _ptr(d0), _ptr(kt), _ptr(dT), _ptr(lr),
                                      int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_precond_scan failed (%d)" % rc)
-    return kt, dT
+    return (kt, dT, lr) if log_ratio else (kt, dT)
 
 
 def delta_fwd(q, k, ktilde, v, beta, alpha=None, S0=None, nthreads=None):

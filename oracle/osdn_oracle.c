@@ -16,6 +16,9 @@
  *         ktilde_t = d_t (.) k_t
  *   h_t(d) = ((1 - beta_t <d, k_t^2>)^2 - 1) / (2 ||k_t||^2)   (section 2.2)
  *   d_{t+1} = r_t d_t  (-)  eta grad_d h_t(d_t)                (section 2.3)
+ *   f_t(S_t) / f_t(S_{t-1}) = (1 - beta_t <d_t, k_t^2>)^2      (section 3,
+ *         theorem 5.2: the token-local residual ratio; its geometric mean
+ *         over a sequence is the q_geo diagnostic of section 4.2)
  *
  * Readings taken where the pages are silent or garbled:
  *  - the APF step is taken as DESCENT on h (d <- r d - eta grad h); the pages
@@ -38,6 +41,7 @@
  *   beta, r, alpha : [B][H][T]       d0, dT : [B][H][K]
  *   S0, ST : [B][H][V][K]  (S[i][j]: i = value row, j = key column)
  */
+#include <math.h>
 #include <pthread.h>
 #include <stddef.h>
 #include <stdlib.h>
@@ -48,8 +52,10 @@
 /* ---------------------------------------------------------------------- */
 static void phase1_sequence(int T, int K, const double *k, const double *beta,
                             const double *r, double eta, const double *d0,
-                            double *ktilde, double *dT, double *d /* K scratch */)
+                            double *ktilde, double *dT, double *logratio,
+                            double *d /* K scratch */)
 {
+    double lr = 0.0;
     for (int j = 0; j < K; ++j) d[j] = d0 ? d0[j] : 1.0;
     for (int t = 0; t < T; ++t) {
         const double *kt = k + (size_t)t * K;
@@ -63,6 +69,13 @@ static void phase1_sequence(int T, int K, const double *k, const double *beta,
             n += w;
             a += d[j] * w;
         }
+        /* residual ratio of this token's state write (theorem 5.2):
+         * S_t k_t - v_t = (S_{t-1} k_t - v_t)(1 - beta_t <ktilde_t, k_t>) and
+         * <ktilde_t, k_t> = <d_t, k_t^2> */
+        {
+            double y = 1.0 - bt * a;
+            lr += log(y * y);
+        }
         /* preconditioned key with the preconditioner before this step */
         for (int j = 0; j < K; ++j) ktilde[(size_t)t * K + j] = d[j] * kt[j];
         /* d <- r d - eta * grad_d h_t(d),
@@ -75,6 +88,7 @@ static void phase1_sequence(int T, int K, const double *k, const double *beta,
     }
     if (dT)
         for (int j = 0; j < K; ++j) dT[j] = d[j];
+    if (logratio) *logratio = lr;
 }
 
 /* ---------------------------------------------------------------------- */
@@ -126,7 +140,7 @@ typedef struct {
     int T, K, V;
     const double *q, *k, *ktilde_in, *v, *beta, *r, *alpha, *d0, *S0;
     double eta;
-    double *ktilde, *dT, *o, *ST;
+    double *ktilde, *dT, *o, *ST, *logratio;
     int failed;
 } job_t;
 
@@ -144,7 +158,8 @@ static void *run_job(void *arg)
             phase1_sequence(jb->T, jb->K, jb->k + s * T * K, jb->beta + s * T,
                             jb->r ? jb->r + s * T : NULL, jb->eta,
                             jb->d0 ? jb->d0 + s * K : NULL, jb->ktilde + s * T * K,
-                            jb->dT ? jb->dT + s * K : NULL, scratch);
+                            jb->dT ? jb->dT + s * K : NULL,
+                            jb->logratio ? jb->logratio + s : NULL, scratch);
         } else {
             phase2_sequence(jb->T, jb->K, jb->V, jb->q + s * T * K, jb->k + s * T * K,
                             jb->ktilde_in + s * T * K, jb->v + s * T * V, jb->beta + s * T,
@@ -191,14 +206,17 @@ static int run_threads(job_t *proto, int nseq, int nthreads)
     return rc;
 }
 
-/* Phase 1 over B*H sequences.  r, d0, dT may be NULL (r = 1, d0 = 1). */
+/* Phase 1 over B*H sequences.  r, d0, dT, logratio may be NULL (r = 1,
+ * d0 = 1).  logratio[b*H + h] = sum_t log((1 - beta_t <d_t, k_t^2>)^2), the
+ * log of the product of the sequence's token residual ratios. */
 int oracle_precond_scan(int B, int H, int T, int K, const double *k, const double *beta,
                         const double *r, double eta, const double *d0, double *ktilde,
-                        double *dT, int nthreads)
+                        double *dT, double *logratio, int nthreads)
 {
     if (B < 1 || H < 1 || T < 0 || K < 1 || !k || !beta || !ktilde) return -1;
     if (T == 0) {
         for (size_t i = 0; dT && i < (size_t)B * H * K; ++i) dT[i] = d0 ? d0[i] : 1.0;
+        for (size_t i = 0; logratio && i < (size_t)B * H; ++i) logratio[i] = 0.0;
         return 0;
     }
     job_t p;
@@ -213,6 +231,7 @@ int oracle_precond_scan(int B, int H, int T, int K, const double *k, const doubl
     p.d0 = d0;
     p.ktilde = ktilde;
     p.dT = dT;
+    p.logratio = logratio;
     return run_threads(&p, B * H, nthreads);
 }
 

@@ -100,6 +100,42 @@ def test_pin_b_c_surrogate_and_ratio(gated):
 
 
 # ---------------------------------------------------------------------------
+# q_geo: the log of the product of the residual ratios, from the states
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("gated", [False, True])
+def test_pin_log_ratio_from_states(gated):
+    """Phase 1's per-sequence sum of log((1 - beta_t <d_t, k_t^2>)^2) equals the
+    sum of log(f_t(S_t) / f_t(S_before)) measured on the Phase 2 states
+    (theorem 5.2's token-local ratios; S_before = alpha_t S_{t-1} when gated)."""
+    x = rand_case(T=30, K=6, V=5, apf=True, gated=gated, s0=True, seed=12)
+    eta = 0.3
+    total = 0.0
+    for t, (d, S_prev, S_new, kt, o) in enumerate(step_states(x, eta)):
+        k, v = x["k"][0, 0, t], x["v"][0, 0, t]
+        al = x["alpha"][0, 0, t] if gated else 1.0
+        total += np.log(f_loss(S_new, k, v) / f_loss(al * S_prev, k, v))
+    sl = lambda a: None if a is None else a[:1, :1]
+    _, _, lr = oracle.precond_scan(sl(x["k"]), sl(x["beta"]), sl(x["r"]), eta, None,
+                                   log_ratio=True)
+    assert lr.shape == (1, 1)
+    assert abs(lr[0, 0] - total) <= 1e-9 * max(1.0, abs(total))
+
+
+def test_pin_log_ratio_plain_deltanet_closed_form():
+    """With d = 1 fixed (eta = 0, r = 1) the ratio of token t is
+    (1 - beta_t ||k_t||^2)^2, the plain delta rule's contraction factor."""
+    x = rand_case(B=2, H=3, T=50, K=8, V=4, seed=13)
+    _, _, lr = oracle.precond_scan(x["k"], x["beta"], None, 0.0, None, log_ratio=True)
+    n = np.sum(x["k"] ** 2, axis=-1)
+    want = np.sum(np.log((1.0 - x["beta"] * n) ** 2), axis=-1)
+    assert np.allclose(lr, want, rtol=1e-12, atol=1e-12)
+    # an empty sequence has an empty product
+    _, _, lr0 = oracle.precond_scan(x["k"][:, :, :0], x["beta"][:, :, :0], None, 0.1, None,
+                                    log_ratio=True)
+    assert np.array_equal(lr0, np.zeros((2, 3)))
+
+
+# ---------------------------------------------------------------------------
 # (d) dense unrolled product for T <= 16
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("gated,s0", [(False, False), (True, True)])
