@@ -107,6 +107,30 @@ int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const f
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Phase 1 with the residual diagnostic.  Computes exactly what
+ * osdn_precond_scan computes and, per sequence,
+ *
+ *     log_ratio[b][h] = sum_t log((1 - beta_t <d_t, k_t^2>)^2)
+ *
+ * the log of the product of the token-local residual ratios
+ * f_t(S_t) / f_t(S_{t-1}) with f_t(S) = 1/2 ||S k_t - v_t||^2 (gist.science
+ * summary of arXiv 2605.13473, section 3, theorem 5.2): writing
+ * ktilde_t = d_t (.) k_t into the state scales the token's residual by
+ * 1 - beta_t <ktilde_t, k_t>.  exp(log_ratio / T) is the geometric-mean
+ * residual ratio q_geo of section 4.2.  With a decay alpha in Phase 2 the
+ * ratio is taken against the decayed state alpha_t S_{t-1}.  A token whose
+ * factor is exactly zero makes the sum -inf; T == 0 gives 0.
+ *
+ *   log_ratio out [B][H] fp32, 16-byte aligned, must not overlap the other
+ *             arguments; the rest as for osdn_precond_scan (same workspace
+ *             size).  NULL log_ratio: OSDN_ERR_NULL.
+ */
+int osdn_precond_scan_residual(int io, int B, int H, int T, int K, const void *k,
+                               const float *beta, const float *r, float eta, const float *d0,
+                               void *ktilde, float *dT, float *log_ratio, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
  * Phase 1 without a workspace, for callers that cannot allocate device
  * memory: code running where cudaMalloc is off limits (inside a region being
  * captured under a memory pool that forbids new allocations, a plugin whose

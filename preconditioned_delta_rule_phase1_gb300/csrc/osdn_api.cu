@@ -9,7 +9,8 @@
 namespace osdn {
 cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
                                 const float *r, float eta, const float *d0, void *ktilde,
-                                float *dT, void *scratch, int *status, cudaStream_t stream);
+                                float *dT, float *logratio, void *scratch, int *status,
+                                cudaStream_t stream);
 size_t precond_scratch_bytes(int BH, int T, int K);
 size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r);
 size_t precond_noalloc_capacity();
@@ -119,9 +120,14 @@ int osdn_check_status(const void *workspace, void *stream) {
     return code;
 }
 
-int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const float *beta,
-                      const float *r, float eta, const float *d0, void *ktilde, float *dT,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// osdn_precond_scan and osdn_precond_scan_residual: one validation, one launch.
+int precond_scan_checked(int io, int B, int H, int T, int K, const void *k, const float *beta,
+                         const float *r, float eta, const float *d0, void *ktilde, float *dT,
+                         float *log_ratio, void *workspace, size_t workspace_bytes, void *stream) {
     if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
     if (!dims_ok(B, H, T) || !width_ok(K)) return OSDN_ERR_DIMS;
     if (!workspace) return OSDN_ERR_WORKSPACE;
@@ -130,19 +136,40 @@ int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const f
     if (BH == 0) return OSDN_OK;
     if (T > 0 && (!k || !beta || !ktilde)) return OSDN_ERR_NULL;
     if (misaligned(k) || misaligned(beta) || misaligned(r) || misaligned(d0) ||
-        misaligned(ktilde) || misaligned(dT) || misaligned(workspace))
+        misaligned(ktilde) || misaligned(dT) || misaligned(log_ratio) || misaligned(workspace))
         return OSDN_ERR_ALIGN;
     const size_t kbytes = BH * (size_t)T * K * io_bytes(io);
     if (overlap(k, kbytes, ktilde, kbytes) || overlap(dT, BH * K * 4, ktilde, kbytes) ||
-        overlap(dT, BH * K * 4, k, kbytes))
+        overlap(dT, BH * K * 4, k, kbytes) || overlap(log_ratio, BH * 4, k, kbytes) ||
+        overlap(log_ratio, BH * 4, ktilde, kbytes) || overlap(log_ratio, BH * 4, dT, BH * K * 4))
         return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     void *scratch = static_cast<char *>(workspace) + kStatusBytes;
     cudaError_t e = osdn::precond_scan_launch(io, (int)BH, T, K, k, beta, r, eta, d0, ktilde, dT,
-                                              scratch, static_cast<int *>(workspace),
+                                              log_ratio, scratch, static_cast<int *>(workspace),
                                               (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osdn_precond_scan(int io, int B, int H, int T, int K, const void *k, const float *beta,
+                      const float *r, float eta, const float *d0, void *ktilde, float *dT,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    return precond_scan_checked(io, B, H, T, K, k, beta, r, eta, d0, ktilde, dT, nullptr,
+                                workspace, workspace_bytes, stream);
+}
+
+int osdn_precond_scan_residual(int io, int B, int H, int T, int K, const void *k,
+                               const float *beta, const float *r, float eta, const float *d0,
+                               void *ktilde, float *dT, float *log_ratio, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    if (!log_ratio) return OSDN_ERR_NULL;
+    return precond_scan_checked(io, B, H, T, K, k, beta, r, eta, d0, ktilde, dT, log_ratio,
+                                workspace, workspace_bytes, stream);
 }
 
 int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,

@@ -37,6 +37,13 @@
 // segments after a token whose one-step map could expand (||A_t||_2 > 1).
 // The result is therefore the exact recurrence to fp32 rounding on every
 // input; speculation only decides how much runs in parallel.
+//
+// Residual diagnostic (optional).  Writing ktilde_t into the state scales
+// the token's residual S k_t - v_t by 1 - beta_t <d_t, w_t> (section 3,
+// theorem 5.2: f_t(S_t) / f_t(S_{t-1}) = (1 - beta_t <d_t, w_t>)^2), and the
+// substitution above already forms that factor.  On request each sequence
+// also gets sum_t log((1 - beta_t <d_t, w_t>)^2); its exp over T is the
+// geometric-mean residual ratio q_geo of section 4.2.
 #include <mutex>
 
 #include "osdn_device.cuh"
@@ -72,6 +79,8 @@ struct Params {
     float *dT;
     float *ws_start, *ws_end;   // [BH][nseg][K]
     int *ws_flag;               // [BH][nseg]
+    float *ws_lr;               // [BH][nseg] residual log-ratio of each segment
+    float *logratio;            // [BH] residual log-ratio of each sequence, or NULL
     int *status;
 };
 
@@ -114,6 +123,11 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float2 x) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 __device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
+    return x;
+}
 __device__ __forceinline__ float2 ld_pair(const float *p) { return *reinterpret_cast<const float2 *>(p); }
 __device__ __forceinline__ float2 ld_pair(const __nv_bfloat16 *p) {
     return bf2_to_f2(*reinterpret_cast<const uint32_t *>(p));
@@ -216,12 +230,14 @@ struct GramPass {
 //     e_t = c_t - c_t beta_t rho_t p_t - sum_u coef_u e_u.
 // Also flags a token whose one-step map could expand
 // (||A_t|| = max(|r_t|, |r_t - lambda_t|), lambda_t = eta beta_t^2 |w_t|^2 / n_t).
-// step(u) runs u = C-1 down to 0.
-template <bool HAS_R>
+// step(u) runs u = C-1 down to 0.  With LR it also keeps the same row
+// without the factor c_t (coefy, by), for the residual factor
+//     y_t = 1 - beta_t <d_t, w_t> = 1 - beta_t rho_t p_t - sum_u coefy_u e_u.
+template <bool HAS_R, bool LR>
 struct CoefPass {
-    float coef[C];
-    float ct, cbr, rt;
-    float grow[C], rr[C], cb, pi;
+    float coef[C], coefy[LR ? C : 1];
+    float ct, cbr, by, rt;
+    float grow[C], rr[C], cb, bt, pi;
     __device__ __forceinline__ void start(const float *gb, const float *gr, const float (*sG)[20],
                                           int t, int nv, float eta, bool &expand) {
 #pragma unroll
@@ -235,7 +251,7 @@ struct CoefPass {
         }
         const float nt = sG[t][C];
         const float gtt = sG[t][t];
-        const float bt = gb[t];
+        bt = gb[t];
         rt = HAS_R ? gr[t] : 1.0f;
         const float inv_n = nt > 0.0f ? __frcp_rn(nt) : 0.0f;
         ct = eta * bt * inv_n;
@@ -247,9 +263,13 @@ struct CoefPass {
     }
     __device__ __forceinline__ void step(int t, int u) {
         coef[u] = (u < t) ? cb * pi * grow[u] : 0.0f;
+        if (LR) coefy[u] = (u < t) ? bt * pi * grow[u] : 0.0f;
         if (HAS_R && u < t) pi *= rr[u];
     }
-    __device__ __forceinline__ void finish() { cbr = cb * pi; }
+    __device__ __forceinline__ void finish() {
+        cbr = cb * pi;
+        by = bt * pi;
+    }
 };
 
 // Scan tokens [tb, te) of sequence `seq` with one warp, starting from this
@@ -260,9 +280,11 @@ struct CoefPass {
 // Software-pipelined: while chunk j runs its chain (p from d, the 16-step
 // substitution, the column steps), the warp forms chunk j+1's Gram, n and
 // coupling rows, which do not depend on d.
-template <typename io_t, int K, bool HAS_R>
+//
+// With LR, lanes 0..15 add log(y_t^2) of every token >= tseg to `lr`.
+template <typename io_t, int K, bool HAS_R, bool LR>
 __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int tb, int tseg,
-                          int te, float2 (&d)[K / 64], bool &expand) {
+                          int te, float2 (&d)[K / 64], bool &expand, float &lr) {
     constexpr int EP = K / 64;                      // element pairs per lane
     constexpr int E = 2 * EP;                       // columns per lane
     constexpr int EPP = 16 / (int)sizeof(io_t);     // elements per 16-byte piece
@@ -299,7 +321,7 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
     for (int j = 0; j < NST - 1; ++j) issue(j);
 
     GramPass<io_t, K> gp;
-    CoefPass<HAS_R> cf;
+    CoefPass<HAS_R, LR> cf;
     // chunk 0's input-only half
     cp_wait<NST - 2>();
     __syncwarp();
@@ -359,8 +381,14 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
 
         // ---- chain: the 16-step substitution for e_t ----------------------------
         float acc = cf.ct - cf.cbr * pt;
+        float accy = 1.0f - cf.by * pt;
 #pragma unroll
-        for (int u = 0; u < C - 1; ++u) acc = fmaf(-cf.coef[u], __shfl_sync(kFullMask, acc, u), acc);
+        for (int u = 0; u < C - 1; ++u) {
+            const float eu = __shfl_sync(kFullMask, acc, u);
+            acc = fmaf(-cf.coef[u], eu, acc);
+            if (LR) accy = fmaf(-cf.coefy[u], eu, accy);
+        }
+        if (LR && lane < C && t < nv && t0 + t >= tseg) lr += logf(accy * accy);
         if (lane < C) {
             const float et = t < nv ? acc : 0.0f, rt = t < nv ? cf.rt : 1.0f;
             st.sER[t] = make_float4(et, et, rt, rt);
@@ -395,7 +423,7 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
 }
 
 // One warp per (segment, sequence): warp id = segment + nseg * sequence.
-template <typename io_t, int K, bool HAS_R>
+template <typename io_t, int K, bool HAS_R, bool LR>
 __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     constexpr int EP = K / 64, E = 2 * EP;
@@ -422,16 +450,20 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params 
         tb = tseg - kWarm;
     }
     bool expand = false;
-    if (seg > 0) warp_scan<io_t, K, HAS_R>(p, st, seq, tb, tseg, tseg, d, expand);
+    float lr = 0.0f;   // warm-up tokens (< tseg) add nothing
+    if (seg > 0) warp_scan<io_t, K, HAS_R, LR>(p, st, seq, tb, tseg, tseg, d, expand, lr);
     const size_t slot = (size_t)seq * p.nseg + seg;
     if (p.nseg > 1) st_pairs<EP>(p.ws_start + slot * K + E * lane, d);
-    warp_scan<io_t, K, HAS_R>(p, st, seq, tseg, tseg, te, d, expand);
+    warp_scan<io_t, K, HAS_R, LR>(p, st, seq, tseg, tseg, te, d, expand, lr);
     expand = __any_sync(kFullMask, expand);
+    if (LR) lr = warp_sum(lr);
     if (p.nseg > 1) {
         st_pairs<EP>(p.ws_end + slot * K + E * lane, d);
         if (lane == 0) p.ws_flag[slot] = expand ? 1 : 0;
-    } else if (p.dT) {
-        st_pairs<EP>(p.dT + (size_t)seq * K + E * lane, d);
+        if (LR && lane == 0) p.ws_lr[slot] = lr;
+    } else {
+        if (p.dT) st_pairs<EP>(p.dT + (size_t)seq * K + E * lane, d);
+        if (LR && lane == 0) p.logratio[seq] = lr;
     }
 }
 
@@ -458,7 +490,7 @@ __device__ __forceinline__ void warp_diff(const float2 (&a)[EP], const float2 (&
 // write d_T.  Without a repair every boundary check is independent (the
 // predecessor's end is then exact), so the warps check all boundaries at
 // once; warp 0 then walks sequentially from the first one that fails.
-template <typename io_t, int K, bool HAS_R>
+template <typename io_t, int K, bool HAS_R, bool LR>
 __global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     constexpr int EP = K / 64, E = 2 * EP;
@@ -501,13 +533,25 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p
             for (int e = 0; e < EP; ++e) dd[e] = prev_end[e];
             const int tseg = i * p.L, te = min(p.T, tseg + p.L);
             bool unused = false;
-            warp_scan<io_t, K, HAS_R>(p, st, seq, tseg, tseg, te, dd, unused);
+            float lr = 0.0f;
+            warp_scan<io_t, K, HAS_R, LR>(p, st, seq, tseg, tseg, te, dd, unused, lr);
             st_pairs<EP>(p.ws_end + (base + i) * K + E * lane, dd);
+            if (LR) {
+                lr = warp_sum(lr);
+                if (lane == 0) p.ws_lr[base + i] = lr;
+            }
         }
 #pragma unroll
         for (int e = 0; e < EP; ++e) prev_end[e] = dd[e];
     }
     if (p.dT) st_pairs<EP>(p.dT + (size_t)seq * K + E * lane, prev_end);
+    if (LR) {   // the segments' sums, in segment order within each lane
+        __syncwarp();
+        float lr = 0.0f;
+        for (int i = lane; i < p.nseg; i += 32) lr += p.ws_lr[base + i];
+        lr = warp_sum(lr);
+        if (lane == 0) p.logratio[seq] = lr;
+    }
 }
 
 // T == 0: the final preconditioner is the initial one.
@@ -518,16 +562,16 @@ __global__ void copy_or_fill_kernel(size_t n, const float *__restrict__ src, flo
         dst[i] = src ? src[i] : fill;
 }
 
-template <typename io_t, int K, bool HAS_R>
+template <typename io_t, int K, bool HAS_R, bool LR>
 static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K, HAS_R>,
+        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K, HAS_R, LR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kMaxWarps * kStage);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K, HAS_R>,
+            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K, HAS_R, LR>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kStage);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -536,16 +580,18 @@ static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     const long long nwarps = (long long)p.BH * p.nseg;
     const int wpc = nwarps >= 2LL * kSmCount ? kMaxWarps : 1;
     const unsigned grid = (unsigned)((nwarps + wpc - 1) / wpc);
-    precond_segment_kernel<io_t, K, HAS_R><<<grid, 32 * wpc, wpc * kStage, stream>>>(p);
+    precond_segment_kernel<io_t, K, HAS_R, LR><<<grid, 32 * wpc, wpc * kStage, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nseg == 1) return e;
-    precond_verify_kernel<io_t, K, HAS_R><<<p.BH, 32 * kMaxWarps, kStage, stream>>>(p);
+    precond_verify_kernel<io_t, K, HAS_R, LR><<<p.BH, 32 * kMaxWarps, kStage, stream>>>(p);
     return cudaGetLastError();
 }
 
 template <typename io_t, int K>
 static cudaError_t launch(const Params &p, cudaStream_t stream) {
-    return p.r ? launch_t<io_t, K, true>(p, stream) : launch_t<io_t, K, false>(p, stream);
+    if (p.logratio)
+        return p.r ? launch_t<io_t, K, true, true>(p, stream) : launch_t<io_t, K, false, true>(p, stream);
+    return p.r ? launch_t<io_t, K, true, false>(p, stream) : launch_t<io_t, K, false, false>(p, stream);
 }
 
 }  // namespace p1
@@ -570,18 +616,31 @@ int precond_segments(int BH, int T, bool has_r, int *L_out) {
     return (T + L - 1) / L;
 }
 
+// Scratch of the segmented scan: segment starts and ends [n][K] fp32, then
+// the flags [n] int and the residual sums [n] fp32, each padded to 256 bytes
+// (n = BH * nseg).
+static size_t segment_scratch_bytes(size_t n, int K) {
+    return n * K * 4 * 2 + 2 * (((n * 4 + 255) / 256) * 256);
+}
+
 size_t precond_scratch_bytes(int BH, int T, int K) {
     int L;
     const int nseg = precond_segments(BH, T, true, &L);
     if (nseg <= 1) return 0;
-    const size_t n = (size_t)BH * nseg;
-    return n * K * 4 * 2 + ((n * 4 + 255) / 256) * 256;
+    return segment_scratch_bytes((size_t)BH * nseg, K);
 }
 
 cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
                                 const float *r, float eta, const float *d0, void *ktilde,
-                                float *dT, void *scratch, int *status, cudaStream_t stream) {
-    if (T == 0) {
+                                float *dT, float *logratio, void *scratch, int *status,
+                                cudaStream_t stream) {
+    if (T == 0) {   // d_T = d_0; an empty product of residual ratios is 1
+        if (logratio) {
+            p1::copy_or_fill_kernel<<<(unsigned)((BH + 255) / 256), 256, 0, stream>>>(
+                (size_t)BH, nullptr, 0.0f, logratio);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         if (!dT) return cudaSuccess;
         size_t n = (size_t)BH * K;
         p1::copy_or_fill_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(n, d0, 1.0f, dT);
@@ -598,12 +657,15 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
     p.eta = eta;
     p.ktilde = ktilde;
     p.dT = dT;
+    p.logratio = logratio;
     p.status = status;
     float *f = static_cast<float *>(scratch);
     const size_t n = (size_t)BH * p.nseg;
+    const size_t pad = ((n * 4 + 255) / 256) * 256 / 4;   // floats per padded [n] array
     p.ws_start = p.nseg > 1 ? f : nullptr;
     p.ws_end = p.nseg > 1 ? f + n * K : nullptr;
     p.ws_flag = p.nseg > 1 ? reinterpret_cast<int *>(f + 2 * n * K) : nullptr;
+    p.ws_lr = p.nseg > 1 ? f + 2 * n * K + pad : nullptr;
     if (io == OSDN_BF16)
         return K == 64 ? p1::launch<__nv_bfloat16, 64>(p, stream)
                        : p1::launch<__nv_bfloat16, 128>(p, stream);
@@ -655,8 +717,8 @@ cudaError_t precond_scan_noalloc_launch(int io, int BH, int T, int K, const void
     void *scratch = nullptr;
     cudaError_t e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return e;
-    return precond_scan_launch(io, BH, T, K, k, beta, r, eta, d0, ktilde, dT, scratch, nullptr,
-                               stream);
+    return precond_scan_launch(io, BH, T, K, k, beta, r, eta, d0, ktilde, dT, nullptr, scratch,
+                               nullptr, stream);
 }
 
 // Bytes of scratch the scan needs for this call (0 without a retention gate).
@@ -664,8 +726,7 @@ size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r) {
     int L;
     const int nseg = precond_segments(BH, T, has_r, &L);
     if (nseg <= 1 || T == 0) return 0;
-    const size_t n = (size_t)BH * nseg;
-    return n * K * 4 * 2 + ((n * 4 + 255) / 256) * 256;
+    return segment_scratch_bytes((size_t)BH * nseg, K);
 }
 
 cudaError_t fill_state_launch(size_t n, const float *src, float fill, float *dst,

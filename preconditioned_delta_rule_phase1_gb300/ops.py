@@ -30,6 +30,9 @@ _SIGS = {
     "osdn_precond_scan": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
                           [ctypes.c_float] + [ctypes.c_void_p] * 4 +
                           [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_precond_scan_residual": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
+                                   [ctypes.c_float] + [ctypes.c_void_p] * 5 +
+                                   [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_chunk_fwd": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
                        [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_precond_scan_noalloc": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 +
@@ -140,8 +143,13 @@ def chunk_fwd_workspace_bytes(io, B, H, T, K, V) -> int:
 
 
 def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, workspace=None,
-                 stream=None):
-    """Phase 1 (osdn_precond_scan): returns (ktilde, dT)."""
+                 stream=None, log_ratio=None):
+    """Phase 1 (osdn_precond_scan): returns (ktilde, dT).
+
+    With ``log_ratio`` (True, or a [B, H] fp32 tensor to fill) the call goes
+    through osdn_precond_scan_residual and returns (ktilde, dT, log_ratio):
+    per sequence sum_t log((1 - beta_t <d_t, k_t^2>)^2).
+    """
     B, H, T, K = k.shape
     io = _io(k)
     if ktilde is None:
@@ -150,11 +158,19 @@ def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, worksp
         dT = torch.empty(B, H, K, dtype=torch.float32, device=k.device)
     ws = workspace or Workspace(device=k.device)
     ws.ensure(precond_scan_workspace_bytes(B, H, T, K))
-    code = lib().osdn_precond_scan(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r), float(eta),
-                                   _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr, ws.nbytes,
-                                   _stream(stream))
-    _check(code, "osdn_precond_scan")
-    return ktilde, dT
+    if log_ratio is None or log_ratio is False:
+        code = lib().osdn_precond_scan(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r), float(eta),
+                                       _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr, ws.nbytes,
+                                       _stream(stream))
+        _check(code, "osdn_precond_scan")
+        return ktilde, dT
+    if log_ratio is True:
+        log_ratio = torch.empty(B, H, dtype=torch.float32, device=k.device)
+    code = lib().osdn_precond_scan_residual(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
+                                            float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
+                                            _ptr(log_ratio), ws.ptr, ws.nbytes, _stream(stream))
+    _check(code, "osdn_precond_scan_residual")
+    return ktilde, dT, log_ratio
 
 
 def precond_scan_noalloc(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, stream=None):

@@ -75,6 +75,20 @@ def test_host_validation_precond_scan(L):
     assert scan(L, B=0) == 0               # empty batch: nothing to do
 
 
+def resid(L, io=1, B=1, H=1, T=8, K=64, k=FAKE, kt=2 * FAKE, lr=4 * FAKE, ws=3 * FAKE, wsb=256):
+    return L.osdn_precond_scan_residual(io, B, H, T, K, k, FAKE, None, 0.1, None, kt, None, lr,
+                                        ws, wsb, None)
+
+
+def test_host_validation_precond_scan_residual(L):
+    assert resid(L, lr=None) == -1           # the diagnostic output is this call's point
+    assert resid(L, io=7) == -3 and resid(L, K=96) == -2
+    assert resid(L, lr=4 * FAKE + 4) == -4
+    assert resid(L, lr=FAKE) == -9           # log_ratio overlaps k
+    assert resid(L, lr=2 * FAKE) == -9       # log_ratio overlaps ktilde
+    assert resid(L, B=0) == 0
+
+
 def test_host_validation_chunk_fwd(L):
     assert chunk(L, io=2) == -3
     assert chunk(L, V=32) == -2 and chunk(L, H=-2) == -2
