@@ -505,13 +505,23 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p
     if (threadIdx.x == 0) first_bad = all_suspect ? 1 : p.nseg;
     __syncthreads();
     if (!all_suspect) {
-        for (int i = 1 + warp; i < p.nseg; i += nw) {
-            float2 prev[EP], cur[EP];
-            ld_pairs<EP>(p.ws_end + (base + i - 1) * K + E * lane, prev);
-            ld_pairs<EP>(p.ws_start + (base + i) * K + E * lane, cur);
-            float diff, mag;
-            warp_diff<EP>(prev, cur, diff, mag);
-            if (lane == 0 && !(diff <= kRelTol * mag)) atomicMin(&first_bad, i);
+        // kB boundaries per warp and pass, all loads in flight before the checks
+        constexpr int kB = 8;
+        for (int b0 = 1 + warp * kB; b0 < p.nseg; b0 += nw * kB) {
+            float2 prev[kB][EP], cur[kB][EP];
+#pragma unroll
+            for (int m = 0; m < kB; ++m) {
+                const int i = min(b0 + m, p.nseg - 1);   // past the end: a repeat of the last
+                ld_pairs<EP>(p.ws_end + (base + i - 1) * K + E * lane, prev[m]);
+                ld_pairs<EP>(p.ws_start + (base + i) * K + E * lane, cur[m]);
+            }
+#pragma unroll
+            for (int m = 0; m < kB; ++m) {
+                float diff, mag;
+                warp_diff<EP>(prev[m], cur[m], diff, mag);
+                if (lane == 0 && b0 + m < p.nseg && !(diff <= kRelTol * mag))
+                    atomicMin(&first_bad, b0 + m);
+            }
         }
     }
     __syncthreads();
