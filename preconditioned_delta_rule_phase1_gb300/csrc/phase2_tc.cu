@@ -82,10 +82,13 @@ struct Params {
 // Barriers.  The bf16 state copy entering chunk c sits in buffer c % NSB:
 // s_issued[b] completes when the state product reading it has been issued
 // (so the copy is complete), o_read[b] when the output product reading it
-// has completed (the buffer may then be overwritten).
+// has completed (the buffer may then be overwritten).  s_tmem completes when
+// every state warp has read the accumulator (and, gated, rescaled it): the
+// part of the next state product that does not read S (W V) may then start,
+// while the bf16 copy is still being written (s_ready).
 struct Bars {
     uint64_t fullX[NS], emptyX[NS], fullY[NS], emptyY[NS];
-    uint64_t s_full, s_ready, done_s, done_o;
+    uint64_t s_full, s_ready, s_tmem, done_s, done_o;
     uint64_t s_issued[NSB], o_read[NSB];
     uint64_t o_full[2], o_free[2];
 };
@@ -122,6 +125,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         uint64_t *one[] = {&bars.s_full, &bars.s_ready, &bars.done_s, &bars.done_o,
                            &bars.o_full[0], &bars.o_full[1], &bars.o_free[0], &bars.o_free[1]};
         for (uint64_t *b : one) ptx::mbar_init(b, 1);
+        ptx::mbar_init(&bars.s_tmem, 8);   // one arrival per state warp
         for (int i = 0; i < NSB; ++i) {
             ptx::mbar_init(&bars.s_issued[i], 1);
             ptx::mbar_init(&bars.o_read[i], 1);
@@ -188,17 +192,20 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         if (lane == 0) {
             const uint32_t id_s = ptx::idesc_bf16(K, BV, 0, 1);    // K-major A, MN-major B
             for (int j = 0; j < ncs; ++j) {
+                // S^T += [W | M] [V; S^T]; releases ring X.  W V as soon as the
+                // accumulator has been read, M S^T once the bf16 copy is in place.
                 if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) ||
-                    !wait_poll(&bars.s_ready, j & 1, &s_abort, st))
+                    !wait_poll(&bars.s_tmem, j & 1, &s_abort, st))
                     break;
                 ptx::tc_fence_after();
-                // S^T += [W | M] [V; S^T]; releases ring X
                 const uint32_t x = ptx::smem_u32(stX(j));
                 const uint64_t da = dk0(x), dV = dmn0(x + LY::oVx, 8192);
                 const uint64_t dSp = dmn0(ptx::smem_u32(sS(j)), 8192);
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
                     ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
+                if (!wait_poll(&bars.s_ready, j & 1, &s_abort, st)) break;
+                ptx::tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
                     ptx::umma_bf16(tmem + kColS, da + koff(K, 4 + ks), dSp + mnoff(ks), id_s, 1);
@@ -278,8 +285,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::tmem_st16(tS, lo);
             ptx::tmem_st16(tS + 16, hi);
             ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars.s_tmem);
+            ptx::fence_proxy_async_smem();
             ptx::named_bar(1, 256);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
@@ -311,11 +320,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 }
                 ptx::tmem_st16(tS, lo);
                 ptx::tmem_st16(tS + 16, hi);
+                ptx::tmem_wait_st();
             }
-            if (act) st_row_sw128(sS(n), K, krow, c0, sv, 32);
-            if (GATED) ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
+            // this warp is done with the accumulator
             ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars.s_tmem);
+            if (act) st_row_sw128(sS(n), K, krow, c0, sv, 32);
+            ptx::fence_proxy_async_smem();
             ptx::named_bar(1, 256);
             if (sti == 0) ptx::mbar_arrive(&bars.s_ready);
         }
