@@ -77,16 +77,28 @@ def phase2_flops(w):
 
 
 def launches_per_step(w, x):
-    """Kernels one step enqueues: the Phase 1 segment scan (plus its verify
-    kernel when a retention gate splits sequences into time segments, the
-    same rule the library applies) and Phase 2 (chunk preparation and the
-    state chain for bf16 I/O, one fp32 kernel otherwise)."""
+    """Kernels one step enqueues, by the library's own rules: the Phase 1
+    segment scan (plus its verify kernel when a retention gate splits the
+    sequences into time segments: L halves from 1024 while all segments
+    still fit in 8 warps per SM of 152) and Phase 2 (for bf16 I/O a
+    preparation and a chain launch per slab of at least 64 chunks, at most 64
+    slabs; one fp32 kernel otherwise)."""
     BH, T = w.B * w.H, w.T
     nseg = 1
     if x["r"] is not None and T > 256:
-        L = 1024 if BH * ((T + 1023) // 1024) >= 4 * 152 else 512
+        L = 1024
+        while L > 256 and BH * ((T + L // 2 - 1) // (L // 2)) <= 8 * 152:
+            L //= 2
         nseg = (T + L - 1) // L if L < T else 1
-    return (2 if nseg > 1 else 1) + (2 if w.io == "bf16" else 1)
+    p1 = 2 if nseg > 1 else 1
+    if w.io != "bf16":
+        return p1 + 1
+    nch = (T + 63) // 64
+    per = 64
+    while (nch + per - 1) // per > 64:
+        per *= 2
+    nslab = max(1, (nch + per - 1) // per)
+    return p1 + 2 * nslab
 
 
 def load_peaks():
