@@ -6,9 +6,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "osdn.h"
 
 namespace osdn {
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func`, once per
+// device: the attribute belongs to a device's context, so every device the
+// process launches on needs its own call.  `done` holds one bit per device
+// (devices past 63 set it on every call).
+inline cudaError_t smem_attr_once(const void *func, int bytes,
+                                  std::atomic<unsigned long long> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 constexpr unsigned kFullMask = 0xffffffffu;
 

@@ -575,17 +575,12 @@ __global__ void copy_or_fill_kernel(size_t n, const float *__restrict__ src, flo
 template <typename io_t, int K, bool HAS_R, bool LR>
 static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(precond_segment_kernel<io_t, K, HAS_R, LR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMaxWarps * kStage);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(precond_verify_kernel<io_t, K, HAS_R, LR>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kStage);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr_seg{0}, attr_ver{0};
+    cudaError_t e0 = smem_attr_once((const void *)precond_segment_kernel<io_t, K, HAS_R, LR>,
+                                    kMaxWarps * kStage, attr_seg);
+    if (e0 == cudaSuccess)
+        e0 = smem_attr_once((const void *)precond_verify_kernel<io_t, K, HAS_R, LR>, kStage, attr_ver);
+    if (e0 != cudaSuccess) return e0;
     // few segments: one per CTA, so that they spread over the SMs
     const long long nwarps = (long long)p.BH * p.nseg;
     const int wpc = nwarps >= 2LL * kSmCount ? kMaxWarps : 1;

@@ -463,12 +463,10 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
         !make_map(&mqe, qe, BH, Tp, K) || !make_map(&mae, ae, BH, Tp, C))
         return cudaErrorInvalidValue;
     constexpr int smem = PrepLay<K>::kAlloc;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<K, GATED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<unsigned long long> attr_done{0};
+    {
+        cudaError_t e = smem_attr_once((const void *)chunk_prep_kernel<K, GATED>, smem, attr_done);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     PrepParams p;
     p.T = T;

@@ -352,12 +352,10 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
         !make_map(&mv, v, BH, T, V))
         return cudaErrorInvalidValue;
     constexpr int smem = Lay<K>::kAlloc;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel<K, GATED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<unsigned long long> attr_done{0};
+    {
+        cudaError_t e = smem_attr_once((const void *)chunk_chain_kernel<K, GATED>, smem, attr_done);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     Params p;
     p.T = T;

@@ -163,11 +163,13 @@ def test_segmented_scan_exact(io, case):
     assert rel_err(dT, odT) <= tol, rel_err(dT, odT)
 
 
-def test_phase2_slabs_with_ragged_last_slab():
-    # 129 chunks of 64 tokens: the bf16 Phase 2 runs them as slabs of 64, 64
-    # and 1 chunk, preparing later slabs while earlier ones run and carrying
-    # the state between slabs; decay, S0 and S_T all cross the slab seams
-    T = 64 * 64 * 2 + 37
+@pytest.mark.parametrize("nfull", [128, 256 + 64])
+def test_phase2_slabs_with_ragged_last_slab(nfull):
+    # nfull chunks of 64 tokens and a ragged one: the bf16 Phase 2 runs them
+    # as slabs of 64 chunks and a last one of 1 chunk, preparing later slabs
+    # while earlier ones run and carrying the state between slabs; decay, S0
+    # and S_T all cross the slab seams
+    T = 64 * nfull + 37
     x = synth.make_random(1, 2, T, 64, 64, io="bf16", apf=True, gated=True, s0=True, d0=True,
                           seed=21)
     check_all(x, "bf16", None, "slabs T=%d" % T)
