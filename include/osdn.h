@@ -198,12 +198,17 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
  *   ST           out [B][H][V][K] fp32, or NULL (not written)
  * io == OSDN_BF16 runs on the tensor cores (bf16 operands, fp32
  * accumulation, state carried in fp32); io == OSDN_F32 runs in fp32 FFMA.
- * For sequences longer than 16 chunks of 64 tokens the bf16 path overlaps
+ * For sequences longer than 64 chunks of 64 tokens the bf16 path overlaps
  * the preparation of later chunks with the state recurrence of earlier ones
  * on two library-owned streams per device (created on first use, forked from
  * and joined back to `stream` with events); the library serialises the
  * enqueue of such calls.
  * With T == 0 the call writes ST = S0 and nothing else.
+ * Test hook: with the environment variable OSDN_TEST_STALL_CHAIN set, the
+ * bf16 path's state-recurrence kernel loads nothing, so its bounded waits
+ * run out (after limits shortened to milliseconds) and the call leaves
+ * OSDN_ERR_TIMEOUT in the status word with o and ST unwritten; the device
+ * stays usable.  It exists to test the timeout path.
  */
 int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
                    const void *ktilde, const void *v, const float *beta, const float *alpha,

@@ -33,6 +33,7 @@
 // Every wait is bounded: a wait that runs out records OSDN_ERR_TIMEOUT in the
 // status word and all roles leave their loops.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "tc_common.cuh"
@@ -77,6 +78,11 @@ struct Params {
     __nv_bfloat16 *o;
     float *ST;
     int *status;
+    // Test hook (environment variable OSDN_TEST_STALL_CHAIN): the producer
+    // issues nothing, so the waits run out -- after these limits, shortened
+    // for the test -- and the kernel ends with OSDN_ERR_TIMEOUT.
+    int stall;
+    uint32_t bar_limit, poll_limit;
 };
 
 // Barriers.  The bf16 state copy entering chunk c sits in buffer c % NSB:
@@ -152,10 +158,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::prefetch_tmap(&tm_qe);
             ptx::prefetch_tmap(&tm_v);
             int lastX = -1, lastY = -1;
-            for (int j = 0; j < ncs; ++j) {
+            for (int j = 0; j < (p.stall ? 0 : ncs); ++j) {
                 // rows of global chunk cbase + j in (Qe, Ae, V) and (W, M)
                 const int t0 = (cbase + j) * C, r0 = (cbase + j) * K;
-                if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st)) break;
+                if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st, p.bar_limit)) break;
                 uint8_t *x = stX(j);
                 ptx::mbar_arrive_expect_tx(&bars.fullX[j % NS], LY::kX);
 #pragma unroll
@@ -168,7 +174,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 }
                 ptx::tma_load_3d(x + LY::oVx, &tm_v, &bars.fullX[j % NS], v0, t0, seq);
                 lastX = j;
-                if (j >= NS && !wait_bar(&bars.emptyY[j % NS], ((j / NS) - 1) & 1, &s_abort, st)) break;
+                if (j >= NS && !wait_bar(&bars.emptyY[j % NS], ((j / NS) - 1) & 1, &s_abort, st, p.bar_limit)) break;
                 uint8_t *y = stY(j);
                 ptx::mbar_arrive_expect_tx(&bars.fullY[j % NS], LY::kY);
                 ptx::tma_load_3d(y, &tm_ae, &bars.fullY[j % NS], 0, t0, seq);
@@ -194,8 +200,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             for (int j = 0; j < ncs; ++j) {
                 // S^T += [W | M] [V; S^T]; releases ring X.  W V as soon as the
                 // accumulator has been read, M S^T once the bf16 copy is in place.
-                if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st) ||
-                    !wait_poll(&bars.s_tmem, j & 1, &s_abort, st))
+                if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st, p.poll_limit) ||
+                    !wait_poll(&bars.s_tmem, j & 1, &s_abort, st, p.poll_limit))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t x = ptx::smem_u32(stX(j));
@@ -204,7 +210,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
                     ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
-                if (!wait_poll(&bars.s_ready, j & 1, &s_abort, st)) break;
+                if (!wait_poll(&bars.s_ready, j & 1, &s_abort, st, p.poll_limit)) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
@@ -224,9 +230,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             const uint32_t id_o = ptx::idesc_bf16(64, BV, 0, 1);
             for (int c = 0; c < ncs; ++c) {
                 // O = [Ae | Qe] [V; S^T] of chunk c, behind chunk c's state product
-                if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st) ||
-                    !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st) ||
-                    (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st)))
+                if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st, p.poll_limit) ||
+                    !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st, p.poll_limit) ||
+                    (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st, p.poll_limit)))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t y = ptx::smem_u32(stY(c));
@@ -252,7 +258,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         const int ot = tid - 96;
         const int trow = 16 * q4 + lane;   // M=64 accumulator: lanes 0-15 of each quarter
         for (int j = 0; j < ncs; ++j) {
-            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st), 3, 128)) break;
+            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st, p.bar_limit), 3, 128)) break;
             ptx::tc_fence_after();
             float o[64];
             tmem_ld64(tmem + lane_off + kColO + 64 * (j & 1), o);
@@ -298,8 +304,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             // the copy entering chunk j+1 overwrites the one chunk j-2's output read
             const int n = j + 1;
             const bool okw = (last || n < NSB ||
-                              wait_poll(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st)) &&
-                             wait_poll(&bars.s_full, j & 1, &s_abort, st);
+                              wait_poll(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st, p.poll_limit)) &&
+                             wait_poll(&bars.s_full, j & 1, &s_abort, st, p.poll_limit);
             if (!vote_all(okw, 1, 256)) break;
             ptx::tc_fence_after();
             float sv[32];
@@ -368,6 +374,9 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.ST = ST;
     p.status = status;
+    p.stall = std::getenv("OSDN_TEST_STALL_CHAIN") != nullptr ? 1 : 0;
+    p.bar_limit = p.stall ? 64u : kWaitLimit;
+    p.poll_limit = p.stall ? (1u << 14) : (kWaitLimit << 11);
     dim3 grid(V / BV, BH);
     chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
     return cudaGetLastError();

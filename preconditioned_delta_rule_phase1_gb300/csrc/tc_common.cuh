@@ -154,10 +154,11 @@ __device__ __forceinline__ bool vote_all(bool v, int id, int count) {
     return out != 0;
 }
 
-// Bounded wait that also gives up as soon as another thread has aborted.
+// Bounded wait that also gives up as soon as another thread has aborted
+// (at most `limit` sleeping polls).
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         int *status) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+                                         int *status, uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
         if (*abort_flag) return false;
     }
@@ -166,10 +167,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     return false;
 }
 // Bounded poll without a suspend hint, for waits on a critical path, where a
-// sleeping thread wakes too late.
+// sleeping thread wakes too late (at most `limit` polls).
 __device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int *status) {
-    for (uint32_t i = 0; i < (kWaitLimit << 11); ++i) {
+                                          int *status, uint32_t limit = kWaitLimit << 11) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *abort_flag) return false;
     }
