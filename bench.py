@@ -467,14 +467,14 @@ def load_traffic(kernel, workload):
 
 def run_decode(args, local_rank):
     """--decode: the recurrent step (osdn_decode_step) on a serving batch of
-    128 sequences x 16 heads at d_k = d_v = 128, bf16 I/O, fp32 state.  The
-    state (128 MB) exceeds L2, so every step streams it from HBM; one JSON
-    line, with the step's HBM roofline (8 V K bytes of state per head plus
+    256 sequences x 16 heads at d_k = d_v = 128, bf16 I/O, fp32 state.  The
+    state (268 MB, twice L2) cannot stay in L2, so every step streams it
+    from HBM; one JSON line, with the step's HBM roofline (8 V K bytes of state per head plus
     the token's vectors)."""
     from preconditioned_delta_rule_phase1_gb300 import ops
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    B, H, K, V = 128, 16, 128, 128
+    B, H, K, V = 256, 16, 128, 128
     g = torch.Generator().manual_seed(0)
     q = torch.nn.functional.normalize(torch.randn(B, H, K, generator=g), dim=-1).to(torch.bfloat16).to(dev)
     k = torch.nn.functional.normalize(torch.randn(B, H, K, generator=g), dim=-1).to(torch.bfloat16).to(dev)
@@ -505,12 +505,12 @@ def run_decode(args, local_rank):
     hbm_peak, _, peak_src = load_peaks()
     achieved = nbytes / (ms * 1e-3) / 1e9
     print(json.dumps({
-        "metric": "OSDN decode step tokens/s (T=1, 128 sequences x 16 heads, d=128)",
+        "metric": "OSDN decode step tokens/s (T=1, 256 sequences x 16 heads, d=128)",
         "value": B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode_b128_h16_d128", "B": B, "H": H, "d_k": K, "d_v": V,
-                   "state": "fp32, 128 MB (larger than L2)"},
+        "config": {"workload": "decode_b256_h16_d128", "B": B, "H": H, "d_k": K, "d_v": V,
+                   "state": "fp32, 268 MB (twice L2)"},
         "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "algorithmic_bytes": nbytes, "peak_source": peak_src},
