@@ -77,20 +77,26 @@ def phase2_flops(w):
     return w.B * w.H * w.T * (6 * w.K * w.V + 2 * C * (w.K + w.V))
 
 
+def precond_segments(BH, T, has_r):
+    """Time segments per sequence of the Phase 1 scan, by the library's rule:
+    with a retention gate and T > 256, L halves from 1024 while all segments
+    still fit in 8 warps per SM of 152 (and stays >= 256); else one."""
+    if not has_r or T <= 256:
+        return 1
+    L = 1024
+    while L > 256 and BH * ((T + L // 2 - 1) // (L // 2)) <= 8 * 152:
+        L //= 2
+    return (T + L - 1) // L if L < T else 1
+
+
 def launches_per_step(w, x):
     """Kernels one step enqueues, by the library's own rules: the Phase 1
     segment scan (plus its verify kernel when a retention gate splits the
-    sequences into time segments: L halves from 1024 while all segments
-    still fit in 8 warps per SM of 152) and Phase 2 (for bf16 I/O a
-    preparation and a chain launch per slab of at least 64 chunks, at most 64
-    slabs; one fp32 kernel otherwise)."""
+    sequences into time segments) and Phase 2 (for bf16 I/O a preparation
+    and a chain launch per slab of at least 64 chunks, at most 64 slabs; one
+    fp32 kernel otherwise)."""
     BH, T = w.B * w.H, w.T
-    nseg = 1
-    if x["r"] is not None and T > 256:
-        L = 1024
-        while L > 256 and BH * ((T + L // 2 - 1) // (L // 2)) <= 8 * 152:
-            L //= 2
-        nseg = (T + L - 1) // L if L < T else 1
+    nseg = precond_segments(BH, T, x["r"] is not None)
     p1 = 2 if nseg > 1 else 1
     if w.io != "bf16":
         return p1 + 1

@@ -50,6 +50,21 @@ def test_workspace_sizes(L):
     assert ops.chunk_fwd_workspace_bytes(1, 2, 16, 8192, 128, 128) >= 256
 
 
+@pytest.mark.parametrize("B,H,T,K", [(2, 16, 8192, 128), (1, 16, 65536, 128), (4, 16, 4096, 64),
+                                     (8, 8, 2048, 128), (1, 6, 5000, 64), (64, 32, 8192, 128),
+                                     (1, 1, 257, 64), (1, 2, 256, 64)])
+def test_bench_segment_rule_matches_the_library(L, B, H, T, K):
+    # bench.py counts launches from a copy of the library's segment rule; the
+    # library's Phase 1 workspace holds, per segment, its start and end state
+    # (8 K bytes) and two 4-byte words, each array padded to 256 bytes
+    import bench
+    nseg = bench.precond_segments(B * H, T, True)
+    n = B * H * nseg
+    pad = lambda x: (x + 255) // 256 * 256
+    want = 256 + (n * K * 8 + 2 * pad(n * 4) if nseg > 1 else 0)
+    assert ops.precond_scan_workspace_bytes(B, H, T, K) == want
+
+
 FAKE = 0x10000  # never dereferenced: every case below fails validation first
 
 
