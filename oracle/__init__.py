@@ -10,6 +10,11 @@ Preconditioning in Linear Attention" (gist.science summary pages, sections
 1, 2.1, 2.2 and 2.3) that each step follows.  This module only compiles it
 and marshals numpy arrays in and out.
 
+``oracle/backward.py`` adds reference gradients (fp64 autograd through a
+token-by-token torch restatement of the same recurrence), pinned by
+``tests/test_oracle_backward.py`` against finite differences of this module's
+forward.
+
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts the
 pages and the mathematics fix (DeltaNet special case, definitional
 hypergradient surrogate, residual-ratio identity and its per-sequence log sum,
