@@ -4,6 +4,12 @@ Argument marshalling only: every step of the forward pass runs in the CUDA
 kernels behind the C ABI.  PyTorch provides device memory and the stream.
 There is no CPU path: if the library is not built, or the tensors are not
 on a CUDA device, the calls raise.
+
+The C ABI takes plain pointers, so it cannot see shapes, dtypes or devices;
+the binding checks them (every tensor's shape, dtype and device against the
+call's layout) before any pointer leaves Python, and runs the call with the
+tensors' device current and, by default, on its current stream.  A tensor
+of the wrong type would otherwise be read or written out of its bounds.
 """
 from __future__ import annotations
 
@@ -92,9 +98,43 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+F32 = torch.float32
+
+
+def _expect(name, t, shape, dtype, device):
+    """Raise unless `t` (a tensor, or None for an absent optional argument)
+    has the shape, dtype and device the call reads or writes, and is dense."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor, got %s" % (name, type(t).__name__))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if t.dtype != dtype:
+        raise TypeError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    if t.device != device:
+        raise ValueError("%s is on %s; the call runs on %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous (the library reads it densely)" % name)
+
+
+def _on(device):
+    """The context of a call on `device`: that CUDA device current."""
+    if device.type != "cuda":
+        raise ValueError("OSDN operates on CUDA tensors only")
+    return torch.cuda.device(device)
+
+
+def _workspace(workspace, device):
+    ws = workspace or Workspace(device=device)
+    if ws.buf.device != device:
+        raise ValueError("workspace is on %s; the call runs on %s" % (ws.buf.device, device))
+    return ws
 
 
 def _check(code: int, where: str):
@@ -151,24 +191,34 @@ def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, worksp
     per sequence sum_t log((1 - beta_t <d_t, k_t^2>)^2).
     """
     B, H, T, K = k.shape
-    io = _io(k)
+    io, dev = _io(k), k.device
+    _expect("beta", beta, (B, H, T), F32, dev)
+    _expect("r", r, (B, H, T), F32, dev)
+    _expect("d0", d0, (B, H, K), F32, dev)
     if ktilde is None:
         ktilde = torch.empty_like(k)
     if dT is None:
-        dT = torch.empty(B, H, K, dtype=torch.float32, device=k.device)
-    ws = workspace or Workspace(device=k.device)
-    ws.ensure(precond_scan_workspace_bytes(B, H, T, K))
-    if log_ratio is None or log_ratio is False:
-        code = lib().osdn_precond_scan(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r), float(eta),
-                                       _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr, ws.nbytes,
-                                       _stream(stream))
-        _check(code, "osdn_precond_scan")
-        return ktilde, dT
+        dT = torch.empty(B, H, K, dtype=F32, device=dev)
+    _expect("ktilde", ktilde, (B, H, T, K), k.dtype, dev)
+    _expect("dT", dT, (B, H, K), F32, dev)
+    residual = not (log_ratio is None or log_ratio is False)
     if log_ratio is True:
-        log_ratio = torch.empty(B, H, dtype=torch.float32, device=k.device)
-    code = lib().osdn_precond_scan_residual(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
-                                            float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
-                                            _ptr(log_ratio), ws.ptr, ws.nbytes, _stream(stream))
+        log_ratio = torch.empty(B, H, dtype=F32, device=dev)
+    if residual:
+        _expect("log_ratio", log_ratio, (B, H), F32, dev)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        ws.ensure(precond_scan_workspace_bytes(B, H, T, K))
+        if not residual:
+            code = lib().osdn_precond_scan(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
+                                           float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT), ws.ptr,
+                                           ws.nbytes, _stream(stream, dev))
+            _check(code, "osdn_precond_scan")
+            return ktilde, dT
+        code = lib().osdn_precond_scan_residual(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
+                                                float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
+                                                _ptr(log_ratio), ws.ptr, ws.nbytes,
+                                                _stream(stream, dev))
     _check(code, "osdn_precond_scan_residual")
     return ktilde, dT, log_ratio
 
@@ -177,13 +227,20 @@ def precond_scan_noalloc(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None
     """Phase 1 through osdn_precond_scan_noalloc: no workspace, no device
     allocation inside the call (outputs are allocated here only when not given)."""
     B, H, T, K = k.shape
+    io, dev = _io(k), k.device
+    _expect("beta", beta, (B, H, T), F32, dev)
+    _expect("r", r, (B, H, T), F32, dev)
+    _expect("d0", d0, (B, H, K), F32, dev)
     if ktilde is None:
         ktilde = torch.empty_like(k)
     if dT is None:
-        dT = torch.empty(B, H, K, dtype=torch.float32, device=k.device)
-    code = lib().osdn_precond_scan_noalloc(_io(k), B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
-                                           float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
-                                           _stream(stream))
+        dT = torch.empty(B, H, K, dtype=F32, device=dev)
+    _expect("ktilde", ktilde, (B, H, T, K), k.dtype, dev)
+    _expect("dT", dT, (B, H, K), F32, dev)
+    with _on(dev):
+        code = lib().osdn_precond_scan_noalloc(io, B, H, T, K, _ptr(k), _ptr(beta), _ptr(r),
+                                               float(eta), _ptr(d0), _ptr(ktilde), _ptr(dT),
+                                               _stream(stream, dev))
     _check(code, "osdn_precond_scan_noalloc")
     return ktilde, dT
 
@@ -193,16 +250,25 @@ def chunk_fwd(q, k, ktilde, v, beta, alpha=None, S0=None, o=None, ST=None, works
     """Phase 2 (osdn_chunk_fwd): returns (o, ST)."""
     B, H, T, K = k.shape
     V = v.shape[-1]
-    io = _io(k)
+    io, dev = _io(k), k.device
+    _expect("q", q, (B, H, T, K), k.dtype, dev)
+    _expect("ktilde", ktilde, (B, H, T, K), k.dtype, dev)
+    _expect("v", v, (B, H, T, V), k.dtype, dev)
+    _expect("beta", beta, (B, H, T), F32, dev)
+    _expect("alpha", alpha, (B, H, T), F32, dev)
+    _expect("S0", S0, (B, H, V, K), F32, dev)
     if o is None:
-        o = torch.empty(B, H, T, V, dtype=k.dtype, device=k.device)
+        o = torch.empty(B, H, T, V, dtype=k.dtype, device=dev)
     if ST is None:
-        ST = torch.empty(B, H, V, K, dtype=torch.float32, device=k.device)
-    ws = workspace or Workspace(device=k.device)
-    ws.ensure(chunk_fwd_workspace_bytes(io, B, H, T, K, V))
-    code = lib().osdn_chunk_fwd(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v),
-                                _ptr(beta), _ptr(alpha), _ptr(S0), _ptr(o), _ptr(ST), ws.ptr,
-                                ws.nbytes, _stream(stream))
+        ST = torch.empty(B, H, V, K, dtype=F32, device=dev)
+    _expect("o", o, (B, H, T, V), k.dtype, dev)
+    _expect("ST", ST, (B, H, V, K), F32, dev)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        ws.ensure(chunk_fwd_workspace_bytes(io, B, H, T, K, V))
+        code = lib().osdn_chunk_fwd(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v),
+                                    _ptr(beta), _ptr(alpha), _ptr(S0), _ptr(o), _ptr(ST), ws.ptr,
+                                    ws.nbytes, _stream(stream, dev))
     _check(code, "osdn_chunk_fwd")
     return o, ST
 
@@ -210,7 +276,7 @@ def chunk_fwd(q, k, ktilde, v, beta, alpha=None, S0=None, o=None, ST=None, works
 def forward(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, workspace=None,
             stream=None):
     """Both phases: returns (ktilde, dT, o, ST)."""
-    ws = workspace or Workspace(device=k.device)
+    ws = _workspace(workspace, k.device)
     ktilde, dT = precond_scan(k, beta, r, eta, d0, workspace=ws, stream=stream)
     o, ST = chunk_fwd(q, k, ktilde, v, beta, alpha, S0, workspace=ws, stream=stream)
     return ktilde, dT, o, ST
@@ -223,14 +289,24 @@ def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde
     (o, ktilde)."""
     B, H, K = k.shape
     V = v.shape[-1]
-    io = _io(k)
+    io, dev = _io(k), k.device
+    _expect("q", q, (B, H, K), k.dtype, dev)
+    _expect("v", v, (B, H, V), k.dtype, dev)
+    _expect("beta", beta, (B, H), F32, dev)
+    _expect("r", r, (B, H), F32, dev)
+    _expect("alpha", alpha, (B, H), F32, dev)
+    _expect("d", d, (B, H, K), F32, dev)
+    _expect("S", S, (B, H, V, K), F32, dev)
     if o is None:
-        o = torch.empty(B, H, V, dtype=k.dtype, device=k.device)
+        o = torch.empty(B, H, V, dtype=k.dtype, device=dev)
     if ktilde is None:
-        ktilde = torch.empty(B, H, K, dtype=k.dtype, device=k.device)
-    ws = workspace or Workspace(device=k.device)
-    code = lib().osdn_decode_step(io, B, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(r),
-                                  float(eta), _ptr(alpha), _ptr(d), _ptr(S), _ptr(o),
-                                  _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream))
+        ktilde = torch.empty(B, H, K, dtype=k.dtype, device=dev)
+    _expect("o", o, (B, H, V), k.dtype, dev)
+    _expect("ktilde", ktilde, (B, H, K), k.dtype, dev)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        code = lib().osdn_decode_step(io, B, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                      _ptr(r), float(eta), _ptr(alpha), _ptr(d), _ptr(S), _ptr(o),
+                                      _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream, dev))
     _check(code, "osdn_decode_step")
     return o, ktilde
