@@ -1,5 +1,6 @@
 /*
- * osdn.h -- C ABI of the GB300 (sm_103a) Online Scaled DeltaNet forward pass.
+ * osdn.h -- C ABI of the GB300 (sm_103a) Online Scaled DeltaNet forward pass
+ * and its gradients.
  *
  * The method: "OSDN: Improving Delta Rule with Provable Online
  * Preconditioning in Linear Attention" (arXiv 2605.13473), as summarised on
@@ -12,6 +13,11 @@
  *   Phase 2  osdn_chunk_fwd     -- the chunkwise delta-rule pass with ktilde
  *            in place of k in the chunk Gram matrix and the intra-chunk scores
  *            (section 2.1), producing o_t = S_t q_t and the final state.
+ *
+ * Around them: osdn_precond_scan_residual (Phase 1 plus the per-sequence
+ * log of the residual ratios, section 3 and section 4.2), osdn_decode_step
+ * (both phases at T = 1, in place, for inference) and osdn_backward (the
+ * gradients of both phases, for training).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -238,6 +244,55 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
                      const void *v, const float *beta, const float *r, float eta,
                      const float *alpha, float *d, float *S, void *o, void *ktilde,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of workspace osdn_backward needs for this shape (>= 256): the state
+ * of each value row every 16 tokens (4 B*H*ceil(T/16)*V*K), one partial of
+ * the row-summed gradients per block of 8 value rows (4 B*H*(V/8)*T*(3K+2)),
+ * and 4 B*H*(T*(2K+1) + ceil(T/16)*K) for Phase 1's inputs and checkpoints,
+ * each rounded up to 256 bytes.
+ */
+size_t osdn_backward_workspace_bytes(int B, int H, int T, int K, int V);
+
+/*
+ * Gradients of the forward pass through both phases (the derivative of the
+ * recurrences of osdn_precond_scan and osdn_chunk_fwd: sections 2.1, 2.2 and
+ * 2.3), for training.  Given the forward's inputs, the ktilde it produced and
+ * the cotangents of its outputs, the call returns the gradient of
+ *     L = <o, d_o> + <S_T, d_ST> + <d_T, d_dT> + <ktilde, d_ktilde>
+ * with respect to every input.  Cotangents given as NULL count as zero.
+ *
+ * Inputs (the forward's, with its defaults for NULL):
+ *   q, k, ktilde in [B][H][T][K] io  (ktilde as osdn_precond_scan wrote it)
+ *   v            in [B][H][T][V] io
+ *   beta         in [B][H][T] fp32;  r, alpha in [B][H][T] fp32 or NULL (1)
+ *   eta          the step size;  d0 in [B][H][K] fp32 or NULL (ones)
+ *   S0           in [B][H][V][K] fp32 or NULL (zeros)
+ *   d_o          in [B][H][T][V] io or NULL;   d_ST in [B][H][V][K] fp32 or NULL
+ *   d_dT         in [B][H][K] fp32 or NULL;    d_ktilde in [B][H][T][K] io or NULL
+ * Outputs:
+ *   dq, dk       out [B][H][T][K] io;   dv out [B][H][T][V] io
+ *   dbeta        out [B][H][T] fp32
+ *   dr, dalpha   out [B][H][T] fp32, or NULL (not written)
+ *   dd0          out [B][H][K] fp32, or NULL;  dS0 out [B][H][V][K] fp32, or NULL
+ *   deta         out [B][H] fp32, or NULL: each sequence's share of dL/deta
+ *                (the gradient of the shared scalar eta is their sum)
+ * The arithmetic is fp32 for both I/O types (bf16 inputs are widened, bf16
+ * outputs rounded once at the end).  The pass runs token by token in
+ * reverse time: Phase 2's state gradient one value row per warp, with the
+ * forward states recomputed 16 tokens at a time from checkpoints; then the
+ * Phase 1 adjoint one sequence per warp.  The results are deterministic
+ * (row sums in a fixed order, no atomics).  Outputs must not overlap inputs
+ * or each other (OSDN_ERR_ALIAS).  With T == 0 the call writes dS0 = d_ST,
+ * dd0 = d_dT (zeros for NULL) and deta = 0.
+ */
+int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                  const void *ktilde, const void *v, const float *beta, const float *r,
+                  float eta, const float *d0, const float *alpha, const float *S0,
+                  const void *d_o, const float *d_ST, const float *d_dT, const void *d_ktilde,
+                  void *dq, void *dk, void *dv, float *dbeta, float *dr, float *dalpha,
+                  float *dd0, float *dS0, float *deta, void *workspace, size_t workspace_bytes,
+                  void *stream);
 
 /* Zero the 256-byte status area at the start of a workspace (async). */
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);

@@ -1,0 +1,471 @@
+// backward.cu -- gradients of the OSDN forward pass through both phases, in
+// fp32 arithmetic (both I/O types), token by token in reverse time.
+//
+// The forward ("OSDN: Improving Delta Rule with Provable Online
+// Preconditioning in Linear Attention", gist.science summary, sections 2.1,
+// 2.2 and 2.3):
+//
+//     ktilde_t = d_t (.) k_t
+//     d_{t+1}  = r_t d_t + c_t w_t,   w_t = k_t^2,  n_t = |k_t|^2,
+//                c_t = eta beta_t (1 - beta_t <d_t, w_t>) / n_t  (0 if n_t = 0)
+//     S_t      = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) ktilde_t^T
+//     o_t      = S_t q_t
+//
+// Its derivative is taken by hand and run in three kernels:
+//
+//  1. state_adjoint_kernel -- Phase 2.  The rows of S evolve independently,
+//     so one warp owns value row i (lane l holds key columns l*NC..l*NC+NC-1,
+//     NC = K/32) and a CTA holds 8 rows.  A forward sweep writes the row's
+//     state every 16 tokens; the reverse sweep recomputes each 16-token
+//     sub-chunk (states in shared memory) and walks it backwards with the
+//     row's state gradient G = dL/dS_t[i,:]:
+//         G += dO_t[i] q_t;  du = <G, ktilde_t>;  dSbar = G - beta du k_t
+//         dv_t[i] = beta du;  G <- alpha dSbar
+//     and the row's shares of the gradients that sum over rows
+//         dq_t += dO_t[i] S_t[i],  dktilde_t += u_t[i] G,
+//         dk_t += -beta du alpha S_{t-1}[i],  dbeta_t += du e_t[i],
+//         dalpha_t += <dSbar, S_{t-1}[i]>      (e = v - alpha S_{t-1} k)
+//     which the CTA adds over its 8 rows in warp order and writes as one
+//     partial per row block (no atomics: the result is deterministic).
+//  2. partial_sum_kernel -- adds the row-block partials in a fixed order:
+//     dq and dalpha are final; dktilde (plus the caller's cotangent of the
+//     ktilde output), Phase 2's share of dk and of dbeta go to scratch.
+//  3. precond_adjoint_kernel -- Phase 1.  One warp per sequence runs the
+//     adjoint lam = dL/dd_t backwards; the step's Jacobian r I - mu w w^T is
+//     symmetric, so the adjoint has the forward's form:
+//         dr_t = <lam, d_t>,  dc = <lam, w_t>,  da = -dc eta beta^2 / n
+//         dbeta_t += dc eta (1 - 2 beta a) / n,  deta += dc beta (1 - beta a) / n
+//         dk_t += g d_t + 2 k_t (c_t lam + da d_t + dn),  dn = -dc c_t / n
+//         lam <- r_t lam + da w_t + g k_t,   g = dktilde_t (both shares)
+//     with d_t recomputed by 16-token sub-chunks from checkpoints.
+//
+// Every access is a plain load or store inside the caller's buffers or the
+// workspace; there are no waits, so nothing can stall.
+#include <atomic>
+
+#include "osdn_device.cuh"
+
+namespace osdn {
+
+constexpr int kBwdSub = 16;    // tokens per recomputed sub-chunk
+constexpr int kBwdRows = 8;    // value rows (one warp each) per state-adjoint CTA
+constexpr int kBwdSeqs = 4;    // sequences (one warp each) per precond-adjoint CTA
+constexpr int kSumTok = 8;     // tokens per partial-sum CTA
+
+__host__ __device__ constexpr int bwd_part_width(int K) { return 3 * K + 2; }
+// row stride of the shared reduction buffer: a multiple of 4 floats keeps the
+// vector stores into it 16-byte aligned
+__host__ __device__ constexpr int bwd_red_stride(int K) { return (bwd_part_width(K) + 3) & ~3; }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(kFullMask, x, m);
+    return x;
+}
+__device__ __forceinline__ float2 warp_sum2(float2 x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        x.x += __shfl_xor_sync(kFullMask, x.x, m);
+        x.y += __shfl_xor_sync(kFullMask, x.y, m);
+    }
+    return x;
+}
+
+// NC consecutive elements (NC = 2 or 4) at p, converted to fp32.
+template <int NC, typename T>
+__device__ __forceinline__ void load_cols(const T *p, float (&x)[NC]) {
+    if constexpr (NC == 4) load4(p, x); else load2(p, x);
+}
+template <int NC, typename T>
+__device__ __forceinline__ void store_cols(T *p, const float (&x)[NC]) {
+    if constexpr (NC == 4) store4(p, x); else store2(p, x);
+}
+
+// ---------------------------------------------------------------- kernel 1
+template <typename io_t, int K>
+__global__ void __launch_bounds__(kBwdRows * 32)
+state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
+                     const io_t *__restrict__ k, const io_t *__restrict__ kt,
+                     const io_t *__restrict__ v, const float *__restrict__ beta,
+                     const float *__restrict__ alpha, const float *__restrict__ S0,
+                     const io_t *__restrict__ dO, const float *__restrict__ dST,
+                     io_t *__restrict__ dv, float *__restrict__ dS0, float *__restrict__ ck,
+                     float *__restrict__ part) {
+    constexpr int NC = K / 32;
+    constexpr int P = bwd_part_width(K);
+    constexpr int PS = bwd_red_stride(K);
+    extern __shared__ __align__(16) float smem[];
+    float *Sp = smem;                                  // [kBwdRows][kBwdSub][K]
+    float *red = smem + kBwdRows * kBwdSub * K;        // [2][kBwdRows][PS]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = blockIdx.x, nrb = gridDim.x;
+    const int i = rb * kBwdRows + warp;               // this warp's value row
+    const size_t seq = blockIdx.y;
+    const int c0 = lane * NC;
+    const size_t tok0 = seq * (size_t)T;               // first token of the sequence
+    float *Spw = Sp + warp * kBwdSub * K;
+
+    // forward sweep: the row's state every kBwdSub tokens
+    float S[NC];
+    if (S0) {
+        load_cols<NC>(S0 + (seq * V + i) * (size_t)K + c0, S);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) S[m] = 0.0f;
+    }
+    for (int t = 0; t < T; ++t) {
+        if (t % kBwdSub == 0)
+            store_cols<NC>(ck + ((seq * nsub + t / kBwdSub) * V + i) * (size_t)K + c0, S);
+        float kc[NC], tc[NC];
+        load_cols<NC>(k + (tok0 + t) * K + c0, kc);
+        load_cols<NC>(kt + (tok0 + t) * K + c0, tc);
+        const float a = alpha ? alpha[tok0 + t] : 1.0f;
+        float sk = 0.0f;
+#pragma unroll
+        for (int m = 0; m < NC; ++m) sk = fmaf(S[m], kc[m], sk);
+        sk = warp_sum(sk);
+        const float u = beta[tok0 + t] * (to_f32(v[(tok0 + t) * V + i]) - a * sk);
+#pragma unroll
+        for (int m = 0; m < NC; ++m) S[m] = fmaf(a, S[m], u * tc[m]);
+    }
+
+    // reverse sweep
+    float G[NC];
+    if (dST) {
+        load_cols<NC>(dST + (seq * V + i) * (size_t)K + c0, G);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) G[m] = 0.0f;
+    }
+    int buf = 0;
+    for (int j = nsub - 1; j >= 0; --j) {
+        const int t0 = j * kBwdSub;
+        const int tn = min(kBwdSub, T - t0);
+        // recompute the sub-chunk: S_{t-1} of each token into shared memory,
+        // e_t and u_t of token t0+tt kept by lane tt
+        load_cols<NC>(ck + ((seq * nsub + j) * V + i) * (size_t)K + c0, S);
+        float my_e = 0.0f, my_u = 0.0f;
+        for (int tt = 0; tt < tn; ++tt) {
+            const size_t g = tok0 + t0 + tt;
+            store_cols<NC>(Spw + tt * K + c0, S);
+            float kc[NC], tc[NC];
+            load_cols<NC>(k + g * K + c0, kc);
+            load_cols<NC>(kt + g * K + c0, tc);
+            const float a = alpha ? alpha[g] : 1.0f;
+            float sk = 0.0f;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) sk = fmaf(S[m], kc[m], sk);
+            sk = warp_sum(sk);
+            const float e = to_f32(v[g * V + i]) - a * sk;
+            const float u = beta[g] * e;
+            if (lane == tt) { my_e = e; my_u = u; }
+#pragma unroll
+            for (int m = 0; m < NC; ++m) S[m] = fmaf(a, S[m], u * tc[m]);
+        }
+        // walk it backwards (each lane reads back only its own columns of Spw)
+        for (int tt = tn - 1; tt >= 0; --tt) {
+            const size_t g = tok0 + t0 + tt;
+            const float e = __shfl_sync(kFullMask, my_e, tt);
+            const float u = __shfl_sync(kFullMask, my_u, tt);
+            float sp[NC], qc[NC], kc[NC], tc[NC];
+            load_cols<NC>(Spw + tt * K + c0, sp);
+            load_cols<NC>(q + g * K + c0, qc);
+            load_cols<NC>(k + g * K + c0, kc);
+            load_cols<NC>(kt + g * K + c0, tc);
+            const float a = alpha ? alpha[g] : 1.0f;
+            const float b = beta[g];
+            const float dOi = dO ? to_f32(dO[g * V + i]) : 0.0f;
+            float du = 0.0f;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                G[m] = fmaf(dOi, qc[m], G[m]);
+                du = fmaf(G[m], tc[m], du);
+            }
+            du = warp_sum(du);
+            float dSb[NC], dal = 0.0f;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                dSb[m] = G[m] - b * du * kc[m];
+                dal = fmaf(dSb[m], sp[m], dal);
+            }
+            dal = warp_sum(dal);
+            float *rw = red + (buf * kBwdRows + warp) * PS;
+            float cq[NC], ct[NC], ck_[NC];
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                cq[m] = dOi * fmaf(a, sp[m], u * tc[m]);   // dO_t[i] S_t[i]
+                ct[m] = u * G[m];                          // u_t[i] G
+                ck_[m] = -b * du * a * sp[m];              // -beta du alpha S_{t-1}[i]
+            }
+            store_cols<NC>(rw + c0, cq);
+            store_cols<NC>(rw + K + c0, ct);
+            store_cols<NC>(rw + 2 * K + c0, ck_);
+            if (lane == 0) {
+                rw[3 * K] = du * e;
+                rw[3 * K + 1] = dal;
+                from_f32(dv[g * V + i], b * du);
+            }
+#pragma unroll
+            for (int m = 0; m < NC; ++m) G[m] = a * dSb[m];
+            __syncthreads();
+            // the CTA's sum over its rows, in warp order; the next token
+            // writes the other buffer, and its barrier orders these reads
+            // before this buffer is written again
+            const float *rsum = red + buf * kBwdRows * PS;
+            float *dst = part + ((seq * nrb + rb) * (size_t)T + t0 + tt) * P;
+            for (int x = threadIdx.x; x < P; x += kBwdRows * 32) {
+                float s = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kBwdRows; ++w) s += rsum[w * PS + x];
+                dst[x] = s;
+            }
+            buf ^= 1;
+        }
+    }
+    if (dS0) store_cols<NC>(dS0 + (seq * V + i) * (size_t)K + c0, G);
+}
+
+// ---------------------------------------------------------------- kernel 2
+template <typename io_t, int K>
+__global__ void __launch_bounds__(256)
+partial_sum_kernel(int T, int nrb, const float *__restrict__ part,
+                   const io_t *__restrict__ dkt_ext, io_t *__restrict__ dq,
+                   float *__restrict__ dalpha, float *__restrict__ dkt_tot,
+                   float *__restrict__ dk2, float *__restrict__ db2) {
+    constexpr int P = bwd_part_width(K);
+    const size_t seq = blockIdx.y;
+    const int tb = blockIdx.x * kSumTok;
+    for (int x = threadIdx.x; x < kSumTok * P; x += blockDim.x) {
+        const int tt = x / P, col = x % P;
+        const int t = tb + tt;
+        if (t >= T) continue;
+        float s = 0.0f;
+        for (int r = 0; r < nrb; ++r) s += part[((seq * nrb + r) * (size_t)T + t) * P + col];
+        const size_t g = seq * (size_t)T + t;
+        if (col < K) {
+            from_f32(dq[g * K + col], s);
+        } else if (col < 2 * K) {
+            const int c = col - K;
+            dkt_tot[g * K + c] = s + (dkt_ext ? to_f32(dkt_ext[g * K + c]) : 0.0f);
+        } else if (col < 3 * K) {
+            dk2[g * K + col - 2 * K] = s;
+        } else if (col == 3 * K) {
+            db2[g] = s;
+        } else if (dalpha) {
+            dalpha[g] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel 3
+template <typename io_t, int K>
+__global__ void __launch_bounds__(kBwdSeqs * 32)
+precond_adjoint_kernel(int BH, int T, int nsub, const io_t *__restrict__ k,
+                       const float *__restrict__ beta, const float *__restrict__ r, float eta,
+                       const float *__restrict__ d0, const float *__restrict__ dkt_tot,
+                       const float *__restrict__ ddT, const float *__restrict__ dk2,
+                       const float *__restrict__ db2, io_t *__restrict__ dk,
+                       float *__restrict__ dbeta, float *__restrict__ dr,
+                       float *__restrict__ dd0, float *__restrict__ deta,
+                       float *__restrict__ ck) {
+    constexpr int NC = K / 32;
+    __shared__ __align__(16) float dsub[kBwdSeqs][kBwdSub][K];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sid = blockIdx.x * kBwdSeqs + warp;
+    if (sid >= BH) return;                     // whole warps only: no block barrier below
+    const size_t seq = sid;
+    const int c0 = lane * NC;
+    const size_t tok0 = seq * (size_t)T;
+
+    // forward sweep: d every kBwdSub tokens
+    float d[NC];
+    if (d0) {
+        load_cols<NC>(d0 + seq * K + c0, d);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) d[m] = 1.0f;
+    }
+    for (int t = 0; t < T; ++t) {
+        if (t % kBwdSub == 0) store_cols<NC>(ck + (seq * nsub + t / kBwdSub) * K + c0, d);
+        float kc[NC];
+        load_cols<NC>(k + (tok0 + t) * K + c0, kc);
+        float2 na = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+            const float w = kc[m] * kc[m];
+            na.x += w;
+            na.y = fmaf(d[m], w, na.y);
+        }
+        na = warp_sum2(na);
+        const float b = beta[tok0 + t];
+        const float c = na.x > 0.0f ? eta * b * (1.0f - b * na.y) / na.x : 0.0f;
+        const float rt = r ? r[tok0 + t] : 1.0f;
+#pragma unroll
+        for (int m = 0; m < NC; ++m) d[m] = fmaf(rt, d[m], c * (kc[m] * kc[m]));
+    }
+
+    // reverse sweep
+    float lam[NC];
+    if (ddT) {
+        load_cols<NC>(ddT + seq * K + c0, lam);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) lam[m] = 0.0f;
+    }
+    float deta_acc = 0.0f;
+    for (int j = nsub - 1; j >= 0; --j) {
+        const int t0 = j * kBwdSub;
+        const int tn = min(kBwdSub, T - t0);
+        load_cols<NC>(ck + (seq * nsub + j) * K + c0, d);
+        float my_n = 0.0f, my_a = 0.0f;
+        for (int tt = 0; tt < tn; ++tt) {
+            const size_t g = tok0 + t0 + tt;
+            store_cols<NC>(&dsub[warp][tt][c0], d);
+            float kc[NC];
+            load_cols<NC>(k + g * K + c0, kc);
+            float2 na = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                const float w = kc[m] * kc[m];
+                na.x += w;
+                na.y = fmaf(d[m], w, na.y);
+            }
+            na = warp_sum2(na);
+            if (lane == tt) { my_n = na.x; my_a = na.y; }
+            const float b = beta[g];
+            const float c = na.x > 0.0f ? eta * b * (1.0f - b * na.y) / na.x : 0.0f;
+            const float rt = r ? r[g] : 1.0f;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) d[m] = fmaf(rt, d[m], c * (kc[m] * kc[m]));
+        }
+        for (int tt = tn - 1; tt >= 0; --tt) {
+            const size_t g = tok0 + t0 + tt;
+            const float n = __shfl_sync(kFullMask, my_n, tt);
+            const float a = __shfl_sync(kFullMask, my_a, tt);
+            float dc_[NC], kc[NC], gk[NC], k2[NC];
+            load_cols<NC>(&dsub[warp][tt][c0], dc_);
+            load_cols<NC>(k + g * K + c0, kc);
+            load_cols<NC>(dkt_tot + g * K + c0, gk);
+            load_cols<NC>(dk2 + g * K + c0, k2);
+            float2 rc = make_float2(0.0f, 0.0f);       // (<lam, d_t>, <lam, w_t>)
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                rc.x = fmaf(lam[m], dc_[m], rc.x);
+                rc.y = fmaf(lam[m], kc[m] * kc[m], rc.y);
+            }
+            rc = warp_sum2(rc);
+            const float b = beta[g];
+            const float rt = r ? r[g] : 1.0f;
+            float c = 0.0f, da = 0.0f, db1 = 0.0f, dn = 0.0f;
+            if (n > 0.0f) {
+                const float res = 1.0f - b * a;
+                c = eta * b * res / n;
+                da = -rc.y * eta * b * b / n;
+                db1 = rc.y * eta * (1.0f - 2.0f * b * a) / n;
+                deta_acc += rc.y * b * res / n;
+                dn = -rc.y * c / n;
+            }
+            float out[NC];
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                out[m] = k2[m] + gk[m] * dc_[m] +
+                         2.0f * kc[m] * (c * lam[m] + da * dc_[m] + dn);
+                lam[m] = fmaf(rt, lam[m], fmaf(da, kc[m] * kc[m], gk[m] * kc[m]));
+            }
+            store_cols<NC>(dk + g * K + c0, out);
+            if (lane == 0) {
+                dbeta[g] = db2[g] + db1;
+                if (dr) dr[g] = rc.x;
+            }
+        }
+    }
+    if (dd0) store_cols<NC>(dd0 + seq * K + c0, lam);
+    if (deta && lane == 0) deta[seq] = deta_acc;
+}
+
+// ---------------------------------------------------------------- host side
+static size_t pad256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct BwdScratch {
+    float *ck2, *part, *dkt_tot, *dk2, *db2, *ck1;
+};
+
+static size_t bwd_layout(int BH, int T, int K, int V, char *base, BwdScratch *s) {
+    const size_t nsub = ((size_t)T + kBwdSub - 1) / kBwdSub;
+    const size_t sz[6] = {
+        pad256((size_t)BH * nsub * V * K * 4),                                   // ck2
+        pad256((size_t)BH * (V / kBwdRows) * T * bwd_part_width(K) * 4),         // part
+        pad256((size_t)BH * T * K * 4),                                           // dkt_tot
+        pad256((size_t)BH * T * K * 4),                                           // dk2
+        pad256((size_t)BH * T * 4),                                               // db2
+        pad256((size_t)BH * nsub * K * 4),                                        // ck1
+    };
+    size_t off = 0;
+    float **dst[6] = {&s->ck2, &s->part, &s->dkt_tot, &s->dk2, &s->db2, &s->ck1};
+    for (int a = 0; a < 6; ++a) {
+        if (base) *dst[a] = reinterpret_cast<float *>(base + off);
+        off += sz[a];
+    }
+    return off;
+}
+
+size_t backward_scratch_bytes(int BH, int T, int K, int V) {
+    BwdScratch s;
+    return bwd_layout(BH, T, K, V, nullptr, &s);
+}
+
+template <typename io_t, int K>
+static cudaError_t launch_backward(int BH, int T, int V, const void *q, const void *k,
+                                   const void *kt, const void *v, const float *beta,
+                                   const float *r, float eta, const float *d0,
+                                   const float *alpha, const float *S0, const void *dO,
+                                   const float *dST, const float *ddT, const void *dkt_ext,
+                                   void *dq, void *dk, void *dv, float *dbeta, float *dr,
+                                   float *dalpha, float *dd0, float *dS0, float *deta,
+                                   void *scratch, cudaStream_t stream) {
+    static std::atomic<unsigned long long> attr_done{0};
+    BwdScratch s;
+    bwd_layout(BH, T, K, V, static_cast<char *>(scratch), &s);
+    const int nsub = T / kBwdSub + (T % kBwdSub != 0);   // no overflow near INT_MAX
+    const int nrb = V / kBwdRows;
+    const int smem = (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K)) * 4;
+    auto *k1 = state_adjoint_kernel<io_t, K>;
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
+    if (e != cudaSuccess) return e;
+    k1<<<dim3(nrb, BH), kBwdRows * 32, smem, stream>>>(
+        T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
+        static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
+        static_cast<const io_t *>(dO), dST, static_cast<io_t *>(dv), dS0, s.ck2, s.part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    partial_sum_kernel<io_t, K><<<dim3(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
+        T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
+        s.dkt_tot, s.dk2, s.db2);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    precond_adjoint_kernel<io_t, K><<<(BH + kBwdSeqs - 1) / kBwdSeqs, kBwdSeqs * 32, 0, stream>>>(
+        BH, T, nsub, static_cast<const io_t *>(k), beta, r, eta, d0, s.dkt_tot, ddT, s.dk2,
+        s.db2, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.ck1);
+    return cudaGetLastError();
+}
+
+cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
+                            const void *kt, const void *v, const float *beta, const float *r,
+                            float eta, const float *d0, const float *alpha, const float *S0,
+                            const void *dO, const float *dST, const float *ddT,
+                            const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
+                            float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
+                            void *scratch, cudaStream_t stream) {
+#define OSDN_BWD(T_, K_)                                                                      \
+    return launch_backward<T_, K_>(BH, T, V, q, k, kt, v, beta, r, eta, d0, alpha, S0, dO,   \
+                                   dST, ddT, dkt_ext, dq, dk, dv, dbeta, dr, dalpha, dd0,     \
+                                   dS0, deta, scratch, stream)
+    if (io == OSDN_BF16) {
+        if (K == 64) OSDN_BWD(__nv_bfloat16, 64);
+        OSDN_BWD(__nv_bfloat16, 128);
+    }
+    if (K == 64) OSDN_BWD(float, 64);
+    OSDN_BWD(float, 128);
+#undef OSDN_BWD
+}
+
+}  // namespace osdn

@@ -29,6 +29,14 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
                             cudaStream_t stream);
+size_t backward_scratch_bytes(int BH, int T, int K, int V);
+cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
+                            const void *kt, const void *v, const float *beta, const float *r,
+                            float eta, const float *d0, const float *alpha, const float *S0,
+                            const void *dO, const float *dST, const float *ddT,
+                            const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
+                            float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
+                            void *scratch, cudaStream_t stream);
 cudaError_t decode_step_launch(int io, int BH, int K, int V, const void *q, const void *k,
                                const void *v, const float *beta, const float *r, float eta,
                                const float *alpha, float *d, float *S, void *o, void *ktilde,
@@ -100,6 +108,11 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
     if (io != OSDN_BF16 || T == 0) return kStatusBytes;
     // the tensor-core path keeps each chunk's prepared operands in the workspace
     return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K, V);
+}
+
+size_t osdn_backward_workspace_bytes(int B, int H, int T, int K, int V) {
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V) || T == 0) return kStatusBytes;
+    return kStatusBytes + osdn::backward_scratch_bytes(B * H, T, K, V);
 }
 
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
@@ -266,6 +279,56 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
     if (dev != OSDN_OK) return dev;
     cudaError_t e = osdn::decode_step_launch(io, (int)BH, K, V, q, k, v, beta, r, eta, alpha, d, S,
                                              o, ktilde, (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                  const void *ktilde, const void *v, const float *beta, const float *r,
+                  float eta, const float *d0, const float *alpha, const float *S0,
+                  const void *d_o, const float *d_ST, const float *d_dT, const void *d_ktilde,
+                  void *dq, void *dk, void *dv, float *dbeta, float *dr, float *dalpha,
+                  float *dd0, float *dS0, float *deta, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (!workspace) return OSDN_ERR_WORKSPACE;
+    if (workspace_bytes < osdn_backward_workspace_bytes(B, H, T, K, V)) return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (T > 0 && (!q || !k || !ktilde || !v || !beta || !dq || !dk || !dv || !dbeta))
+        return OSDN_ERR_NULL;
+    const void *ins[14] = {q, k, ktilde, v, beta, r, d0, alpha, S0, d_o, d_ST, d_dT, d_ktilde,
+                           workspace};
+    void *outs[9] = {dq, dk, dv, dbeta, dr, dalpha, dd0, dS0, deta};
+    for (const void *p : ins)
+        if (misaligned(p)) return OSDN_ERR_ALIGN;
+    for (const void *p : outs)
+        if (misaligned(p)) return OSDN_ERR_ALIGN;
+    const size_t es = io_bytes(io);
+    const size_t kb = BH * (size_t)T * K * es, vb = BH * (size_t)T * V * es;
+    const size_t gb = BH * (size_t)T * 4, db = BH * (size_t)K * 4, sb = BH * (size_t)V * K * 4;
+    const size_t insz[13] = {kb, kb, kb, vb, gb, gb, db, gb, sb, vb, sb, db, kb};
+    const size_t outsz[9] = {kb, kb, vb, gb, gb, gb, db, sb, BH * 4};
+    for (int a = 0; a < 9; ++a) {
+        for (int i = 0; i < 13; ++i)
+            if (overlap(outs[a], outsz[a], ins[i], insz[i])) return OSDN_ERR_ALIAS;
+        for (int b = a + 1; b < 9; ++b)
+            if (overlap(outs[a], outsz[a], outs[b], outsz[b])) return OSDN_ERR_ALIAS;
+    }
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (T == 0) {
+        e = osdn::fill_state_launch(dS0 ? sb / 4 : 0, d_ST, 0.0f, dS0, st);
+        if (e == cudaSuccess) e = osdn::fill_state_launch(dd0 ? db / 4 : 0, d_dT, 0.0f, dd0, st);
+        if (e == cudaSuccess) e = osdn::fill_state_launch(deta ? BH : 0, nullptr, 0.0f, deta, st);
+    } else {
+        e = osdn::backward_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, r, eta, d0, alpha,
+                                  S0, d_o, d_ST, d_dT, d_ktilde, dq, dk, dv, dbeta, dr, dalpha,
+                                  dd0, dS0, deta, static_cast<char *>(workspace) + kStatusBytes,
+                                  st);
+    }
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

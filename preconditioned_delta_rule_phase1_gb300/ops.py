@@ -1,7 +1,7 @@
 """Thin ctypes binding of ``libosdn.so`` (include/osdn.h).
 
-Argument marshalling only: every step of the forward pass runs in the CUDA
-kernels behind the C ABI.  PyTorch provides device memory and the stream.
+Argument marshalling only: every step of the forward pass and of its
+gradients runs in the CUDA kernels behind the C ABI.  PyTorch provides device memory and the stream.
 There is no CPU path: if the library is not built, or the tensors are not
 on a CUDA device, the calls raise.
 
@@ -46,6 +46,10 @@ _SIGS = {
     "osdn_decode_step": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5 +
                          [ctypes.c_float] + [ctypes.c_void_p] * 6 +
                          [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_backward_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "osdn_backward": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 6 +
+                      [ctypes.c_float] + [ctypes.c_void_p] * 17 +
+                      [ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 
@@ -182,6 +186,10 @@ def chunk_fwd_workspace_bytes(io, B, H, T, K, V) -> int:
     return int(lib().osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V))
 
 
+def backward_workspace_bytes(B, H, T, K, V) -> int:
+    return int(lib().osdn_backward_workspace_bytes(B, H, T, K, V))
+
+
 def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, workspace=None,
                  stream=None, log_ratio=None):
     """Phase 1 (osdn_precond_scan): returns (ktilde, dT).
@@ -310,3 +318,51 @@ def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde
                                       _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream, dev))
     _check(code, "osdn_decode_step")
     return o, ktilde
+
+
+def backward(q, k, ktilde, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, *, do=None,
+             dST=None, ddT=None, dktilde=None, workspace=None, stream=None):
+    """Gradients of both phases (osdn_backward).
+
+    Takes the forward's inputs, the ktilde it produced and the cotangents of
+    its outputs (o, ST, dT, ktilde; None counts as zero).  Returns a dict
+    keyed like the inputs: q, k, v, beta (io / fp32), eta ([B, H]: each
+    sequence's share; the scalar gradient is the sum), and r, alpha, d0, S0
+    for those given (an input given as None has no entry).
+    """
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    io, dev = _io(k), k.device
+    for name, t, shape, dt in (("q", q, (B, H, T, K), k.dtype),
+                               ("ktilde", ktilde, (B, H, T, K), k.dtype),
+                               ("v", v, (B, H, T, V), k.dtype),
+                               ("beta", beta, (B, H, T), F32), ("r", r, (B, H, T), F32),
+                               ("d0", d0, (B, H, K), F32), ("alpha", alpha, (B, H, T), F32),
+                               ("S0", S0, (B, H, V, K), F32), ("do", do, (B, H, T, V), k.dtype),
+                               ("dST", dST, (B, H, V, K), F32), ("ddT", ddT, (B, H, K), F32),
+                               ("dktilde", dktilde, (B, H, T, K), k.dtype)):
+        _expect(name, t, shape, dt, dev)
+    if q is None or ktilde is None or v is None or beta is None:
+        raise ValueError("q, ktilde, v and beta are required")
+    new = lambda *shape, dtype=F32: torch.empty(*shape, dtype=dtype, device=dev)
+    g = {"q": new(B, H, T, K, dtype=k.dtype), "k": new(B, H, T, K, dtype=k.dtype),
+         "v": new(B, H, T, V, dtype=k.dtype), "beta": new(B, H, T), "eta": new(B, H)}
+    if r is not None:
+        g["r"] = new(B, H, T)
+    if alpha is not None:
+        g["alpha"] = new(B, H, T)
+    if d0 is not None:
+        g["d0"] = new(B, H, K)
+    if S0 is not None:
+        g["S0"] = new(B, H, V, K)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        ws.ensure(backward_workspace_bytes(B, H, T, K, V))
+        code = lib().osdn_backward(
+            io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v), _ptr(beta), _ptr(r),
+            float(eta), _ptr(d0), _ptr(alpha), _ptr(S0), _ptr(do), _ptr(dST), _ptr(ddT),
+            _ptr(dktilde), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), _ptr(g["beta"]),
+            _ptr(g.get("r")), _ptr(g.get("alpha")), _ptr(g.get("d0")), _ptr(g.get("S0")),
+            _ptr(g["eta"]), ws.ptr, ws.nbytes, _stream(stream, dev))
+    _check(code, "osdn_backward")
+    return g

@@ -156,3 +156,52 @@ def test_host_validation_decode_step(L):
     assert decode(L, o=FAKE) == -9          # o aliases q
     assert decode(L, S=5 * FAKE) == -9      # S overlaps d
     assert decode(L, H=0) == 0
+
+
+def bwd(L, io=1, B=1, H=1, T=8, K=64, V=64, ins=None, outs=None, ws=40 * FAKE, wsb=None):
+    # inputs q, k, ktilde, v, beta, r, d0, alpha, S0, d_o, d_ST, d_dT, d_ktilde and
+    # outputs dq, dk, dv, dbeta, dr, dalpha, dd0, dS0, deta at disjoint fake addresses
+    a = {n: (i + 1) * FAKE for i, n in enumerate(
+        ["q", "k", "kt", "v", "beta", "r", "d0", "alpha", "S0", "do", "dST", "ddT", "dkt",
+         "dq", "dk", "dv", "dbeta", "dr", "dalpha", "dd0", "dS0", "deta"])}
+    a.update(ins or {})
+    a.update(outs or {})
+    if wsb is None:
+        wsb = L.osdn_backward_workspace_bytes(B, H, T, K, V)
+    return L.osdn_backward(io, B, H, T, K, V, a["q"], a["k"], a["kt"], a["v"], a["beta"], a["r"],
+                           0.1, a["d0"], a["alpha"], a["S0"], a["do"], a["dST"], a["ddT"],
+                           a["dkt"], a["dq"], a["dk"], a["dv"], a["dbeta"], a["dr"], a["dalpha"],
+                           a["dd0"], a["dS0"], a["deta"], ws, wsb, None)
+
+
+def test_host_validation_backward(L):
+    assert bwd(L, io=5) == -3
+    assert bwd(L, K=96) == -2 and bwd(L, V=32) == -2 and bwd(L, T=-3) == -2
+    assert bwd(L, B=256, H=256) == -2
+    assert bwd(L, ws=None) == -5 and bwd(L, wsb=16) == -5
+    need = L.osdn_backward_workspace_bytes(1, 1, 8, 64, 64)
+    assert bwd(L, wsb=need - 1) == -5
+    for n in ("q", "k", "kt", "v", "beta"):
+        assert bwd(L, ins={n: None}) == -1, n
+    for n in ("dq", "dk", "dv", "dbeta"):
+        assert bwd(L, outs={n: None}) == -1, n
+    assert bwd(L, ins={"alpha": 8 * FAKE + 4}) == -4
+    assert bwd(L, outs={"deta": 22 * FAKE + 8}) == -4
+    assert bwd(L, outs={"dq": FAKE}) == -9              # dq aliases q
+    assert bwd(L, outs={"dS0": 11 * FAKE}) == -9        # dS0 aliases the cotangent d_ST
+    assert bwd(L, outs={"dr": 17 * FAKE + 16}) == -9    # dr overlaps dbeta (8 tokens, 32 bytes)
+    assert bwd(L, outs={"dr": 17 * FAKE + 32}) != -9    # ... and starts right after it
+    assert bwd(L, H=0) == 0
+
+
+def test_backward_workspace_size(L):
+    # the state of each value row every 16 tokens, one partial of the row sums
+    # (3K + 2 values a token) per block of 8 rows, Phase 1's inputs and
+    # checkpoints; each array padded to 256 bytes
+    r = lambda x: -(-x // 256) * 256
+    assert L.osdn_backward_workspace_bytes(1, 2, 0, 64, 64) == 256
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (2, 16, 8192, 128, 128)]:
+        BH, ns = B * H, -(-T // 16)
+        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (3 * K + 2) * 4)
+                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
+        assert L.osdn_backward_workspace_bytes(B, H, T, K, V) == want

@@ -63,7 +63,15 @@ def test_valid_calls_pass(fake, io, opts):
     sl = lambda n: None if x[n] is None else x[n][:, :, 0].contiguous()
     ops.decode_step(sl("q"), sl("k"), sl("v"), sl("beta"), d, S, r=sl("r"), eta=x["eta"],
                     alpha=sl("alpha"), workspace=ops.Workspace(device="cpu"))
+    g = ops.backward(x["q"], x["k"], kt, x["v"], x["beta"], x["r"], x["eta"], x["d0"], x["alpha"],
+                     x["S0"], do=torch.zeros(2, 3, 40, 64, dtype=x["k"].dtype),
+                     dST=torch.zeros(2, 3, 64, 128), ddT=torch.zeros(2, 3, 128),
+                     dktilde=torch.zeros_like(kt), workspace=ops.Workspace(device="cpu"))
+    want = {"q", "k", "v", "beta", "eta"} | {n for n in ("r", "alpha", "d0", "S0")
+                                             if x[n] is not None}
+    assert set(g) == want and g["eta"].shape == (2, 3) and g["S0" if "S0" in g else "q"].numel()
     assert "osdn_decode_step" in fake.calls and "osdn_precond_scan_residual" in fake.calls
+    assert "osdn_backward" in fake.calls
 
 
 def test_mistakes_are_refused_before_the_library(fake):
@@ -86,6 +94,11 @@ def test_mistakes_are_refused_before_the_library(fake):
         lambda: ops.decode_step(x["q"][:, :, 0], x["k"][:, :, 0], x["v"][:, :, 0],
                                 x["beta"][:, :, 0], torch.ones(2, 3, 64).double(),
                                 torch.zeros(2, 3, 64, 64), workspace=ws),             # d dtype
+        lambda: ops.backward(x["q"], x["k"], x["k"], x["v"], x["beta"],
+                             do=x["v"].float(), workspace=ws),                       # do dtype
+        lambda: ops.backward(x["q"], x["k"], x["k"], x["v"], x["beta"],
+                             dST=torch.zeros(2, 3, 64, 32), workspace=ws),           # dST shape
+        lambda: ops.backward(x["q"], x["k"], None, x["v"], x["beta"], workspace=ws),  # no ktilde
     ]
     for i, call in enumerate(bad):
         n = len(fake.calls)
