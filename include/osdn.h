@@ -209,7 +209,10 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
  * on two library-owned streams per device (created on first use, forked from
  * and joined back to `stream` with events); the library serialises the
  * enqueue of such calls.
- * With T == 0 the call writes ST = S0 and nothing else.
+ * With T == 0 the call writes ST = S0 and nothing else.  With io ==
+ * OSDN_BF16, T may be at most 1,073,741,760 (the chunk rows of the prepared
+ * operands are addressed with 32-bit TMA coordinates); a longer sequence
+ * returns OSDN_ERR_DIMS (split it and chain the state through S0 / ST).
  * Test hook: with the environment variable OSDN_TEST_STALL_CHAIN set, the
  * bf16 path's state-recurrence kernel loads nothing, so its bounded waits
  * run out (after limits shortened to milliseconds) and the call leaves

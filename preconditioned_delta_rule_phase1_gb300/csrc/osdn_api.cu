@@ -54,6 +54,10 @@ bool dims_ok(int B, int H, int T) {
     return B >= 0 && H >= 0 && T >= 0 && (size_t)B * (size_t)H <= 65535;
 }
 bool width_ok(int x) { return x == 64 || x == 128; }
+// The tensor-core Phase 2 addresses each chunk's rows of its prepared
+// operands (chunk index x K, K <= 128) with 32-bit TMA coordinates and int
+// chunk arithmetic: T is capped so that ceil(T/64) * 128 stays below 2^31.
+constexpr int kMaxTcTokens = (0x7fffffff / 128) * 64;
 size_t io_bytes(int io) { return io == OSDN_BF16 ? 2 : 4; }
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -105,7 +109,7 @@ size_t osdn_precond_scan_workspace_bytes(int B, int H, int T, int K) {
 
 size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V) {
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return kStatusBytes;
-    if (io != OSDN_BF16 || T == 0) return kStatusBytes;
+    if (io != OSDN_BF16 || T == 0 || T > kMaxTcTokens) return kStatusBytes;
     // the tensor-core path keeps each chunk's prepared operands in the workspace
     return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K, V);
 }
@@ -216,6 +220,7 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
                    void *stream) {
     if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (io == OSDN_BF16 && T > kMaxTcTokens) return OSDN_ERR_DIMS;
     if (!workspace) return OSDN_ERR_WORKSPACE;
     if (workspace_bytes < osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V))
         return OSDN_ERR_WORKSPACE;

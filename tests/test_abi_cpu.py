@@ -115,6 +115,13 @@ def test_host_validation_chunk_fwd(L):
     assert chunk(L, wsb=need - 1) == -5
     assert chunk(L, H=0) == 0
     assert chunk(L, B=256, H=256) == -2    # more sequences than the grid holds
+    # the tensor-core path's 32-bit chunk-row coordinates cap T; fp32 I/O has no cap
+    cap = (0x7fffffff // 128) * 64
+    assert chunk(L, T=cap + 1, wsb=1 << 62) == -2
+    assert chunk(L, T=0x7fffffff, wsb=1 << 62) == -2
+    assert chunk(L, io=0, T=cap + 1, wsb=1 << 62) != -2
+    assert L.osdn_chunk_fwd_workspace_bytes(1, 1, 1, cap + 1, 128, 128) == 256
+    assert L.osdn_chunk_fwd_workspace_bytes(1, 1, 1, cap, 128, 128) > 1 << 40
 
 
 def test_chunk_fwd_workspace_size(L):
