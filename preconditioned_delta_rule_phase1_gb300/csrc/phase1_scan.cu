@@ -608,17 +608,18 @@ static cudaError_t launch(const Params &p, cudaStream_t stream) {
 // warm-up would double the work.  Only a retention gate (r != NULL) makes the
 // warm-up converge, so without one there is a single segment per sequence.
 int precond_segments(int BH, int T, bool has_r, int *L_out) {
+    // ceil(a / b) in 64 bits: T may be within a segment of INT_MAX
+    auto cdiv = [](long long a, long long b) { return (a + b - 1) / b; };
     int L = T;
     if (has_r && T > 2 * p1::kWarm) {
         L = 1024;
-        while (L > 2 * p1::kWarm &&
-               (long long)BH * ((T + L / 2 - 1) / (L / 2)) <= 8LL * p1::kSmCount)
+        while (L > 2 * p1::kWarm && (long long)BH * cdiv(T, L / 2) <= 8LL * p1::kSmCount)
             L >>= 1;
         if (L >= T) L = T;
     }
     if (L < 1) L = 1;
     if (L_out) *L_out = L;
-    return (T + L - 1) / L;
+    return (int)cdiv(T, L);
 }
 
 // Scratch of the segmented scan: segment starts and ends [n][K] fp32, then
