@@ -523,6 +523,69 @@ def run_decode(args, local_rank):
         "gpu_launches": args.steps}), flush=True)
 
 
+def backward_bytes(w, x):
+    """Algorithmic HBM bytes of one backward pass: read q, k, ktilde, v and
+    the output cotangent dO, the gates and S0; write dq, dk, dv, the gate
+    gradients, dS0, dd0 and deta."""
+    BH, T, K, V, e = w.B * w.H, w.T, w.K, w.V, io_bytes(w)
+    gates = 1 + (x["r"] is not None) + (x["alpha"] is not None)
+    b = BH * T * ((3 * K + 2 * V) * e + 4 * gates)          # inputs, dO
+    b += BH * T * ((2 * K + V) * e + 4 * gates)              # dq, dk, dv, gate gradients
+    b += BH * V * K * 4 * (2 if x["S0"] is not None else 0)  # S0, dS0
+    b += BH * K * 4 * (2 if x["d0"] is not None else 0) + BH * 4
+    return b
+
+
+def run_backward(args, local_rank):
+    """--backward: the gradients of both phases (osdn_backward) at the
+    workload's shape, with the output cotangent dO given.  The forward runs
+    once, untimed, for ktilde.  Inputs are larger than L2, so no flush is
+    needed between steps; one JSON line with the pass's HBM roofline."""
+    from preconditioned_delta_rule_phase1_gb300 import ops
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    gen = torch.Generator().manual_seed(1)
+    dO = torch.randn(w.B, w.H, w.T, w.V, generator=gen).to(g["v"].dtype).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = ops.Workspace(device=dev)
+    kt, _ = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], workspace=ws,
+                             stream=stream)
+    step = lambda: ops.backward(g["q"], g["k"], kt, g["v"], g["beta"], g["r"], g["eta"], g["d0"],
+                                g["alpha"], g["S0"], do=dO, workspace=ws, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(gpu_smi_id(dev, local_rank))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    assert ws.status(stream) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = backward_bytes(w, x)
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "OSDN backward tokens/s (gradients of phase1+2)",
+        "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": w.io, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.K, "d_v": w.V,
+                   "l2": "inputs larger than L2"},
+        "roofline": {"kernel": "osdn_backward (3 kernels)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "algorithmic_bytes": nbytes,
+                     "peak_source": peak_src, "traffic": None},
+        "clocks": clk, "gpu_launches": 3 * args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,12 +596,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time the recurrent decode step instead of the forward pass")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the gradients of both phases instead of the forward pass")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, world, local_rank = env_rank()
     if args.decode:
         run_decode(args, local_rank)
+        return
+    if args.backward:
+        run_backward(args, local_rank)
         return
     if world > 1:
         torch.distributed.init_process_group("gloo")
