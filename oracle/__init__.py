@@ -64,6 +64,8 @@ def _load():
                                                                  _dp, _dp, _dp, _dp, ctypes.c_int]
         lib.oracle_delta_fwd.restype = ctypes.c_int
         lib.oracle_delta_fwd.argtypes = [ctypes.c_int] * 5 + [_dp] * 9 + [ctypes.c_int]
+        lib.oracle_delta_fwd_kda.restype = ctypes.c_int
+        lib.oracle_delta_fwd_kda.argtypes = [ctypes.c_int] * 5 + [_dp] * 9 + [ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -133,6 +135,41 @@ def delta_fwd(q, k, ktilde, v, beta, alpha=None, S0=None, nthreads=None):
     if rc != 0:
         raise RuntimeError("oracle_delta_fwd failed (%d)" % rc)
     return o, ST
+
+
+def delta_fwd_kda(q, k, ktilde, v, beta, alpha_k=None, S0=None, nthreads=None):
+    """Phase 2 with a per-channel decay (the Kimi-Delta-Attention-style gate):
+    S_t = S_{t-1} Diag(alpha_t) + beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) ktilde_t^T.
+
+    alpha_k [B,H,T,K] (None: no decay) and S0 [B,H,V,K] are optional.
+    Returns o [B,H,T,V] and S_T [B,H,V,K].
+    """
+    q, k, ktilde, v = _f64(q), _f64(k), _f64(ktilde), _f64(v)
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    beta, alpha_k, S0 = _f64(beta), _f64(alpha_k), _f64(S0)
+    assert q.shape == k.shape == ktilde.shape and v.shape == (B, H, T, V)
+    assert beta.shape == (B, H, T)
+    assert alpha_k is None or alpha_k.shape == (B, H, T, K)
+    assert S0 is None or S0.shape == (B, H, V, K)
+    o = np.empty((B, H, T, V))
+    ST = np.empty((B, H, V, K))
+    rc = _load().oracle_delta_fwd_kda(B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v),
+                                      _ptr(beta), _ptr(alpha_k), _ptr(S0), _ptr(o), _ptr(ST),
+                                      int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_delta_fwd_kda failed (%d)" % rc)
+    return o, ST
+
+
+def forward_kda(q, k, v, beta, r=None, eta=0.1, d0=None, alpha_k=None, S0=None, nthreads=None):
+    """Both phases with the per-channel decay in Phase 2 (Phase 1 unchanged).
+
+    Returns (ktilde, dT, o, ST).
+    """
+    kt, dT = precond_scan(k, beta, r, eta, d0, nthreads)
+    o, ST = delta_fwd_kda(q, k, kt, v, beta, alpha_k, S0, nthreads)
+    return kt, dT, o, ST
 
 
 def forward(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, nthreads=None):

@@ -13,6 +13,8 @@ Preconditioning in Linear Attention", gist.science summary, sections 2.1,
     d_{t+1}  = r_t d_t + eta beta_t (1 - beta_t <d_t, k_t^2>) k_t^2 / ||k_t||^2
                (no step for a zero key)
     S_t      = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) ktilde_t^T
+               (or, with a decay per key channel, S_{t-1} Diag(alpha_t) in
+               place of alpha_t S_{t-1})
     o_t      = S_t q_t
 
 and differentiates it with ``torch.autograd``: the gradients of a training
@@ -41,7 +43,10 @@ def _t(x, requires_grad=False):
 def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None):
     """Both phases, token by token, in float64 torch ops (differentiable).
 
-    Shapes as in ``oracle.forward``; returns (ktilde, dT, o, ST).
+    Shapes as in ``oracle.forward``; alpha may also be [B, H, T, K], a decay
+    per key channel (``oracle.forward_kda``): S_t = S_{t-1} Diag(alpha_t) +
+    beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) ktilde_t^T.  Returns (ktilde, dT,
+    o, ST).
     """
     B, H, T, K = k.shape
     V = v.shape[-1]
@@ -59,10 +64,15 @@ def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None):
         coef = torch.where(n > 0, eta * bt * (1.0 - bt * a) / safe_n, torch.zeros_like(n))
         rt = r[:, :, t] if r is not None else torch.ones_like(bt)
         d = rt[..., None] * d + coef[..., None] * w         # descent step on h_t
-        at = alpha[:, :, t] if alpha is not None else torch.ones_like(bt)
-        Sk = torch.einsum("bhvk,bhk->bhv", S, kt)           # S_{t-1} k_t
-        u = bt[..., None] * (v[:, :, t] - at[..., None] * Sk)
-        S = at[..., None, None] * S + u[..., :, None] * ktil[..., None, :]
+        if alpha is None:
+            Sbar = S
+        elif alpha.dim() == 4:                               # per key channel
+            Sbar = S * alpha[:, :, t][..., None, :]
+        else:
+            Sbar = alpha[:, :, t][..., None, None] * S
+        Sk = torch.einsum("bhvk,bhk->bhv", Sbar, kt)        # alpha_t S_{t-1} k_t
+        u = bt[..., None] * (v[:, :, t] - Sk)
+        S = Sbar + u[..., :, None] * ktil[..., None, :]
         outs.append(torch.einsum("bhvk,bhk->bhv", S, q[:, :, t]))   # read-out after the write
         kts.append(ktil)
     return torch.stack(kts, 2), d, torch.stack(outs, 2), S

@@ -33,12 +33,18 @@
  *  - the optional per-token decay alpha_t (a Gated-DeltaNet-style gate; the
  *    pages name the GDN backbone in section 4 but print no formula) enters as
  *    S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) ktilde_t^T;
+ *  - the optional per-channel decay alpha_t in R^K (the Kimi Delta Attention
+ *    backbone that section 4 names, with no formula printed: a decay per key
+ *    channel in place of GDN's scalar) scales the key columns of the state,
+ *    S_t = S_{t-1} Diag(alpha_t) + beta_t (v_t - S_{t-1} Diag(alpha_t) k_t)
+ *    ktilde_t^T; with all channels equal it is the scalar gate above;
  *  - the output is o_t = S_t q_t, read from the state after token t, with no
  *    scale on q.
  *
  * Layouts (row-major, all fp64 here):
  *   q, k, ktilde : [B][H][T][K]      v, o : [B][H][T][V]
  *   beta, r, alpha : [B][H][T]       d0, dT : [B][H][K]
+ *   alpha_k (per-channel decay) : [B][H][T][K]
  *   S0, ST : [B][H][V][K]  (S[i][j]: i = value row, j = key column)
  */
 #include <math.h>
@@ -98,8 +104,8 @@ static void phase1_sequence(int T, int K, const double *k, const double *beta,
 /* ---------------------------------------------------------------------- */
 static void phase2_sequence(int T, int K, int V, const double *q, const double *k,
                             const double *ktilde, const double *v, const double *beta,
-                            const double *alpha, const double *S0, double *o,
-                            double *ST, double *S /* V*K scratch */)
+                            const double *alpha, const double *alpha_k, const double *S0,
+                            double *o, double *ST, double *S /* V*K scratch */)
 {
     for (size_t i = 0; i < (size_t)V * K; ++i) S[i] = S0 ? S0[i] : 0.0;
     for (int t = 0; t < T; ++t) {
@@ -107,14 +113,16 @@ static void phase2_sequence(int T, int K, int V, const double *q, const double *
         const double *kt = k + (size_t)t * K;
         const double *kk = ktilde + (size_t)t * K;
         const double *vt = v + (size_t)t * V;
+        const double *akt = alpha_k ? alpha_k + (size_t)t * K : NULL;
         double at = alpha ? alpha[t] : 1.0;
         double bt = beta[t];
         for (int i = 0; i < V; ++i) {
             double *Si = S + (size_t)i * K;
-            /* decayed state row, then its prediction for k_t */
+            /* decayed state row (per channel, or one scalar), then its
+               prediction for k_t */
             double pred = 0.0;
             for (int j = 0; j < K; ++j) {
-                Si[j] *= at;
+                Si[j] *= akt ? akt[j] : at;
                 pred += Si[j] * kt[j];
             }
             /* u = beta (v - S k): the scaled residual of f_t */
@@ -138,7 +146,7 @@ typedef struct {
     int which; /* 1 = phase 1, 2 = phase 2 */
     int first, last;
     int T, K, V;
-    const double *q, *k, *ktilde_in, *v, *beta, *r, *alpha, *d0, *S0;
+    const double *q, *k, *ktilde_in, *v, *beta, *r, *alpha, *alpha_k, *d0, *S0;
     double eta;
     double *ktilde, *dT, *o, *ST, *logratio;
     int failed;
@@ -164,6 +172,7 @@ static void *run_job(void *arg)
             phase2_sequence(jb->T, jb->K, jb->V, jb->q + s * T * K, jb->k + s * T * K,
                             jb->ktilde_in + s * T * K, jb->v + s * T * V, jb->beta + s * T,
                             jb->alpha ? jb->alpha + s * T : NULL,
+                            jb->alpha_k ? jb->alpha_k + s * T * K : NULL,
                             jb->S0 ? jb->S0 + s * V * K : NULL, jb->o + s * T * V,
                             jb->ST ? jb->ST + s * V * K : NULL, scratch);
         }
@@ -259,6 +268,37 @@ int oracle_delta_fwd(int B, int H, int T, int K, int V, const double *q, const d
     p.v = v;
     p.beta = beta;
     p.alpha = alpha;
+    p.S0 = S0;
+    p.o = o;
+    p.ST = ST;
+    return run_threads(&p, B * H, nthreads);
+}
+
+/* Phase 2 with a per-channel decay alpha_k [B][H][T][K] (NULL: no decay)
+ * over B*H sequences.  S0, ST may be NULL. */
+int oracle_delta_fwd_kda(int B, int H, int T, int K, int V, const double *q, const double *k,
+                         const double *ktilde, const double *v, const double *beta,
+                         const double *alpha_k, const double *S0, double *o, double *ST,
+                         int nthreads)
+{
+    if (B < 1 || H < 1 || T < 0 || K < 1 || V < 1) return -1;
+    if (T > 0 && (!q || !k || !ktilde || !v || !beta || !o)) return -1;
+    if (T == 0) {
+        for (size_t i = 0; ST && i < (size_t)B * H * V * K; ++i) ST[i] = S0 ? S0[i] : 0.0;
+        return 0;
+    }
+    job_t p;
+    memset(&p, 0, sizeof(p));
+    p.which = 2;
+    p.T = T;
+    p.K = K;
+    p.V = V;
+    p.q = q;
+    p.k = k;
+    p.ktilde_in = ktilde;
+    p.v = v;
+    p.beta = beta;
+    p.alpha_k = alpha_k;
     p.S0 = S0;
     p.o = o;
     p.ST = ST;
