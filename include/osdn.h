@@ -16,8 +16,10 @@
  *
  * Around them: osdn_precond_scan_residual (Phase 1 plus the per-sequence
  * log of the residual ratios, section 3 and section 4.2), osdn_decode_step
- * (both phases at T = 1, in place, for inference) and osdn_backward (the
- * gradients of both phases, for training).
+ * (both phases at T = 1, in place, for inference), osdn_backward (the
+ * gradients of both phases, for training), and osdn_chunk_fwd_kda /
+ * osdn_backward_kda (Phase 2 and the gradients with a decay per key channel,
+ * the Kimi-Delta-Attention-style backbone of section 4).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -296,6 +298,46 @@ int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, cons
                   void *dq, void *dk, void *dv, float *dbeta, float *dr, float *dalpha,
                   float *dd0, float *dS0, float *deta, void *workspace, size_t workspace_bytes,
                   void *stream);
+
+/*
+ * Phase 2 with a decay per key channel: the Kimi Delta Attention backbone
+ * named in section 4 (no formula printed there), read as GDN's scalar gate
+ * made a K-vector that scales the key columns of the state:
+ *     S_t = S_{t-1} Diag(alpha_t) + beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) ktilde_t^T
+ *     o_t = S_t q_t
+ * Phase 1 (osdn_precond_scan) is unchanged and produces ktilde.
+ *
+ *   q, k, ktilde in [B][H][T][K] io;  v in [B][H][T][V] io
+ *   beta         in [B][H][T] fp32
+ *   alpha_k      in [B][H][T][K] fp32, or NULL (no decay)
+ *   S0           in [B][H][V][K] fp32, or NULL (zeros)
+ *   o            out [B][H][T][V] io;  ST out [B][H][V][K] fp32, or NULL
+ * Both I/O types run the token recurrence in fp32 FFMA, one CTA per 32
+ * value rows.  With T == 0 the call writes ST = S0.  Outputs must not
+ * overlap inputs (OSDN_ERR_ALIAS).
+ */
+size_t osdn_chunk_fwd_kda_workspace_bytes(int io, int B, int H, int T, int K, int V);
+int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                       const void *ktilde, const void *v, const float *beta,
+                       const float *alpha_k, const float *S0, void *o, float *ST,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * osdn_backward for the per-channel decay of osdn_chunk_fwd_kda: the same
+ * arguments and outputs, with alpha_k [B][H][T][K] fp32 (or NULL) in place
+ * of alpha and dalpha_k [B][H][T][K] fp32 (or NULL) in place of dalpha.
+ * Its workspace holds K + 1 rather than 2 values of dalpha and dbeta per
+ * token in each row-block partial: 4 B*H*(V/8)*T*(4K+1) bytes instead of
+ * 4 B*H*(V/8)*T*(3K+2), the rest as osdn_backward_workspace_bytes.
+ */
+size_t osdn_backward_kda_workspace_bytes(int B, int H, int T, int K, int V);
+int osdn_backward_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                      const void *ktilde, const void *v, const float *beta, const float *r,
+                      float eta, const float *d0, const float *alpha_k, const float *S0,
+                      const void *d_o, const float *d_ST, const float *d_dT,
+                      const void *d_ktilde, void *dq, void *dk, void *dv, float *dbeta,
+                      float *dr, float *dalpha_k, float *dd0, float *dS0, float *deta,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /* Zero the 256-byte status area at the start of a workspace (async). */
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);

@@ -27,6 +27,10 @@
 //         dalpha_t += <dSbar, S_{t-1}[i]>      (e = v - alpha S_{t-1} k)
 //     which the CTA adds over its 8 rows in warp order and writes as one
 //     partial per row block (no atomics: the result is deterministic).
+//     With a decay per key channel (alpha_t in R^K scaling the key columns
+//     of S, the Kimi-Delta-Attention-style backbone) the same sweep runs with
+//     Diag(alpha_t) in place of alpha_t, and dalpha_t is a K-vector:
+//     dalpha_t[j] += dSbar[i,j] S_{t-1}[i,j].
 //  2. partial_sum_kernel -- adds the row-block partials in a fixed order:
 //     dq and dalpha are final; dktilde (plus the caller's cotangent of the
 //     ktilde output), Phase 2's share of dk and of dbeta go to scratch.
@@ -52,10 +56,16 @@ constexpr int kBwdRows = 8;    // value rows (one warp each) per state-adjoint C
 constexpr int kBwdSeqs = 4;    // sequences (one warp each) per precond-adjoint CTA
 constexpr int kSumTok = 8;     // tokens per partial-sum CTA
 
-__host__ __device__ constexpr int bwd_part_width(int K) { return 3 * K + 2; }
+// Values a token contributes per row block: dq, dktilde, dk (K each), dbeta,
+// then dalpha (1 value, or K with a decay per key channel).
+__host__ __device__ constexpr int bwd_part_width(int K, bool pch = false) {
+    return 3 * K + 1 + (pch ? K : 1);
+}
 // row stride of the shared reduction buffer: a multiple of 4 floats keeps the
 // vector stores into it 16-byte aligned
-__host__ __device__ constexpr int bwd_red_stride(int K) { return (bwd_part_width(K) + 3) & ~3; }
+__host__ __device__ constexpr int bwd_red_stride(int K, bool pch = false) {
+    return (bwd_part_width(K, pch) + 3) & ~3;
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -81,8 +91,37 @@ __device__ __forceinline__ void store_cols(T *p, const float (&x)[NC]) {
     if constexpr (NC == 4) store4(p, x); else store2(p, x);
 }
 
+// The decay of token g for this lane's NC columns: alpha[g] for every
+// column (a scalar gate), alpha[g*K + c0 ..] (a decay per key channel), or 1.
+template <bool PCH, int NC>
+__device__ __forceinline__ void decay_cols(const float *alpha, size_t g, int K, int c0,
+                                           float (&a)[NC]) {
+    if (!alpha) {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) a[m] = 1.0f;
+    } else if constexpr (PCH) {
+        load_cols<NC>(alpha + g * K + c0, a);
+    } else {
+        const float s = alpha[g];
+#pragma unroll
+        for (int m = 0; m < NC; ++m) a[m] = s;
+    }
+}
+
+// The row's prediction <Diag(a) S_{t-1}[i], k_t>, reduced over the warp.  A
+// scalar gate multiplies after the reduction, a per-channel decay before it.
+template <bool PCH, int NC>
+__device__ __forceinline__ float decayed_pred(const float (&S)[NC], const float (&a)[NC],
+                                              const float (&kc)[NC]) {
+    float sk = 0.0f;
+#pragma unroll
+    for (int m = 0; m < NC; ++m) sk = fmaf(PCH ? a[m] * S[m] : S[m], kc[m], sk);
+    sk = warp_sum(sk);
+    return PCH ? sk : a[0] * sk;
+}
+
 // ---------------------------------------------------------------- kernel 1
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(kBwdRows * 32)
 state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
                      const io_t *__restrict__ k, const io_t *__restrict__ kt,
@@ -92,8 +131,8 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
                      io_t *__restrict__ dv, float *__restrict__ dS0, float *__restrict__ ck,
                      float *__restrict__ part) {
     constexpr int NC = K / 32;
-    constexpr int P = bwd_part_width(K);
-    constexpr int PS = bwd_red_stride(K);
+    constexpr int P = bwd_part_width(K, PCH);
+    constexpr int PS = bwd_red_stride(K, PCH);
     extern __shared__ __align__(16) float smem[];
     float *Sp = smem;                                  // [kBwdRows][kBwdSub][K]
     float *red = smem + kBwdRows * kBwdSub * K;        // [2][kBwdRows][PS]
@@ -117,17 +156,14 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
     for (int t = 0; t < T; ++t) {
         if (t % kBwdSub == 0)
             store_cols<NC>(ck + ((seq * nsub + t / kBwdSub) * V + i) * (size_t)K + c0, S);
-        float kc[NC], tc[NC];
+        float kc[NC], tc[NC], a[NC];
         load_cols<NC>(k + (tok0 + t) * K + c0, kc);
         load_cols<NC>(kt + (tok0 + t) * K + c0, tc);
-        const float a = alpha ? alpha[tok0 + t] : 1.0f;
-        float sk = 0.0f;
+        decay_cols<PCH, NC>(alpha, tok0 + t, K, c0, a);
+        const float u = beta[tok0 + t] * (to_f32(v[(tok0 + t) * V + i]) -
+                                          decayed_pred<PCH, NC>(S, a, kc));
 #pragma unroll
-        for (int m = 0; m < NC; ++m) sk = fmaf(S[m], kc[m], sk);
-        sk = warp_sum(sk);
-        const float u = beta[tok0 + t] * (to_f32(v[(tok0 + t) * V + i]) - a * sk);
-#pragma unroll
-        for (int m = 0; m < NC; ++m) S[m] = fmaf(a, S[m], u * tc[m]);
+        for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
     }
 
     // reverse sweep
@@ -149,31 +185,27 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
         for (int tt = 0; tt < tn; ++tt) {
             const size_t g = tok0 + t0 + tt;
             store_cols<NC>(Spw + tt * K + c0, S);
-            float kc[NC], tc[NC];
+            float kc[NC], tc[NC], a[NC];
             load_cols<NC>(k + g * K + c0, kc);
             load_cols<NC>(kt + g * K + c0, tc);
-            const float a = alpha ? alpha[g] : 1.0f;
-            float sk = 0.0f;
-#pragma unroll
-            for (int m = 0; m < NC; ++m) sk = fmaf(S[m], kc[m], sk);
-            sk = warp_sum(sk);
-            const float e = to_f32(v[g * V + i]) - a * sk;
+            decay_cols<PCH, NC>(alpha, g, K, c0, a);
+            const float e = to_f32(v[g * V + i]) - decayed_pred<PCH, NC>(S, a, kc);
             const float u = beta[g] * e;
             if (lane == tt) { my_e = e; my_u = u; }
 #pragma unroll
-            for (int m = 0; m < NC; ++m) S[m] = fmaf(a, S[m], u * tc[m]);
+            for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
         }
         // walk it backwards (each lane reads back only its own columns of Spw)
         for (int tt = tn - 1; tt >= 0; --tt) {
             const size_t g = tok0 + t0 + tt;
             const float e = __shfl_sync(kFullMask, my_e, tt);
             const float u = __shfl_sync(kFullMask, my_u, tt);
-            float sp[NC], qc[NC], kc[NC], tc[NC];
+            float sp[NC], qc[NC], kc[NC], tc[NC], a[NC];
             load_cols<NC>(Spw + tt * K + c0, sp);
             load_cols<NC>(q + g * K + c0, qc);
             load_cols<NC>(k + g * K + c0, kc);
             load_cols<NC>(kt + g * K + c0, tc);
-            const float a = alpha ? alpha[g] : 1.0f;
+            decay_cols<PCH, NC>(alpha, g, K, c0, a);
             const float b = beta[g];
             const float dOi = dO ? to_f32(dO[g * V + i]) : 0.0f;
             float du = 0.0f;
@@ -183,31 +215,39 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
                 du = fmaf(G[m], tc[m], du);
             }
             du = warp_sum(du);
-            float dSb[NC], dal = 0.0f;
+            float dSb[NC];
 #pragma unroll
-            for (int m = 0; m < NC; ++m) {
-                dSb[m] = G[m] - b * du * kc[m];
-                dal = fmaf(dSb[m], sp[m], dal);
-            }
-            dal = warp_sum(dal);
+            for (int m = 0; m < NC; ++m) dSb[m] = G[m] - b * du * kc[m];
             float *rw = red + (buf * kBwdRows + warp) * PS;
             float cq[NC], ct[NC], ck_[NC];
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
-                cq[m] = dOi * fmaf(a, sp[m], u * tc[m]);   // dO_t[i] S_t[i]
-                ct[m] = u * G[m];                          // u_t[i] G
-                ck_[m] = -b * du * a * sp[m];              // -beta du alpha S_{t-1}[i]
+                cq[m] = dOi * fmaf(a[m], sp[m], u * tc[m]);   // dO_t[i] S_t[i]
+                ct[m] = u * G[m];                             // u_t[i] G
+                ck_[m] = -b * du * a[m] * sp[m];              // -beta du Sbar[i]
             }
             store_cols<NC>(rw + c0, cq);
             store_cols<NC>(rw + K + c0, ct);
             store_cols<NC>(rw + 2 * K + c0, ck_);
+            // dalpha = <dSbar, S_{t-1}[i]>: per key column with a per-channel
+            // decay (scalar stores: the columns start at the odd offset 3K + 1),
+            // else summed over the row
+            if constexpr (PCH) {
+#pragma unroll
+                for (int m = 0; m < NC; ++m) rw[3 * K + 1 + c0 + m] = dSb[m] * sp[m];
+            } else {
+                float dal = 0.0f;
+#pragma unroll
+                for (int m = 0; m < NC; ++m) dal = fmaf(dSb[m], sp[m], dal);
+                dal = warp_sum(dal);
+                if (lane == 0) rw[3 * K + 1] = dal;
+            }
             if (lane == 0) {
                 rw[3 * K] = du * e;
-                rw[3 * K + 1] = dal;
                 from_f32(dv[g * V + i], b * du);
             }
 #pragma unroll
-            for (int m = 0; m < NC; ++m) G[m] = a * dSb[m];
+            for (int m = 0; m < NC; ++m) G[m] = a[m] * dSb[m];
             __syncthreads();
             // the CTA's sum over its rows, in warp order; the next token
             // writes the other buffer, and its barrier orders these reads
@@ -227,13 +267,13 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
 }
 
 // ---------------------------------------------------------------- kernel 2
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(256)
 partial_sum_kernel(int T, int nrb, const float *__restrict__ part,
                    const io_t *__restrict__ dkt_ext, io_t *__restrict__ dq,
                    float *__restrict__ dalpha, float *__restrict__ dkt_tot,
                    float *__restrict__ dk2, float *__restrict__ db2) {
-    constexpr int P = bwd_part_width(K);
+    constexpr int P = bwd_part_width(K, PCH);
     const size_t seq = blockIdx.y;
     const int tb = blockIdx.x * kSumTok;
     for (int x = threadIdx.x; x < kSumTok * P; x += blockDim.x) {
@@ -253,7 +293,8 @@ partial_sum_kernel(int T, int nrb, const float *__restrict__ part,
         } else if (col == 3 * K) {
             db2[g] = s;
         } else if (dalpha) {
-            dalpha[g] = s;
+            if constexpr (PCH) dalpha[g * K + col - 3 * K - 1] = s;
+            else dalpha[g] = s;
         }
     }
 }
@@ -391,11 +432,11 @@ struct BwdScratch {
     float *ck2, *part, *dkt_tot, *dk2, *db2, *ck1;
 };
 
-static size_t bwd_layout(int BH, int T, int K, int V, char *base, BwdScratch *s) {
+static size_t bwd_layout(int BH, int T, int K, int V, bool pch, char *base, BwdScratch *s) {
     const size_t nsub = ((size_t)T + kBwdSub - 1) / kBwdSub;
     const size_t sz[6] = {
         pad256((size_t)BH * nsub * V * K * 4),                                   // ck2
-        pad256((size_t)BH * (V / kBwdRows) * T * bwd_part_width(K) * 4),         // part
+        pad256((size_t)BH * (V / kBwdRows) * T * bwd_part_width(K, pch) * 4),    // part
         pad256((size_t)BH * T * K * 4),                                           // dkt_tot
         pad256((size_t)BH * T * K * 4),                                           // dk2
         pad256((size_t)BH * T * 4),                                               // db2
@@ -410,12 +451,12 @@ static size_t bwd_layout(int BH, int T, int K, int V, char *base, BwdScratch *s)
     return off;
 }
 
-size_t backward_scratch_bytes(int BH, int T, int K, int V) {
+size_t backward_scratch_bytes(int BH, int T, int K, int V, bool per_channel) {
     BwdScratch s;
-    return bwd_layout(BH, T, K, V, nullptr, &s);
+    return bwd_layout(BH, T, K, V, per_channel, nullptr, &s);
 }
 
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH>
 static cudaError_t launch_backward(int BH, int T, int V, const void *q, const void *k,
                                    const void *kt, const void *v, const float *beta,
                                    const float *r, float eta, const float *d0,
@@ -426,11 +467,11 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
                                    void *scratch, cudaStream_t stream) {
     static std::atomic<unsigned long long> attr_done{0};
     BwdScratch s;
-    bwd_layout(BH, T, K, V, static_cast<char *>(scratch), &s);
+    bwd_layout(BH, T, K, V, PCH, static_cast<char *>(scratch), &s);
     const int nsub = T / kBwdSub + (T % kBwdSub != 0);   // no overflow near INT_MAX
     const int nrb = V / kBwdRows;
-    const int smem = (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K)) * 4;
-    auto *k1 = state_adjoint_kernel<io_t, K>;
+    const int smem = (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4;
+    auto *k1 = state_adjoint_kernel<io_t, K, PCH>;
     cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
     if (e != cudaSuccess) return e;
     k1<<<dim3(nrb, BH), kBwdRows * 32, smem, stream>>>(
@@ -438,7 +479,7 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
         static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
         static_cast<const io_t *>(dO), dST, static_cast<io_t *>(dv), dS0, s.ck2, s.part);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    partial_sum_kernel<io_t, K><<<dim3(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
+    partial_sum_kernel<io_t, K, PCH><<<dim3(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
         T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
         s.dkt_tot, s.dk2, s.db2);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -454,17 +495,23 @@ cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, 
                             const void *dO, const float *dST, const float *ddT,
                             const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
                             float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
-                            void *scratch, cudaStream_t stream) {
-#define OSDN_BWD(T_, K_)                                                                      \
-    return launch_backward<T_, K_>(BH, T, V, q, k, kt, v, beta, r, eta, d0, alpha, S0, dO,   \
-                                   dST, ddT, dkt_ext, dq, dk, dv, dbeta, dr, dalpha, dd0,     \
-                                   dS0, deta, scratch, stream)
+                            bool per_channel, void *scratch, cudaStream_t stream) {
+#define OSDN_BWD(T_, K_, P_)                                                                  \
+    return launch_backward<T_, K_, P_>(BH, T, V, q, k, kt, v, beta, r, eta, d0, alpha, S0,   \
+                                       dO, dST, ddT, dkt_ext, dq, dk, dv, dbeta, dr, dalpha, \
+                                       dd0, dS0, deta, scratch, stream)
+#define OSDN_BWD_K(T_, P_)          \
+    do {                            \
+        if (K == 64) OSDN_BWD(T_, 64, P_); \
+        OSDN_BWD(T_, 128, P_);      \
+    } while (0)
     if (io == OSDN_BF16) {
-        if (K == 64) OSDN_BWD(__nv_bfloat16, 64);
-        OSDN_BWD(__nv_bfloat16, 128);
+        if (per_channel) OSDN_BWD_K(__nv_bfloat16, true);
+        OSDN_BWD_K(__nv_bfloat16, false);
     }
-    if (K == 64) OSDN_BWD(float, 64);
-    OSDN_BWD(float, 128);
+    if (per_channel) OSDN_BWD_K(float, true);
+    OSDN_BWD_K(float, false);
+#undef OSDN_BWD_K
 #undef OSDN_BWD
 }
 

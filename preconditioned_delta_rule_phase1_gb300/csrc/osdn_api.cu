@@ -29,14 +29,18 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
                             cudaStream_t stream);
-size_t backward_scratch_bytes(int BH, int T, int K, int V);
+size_t backward_scratch_bytes(int BH, int T, int K, int V, bool per_channel);
 cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, const void *k,
                             const void *kt, const void *v, const float *beta, const float *r,
                             float eta, const float *d0, const float *alpha, const float *S0,
                             const void *dO, const float *dST, const float *ddT,
                             const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
                             float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
-                            void *scratch, cudaStream_t stream);
+                            bool per_channel, void *scratch, cudaStream_t stream);
+cudaError_t delta_simt_kda_launch(int io, int BH, int T, int K, int V, const void *q,
+                                  const void *k, const void *kt, const void *v,
+                                  const float *beta, const float *alpha_k, const float *S0,
+                                  void *o, float *ST, cudaStream_t stream);
 cudaError_t decode_step_launch(int io, int BH, int K, int V, const void *q, const void *k,
                                const void *v, const float *beta, const float *r, float eta,
                                const float *alpha, float *d, float *S, void *o, void *ktilde,
@@ -116,7 +120,17 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
 
 size_t osdn_backward_workspace_bytes(int B, int H, int T, int K, int V) {
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V) || T == 0) return kStatusBytes;
-    return kStatusBytes + osdn::backward_scratch_bytes(B * H, T, K, V);
+    return kStatusBytes + osdn::backward_scratch_bytes(B * H, T, K, V, false);
+}
+
+size_t osdn_backward_kda_workspace_bytes(int B, int H, int T, int K, int V) {
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V) || T == 0) return kStatusBytes;
+    return kStatusBytes + osdn::backward_scratch_bytes(B * H, T, K, V, true);
+}
+
+size_t osdn_chunk_fwd_kda_workspace_bytes(int io, int B, int H, int T, int K, int V) {
+    (void)io; (void)B; (void)H; (void)T; (void)K; (void)V;
+    return kStatusBytes;   // the fp32 FFMA recurrence needs no scratch
 }
 
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
@@ -287,17 +301,25 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 
-int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
-                  const void *ktilde, const void *v, const float *beta, const float *r,
-                  float eta, const float *d0, const float *alpha, const float *S0,
-                  const void *d_o, const float *d_ST, const float *d_dT, const void *d_ktilde,
-                  void *dq, void *dk, void *dv, float *dbeta, float *dr, float *dalpha,
-                  float *dd0, float *dS0, float *deta, void *workspace, size_t workspace_bytes,
-                  void *stream) {
+}  // extern "C"
+
+namespace {
+
+// osdn_backward and osdn_backward_kda: one validation, one launch.  With a
+// per-channel decay alpha and dalpha are [B][H][T][K], else [B][H][T].
+int backward_checked(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                     const void *ktilde, const void *v, const float *beta, const float *r,
+                     float eta, const float *d0, const float *alpha, const float *S0,
+                     const void *d_o, const float *d_ST, const float *d_dT,
+                     const void *d_ktilde, void *dq, void *dk, void *dv, float *dbeta, float *dr,
+                     float *dalpha, float *dd0, float *dS0, float *deta, bool per_channel,
+                     void *workspace, size_t workspace_bytes, void *stream) {
     if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
     if (!workspace) return OSDN_ERR_WORKSPACE;
-    if (workspace_bytes < osdn_backward_workspace_bytes(B, H, T, K, V)) return OSDN_ERR_WORKSPACE;
+    const size_t need = per_channel ? osdn_backward_kda_workspace_bytes(B, H, T, K, V)
+                                    : osdn_backward_workspace_bytes(B, H, T, K, V);
+    if (workspace_bytes < need) return OSDN_ERR_WORKSPACE;
     const size_t BH = (size_t)B * H;
     if (BH == 0) return OSDN_OK;
     if (T > 0 && (!q || !k || !ktilde || !v || !beta || !dq || !dk || !dv || !dbeta))
@@ -312,8 +334,9 @@ int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, cons
     const size_t es = io_bytes(io);
     const size_t kb = BH * (size_t)T * K * es, vb = BH * (size_t)T * V * es;
     const size_t gb = BH * (size_t)T * 4, db = BH * (size_t)K * 4, sb = BH * (size_t)V * K * 4;
-    const size_t insz[13] = {kb, kb, kb, vb, gb, gb, db, gb, sb, vb, sb, db, kb};
-    const size_t outsz[9] = {kb, kb, vb, gb, gb, gb, db, sb, BH * 4};
+    const size_t ab = per_channel ? BH * (size_t)T * K * 4 : gb;   // alpha, dalpha
+    const size_t insz[13] = {kb, kb, kb, vb, gb, gb, db, ab, sb, vb, sb, db, kb};
+    const size_t outsz[9] = {kb, kb, vb, gb, gb, ab, db, sb, BH * 4};
     for (int a = 0; a < 9; ++a) {
         for (int i = 0; i < 13; ++i)
             if (overlap(outs[a], outsz[a], ins[i], insz[i])) return OSDN_ERR_ALIAS;
@@ -331,9 +354,73 @@ int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, cons
     } else {
         e = osdn::backward_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, r, eta, d0, alpha,
                                   S0, d_o, d_ST, d_dT, d_ktilde, dq, dk, dv, dbeta, dr, dalpha,
-                                  dd0, dS0, deta, static_cast<char *>(workspace) + kStatusBytes,
-                                  st);
+                                  dd0, dS0, deta, per_channel,
+                                  static_cast<char *>(workspace) + kStatusBytes, st);
     }
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                  const void *ktilde, const void *v, const float *beta, const float *r,
+                  float eta, const float *d0, const float *alpha, const float *S0,
+                  const void *d_o, const float *d_ST, const float *d_dT, const void *d_ktilde,
+                  void *dq, void *dk, void *dv, float *dbeta, float *dr, float *dalpha,
+                  float *dd0, float *dS0, float *deta, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    return backward_checked(io, B, H, T, K, V, q, k, ktilde, v, beta, r, eta, d0, alpha, S0, d_o,
+                            d_ST, d_dT, d_ktilde, dq, dk, dv, dbeta, dr, dalpha, dd0, dS0, deta,
+                            false, workspace, workspace_bytes, stream);
+}
+
+int osdn_backward_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                      const void *ktilde, const void *v, const float *beta, const float *r,
+                      float eta, const float *d0, const float *alpha_k, const float *S0,
+                      const void *d_o, const float *d_ST, const float *d_dT,
+                      const void *d_ktilde, void *dq, void *dk, void *dv, float *dbeta,
+                      float *dr, float *dalpha_k, float *dd0, float *dS0, float *deta,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_checked(io, B, H, T, K, V, q, k, ktilde, v, beta, r, eta, d0, alpha_k, S0,
+                            d_o, d_ST, d_dT, d_ktilde, dq, dk, dv, dbeta, dr, dalpha_k, dd0, dS0,
+                            deta, true, workspace, workspace_bytes, stream);
+}
+
+int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                       const void *ktilde, const void *v, const float *beta,
+                       const float *alpha_k, const float *S0, void *o, float *ST,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (!workspace || workspace_bytes < osdn_chunk_fwd_kda_workspace_bytes(io, B, H, T, K, V))
+        return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (T > 0 && (!q || !k || !ktilde || !v || !beta || !o)) return OSDN_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(ktilde) || misaligned(v) ||
+        misaligned(beta) || misaligned(alpha_k) || misaligned(S0) || misaligned(o) ||
+        misaligned(ST) || misaligned(workspace))
+        return OSDN_ERR_ALIGN;
+    const size_t es = io_bytes(io);
+    const size_t kb = BH * (size_t)T * K * es, vb = BH * (size_t)T * V * es;
+    const size_t sb = BH * (size_t)V * K * 4, gb = BH * (size_t)T * 4;
+    const size_t ab = BH * (size_t)T * K * 4;
+    const void *ins[7] = {q, k, ktilde, v, beta, alpha_k, S0};
+    const size_t insz[7] = {kb, kb, kb, vb, gb, ab, sb};
+    for (int i = 0; i < 7; ++i)
+        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]))
+            return OSDN_ERR_ALIAS;
+    if (overlap(o, vb, ST, sb)) return OSDN_ERR_ALIAS;
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaError_t e;
+    if (T == 0)
+        e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, (cudaStream_t)stream);
+    else
+        e = osdn::delta_simt_kda_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha_k, S0,
+                                        o, ST, (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

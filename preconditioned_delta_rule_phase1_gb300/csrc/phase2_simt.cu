@@ -1,10 +1,15 @@
 // phase2_simt.cu -- Phase 2 of OSDN in fp32 FFMA: the delta-rule recurrence
 // with preconditioned keys (gist.science summary of arXiv 2605.13473,
 // section 2.1), for fp32 I/O, where tensor-core operand rounding would not
-// meet fp32 accuracy.
+// meet fp32 accuracy, and for the per-channel decay (both I/O types).
 //
 //     S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) ktilde_t^T
 //     o_t = S_t q_t
+//
+// With PCH (a decay per key channel, the Kimi-Delta-Attention-style backbone
+// of section 4) alpha_t is a K-vector that scales the key columns of S:
+//
+//     S_t = S_{t-1} Diag(alpha_t) + beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) ktilde_t^T
 //
 // The rows of S evolve independently (row i only sees v_t[i]), so the grid is
 // one CTA per (sequence, slice of 32 value rows).  Four threads share a row:
@@ -19,7 +24,7 @@ namespace osdn {
 constexpr int kRows = 32;   // value rows per CTA
 constexpr int kStage = 16;  // tokens staged per pass (static smem stays < 48 KB)
 
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(128)
 delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restrict__ k,
                   const io_t *__restrict__ ktilde, const io_t *__restrict__ v,
@@ -29,6 +34,7 @@ delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restri
     __shared__ __align__(16) float ks[kStage][K];
     __shared__ __align__(16) float kts[kStage][K];
     __shared__ __align__(16) float qs[kStage][K];
+    __shared__ __align__(16) float aks[PCH ? kStage : 1][PCH ? K : 4];   // per-channel decay
     __shared__ float vs[kStage][kRows];
     __shared__ float os[kStage][kRows];
     __shared__ float bs[kStage], as[kStage];
@@ -64,6 +70,12 @@ delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restri
                 kts[tt][j + e] = b4[e];
                 qs[tt][j + e] = c4[e];
             }
+            if constexpr (PCH) {
+                float d4[4] = {1, 1, 1, 1};
+                if (alpha && tt < tn) load4(alpha + kbase + (size_t)(t0 + tt) * K + j, d4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) aks[tt][j + e] = d4[e];
+            }
         }
         for (int idx = tid; idx < kStage * kRows; idx += 128) {
             const int tt = idx / kRows, i = idx % kRows;
@@ -71,11 +83,15 @@ delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restri
         }
         if (tid < kStage) {
             bs[tid] = tid < tn ? beta[seq * T + t0 + tid] : 0.0f;
-            as[tid] = (alpha && tid < tn) ? alpha[seq * T + t0 + tid] : 1.0f;
+            as[tid] = (!PCH && alpha && tid < tn) ? alpha[seq * T + t0 + tid] : 1.0f;
         }
         __syncthreads();
 
         for (int tt = 0; tt < tn; ++tt) {
+            if constexpr (PCH) {   // decay the key columns first; the scalar gate below is 1
+#pragma unroll
+                for (int m = 0; m < KP; ++m) S[m] *= aks[tt][p + 4 * m];
+            }
             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
             for (int m = 0; m < KP; m += 4) {
@@ -121,13 +137,13 @@ delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restri
     }
 }
 
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH = false>
 static cudaError_t launch_delta_simt(int BH, int T, int V, const void *q, const void *k,
                                      const void *kt, const void *v, const float *beta,
                                      const float *alpha, const float *S0, void *o, float *ST,
                                      cudaStream_t stream) {
     dim3 grid(V / kRows, BH);
-    delta_simt_kernel<io_t, K><<<grid, 128, 0, stream>>>(
+    delta_simt_kernel<io_t, K, PCH><<<grid, 128, 0, stream>>>(
         T, V, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
         static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
         static_cast<io_t *>(o), ST);
@@ -146,6 +162,21 @@ cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q
     if (K == 64)
         return launch_delta_simt<float, 64>(BH, T, V, q, k, kt, v, beta, alpha, S0, o, ST, stream);
     return launch_delta_simt<float, 128>(BH, T, V, q, k, kt, v, beta, alpha, S0, o, ST, stream);
+}
+
+// Phase 2 with a per-channel decay alpha_k [BH][T][K] (NULL: no decay).
+cudaError_t delta_simt_kda_launch(int io, int BH, int T, int K, int V, const void *q,
+                                  const void *k, const void *kt, const void *v,
+                                  const float *beta, const float *alpha_k, const float *S0,
+                                  void *o, float *ST, cudaStream_t stream) {
+    if (io == OSDN_BF16) {
+        if (K == 64)
+            return launch_delta_simt<__nv_bfloat16, 64, true>(BH, T, V, q, k, kt, v, beta, alpha_k, S0, o, ST, stream);
+        return launch_delta_simt<__nv_bfloat16, 128, true>(BH, T, V, q, k, kt, v, beta, alpha_k, S0, o, ST, stream);
+    }
+    if (K == 64)
+        return launch_delta_simt<float, 64, true>(BH, T, V, q, k, kt, v, beta, alpha_k, S0, o, ST, stream);
+    return launch_delta_simt<float, 128, true>(BH, T, V, q, k, kt, v, beta, alpha_k, S0, o, ST, stream);
 }
 
 }  // namespace osdn

@@ -50,6 +50,13 @@ _SIGS = {
     "osdn_backward": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 6 +
                       [ctypes.c_float] + [ctypes.c_void_p] * 17 +
                       [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_backward_kda_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "osdn_backward_kda": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 6 +
+                          [ctypes.c_float] + [ctypes.c_void_p] * 17 +
+                          [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_chunk_fwd_kda_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "osdn_chunk_fwd_kda": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
+                           [ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 
@@ -188,6 +195,10 @@ def chunk_fwd_workspace_bytes(io, B, H, T, K, V) -> int:
 
 def backward_workspace_bytes(B, H, T, K, V) -> int:
     return int(lib().osdn_backward_workspace_bytes(B, H, T, K, V))
+
+
+def backward_kda_workspace_bytes(B, H, T, K, V) -> int:
+    return int(lib().osdn_backward_kda_workspace_bytes(B, H, T, K, V))
 
 
 def precond_scan(k, beta, r=None, eta=0.1, d0=None, ktilde=None, dT=None, workspace=None,
@@ -330,14 +341,30 @@ def backward(q, k, ktilde, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=Non
     sequence's share; the scalar gradient is the sum), and r, alpha, d0, S0
     for those given (an input given as None has no entry).
     """
+    return _backward(False, q, k, ktilde, v, beta, r, eta, d0, alpha, S0, do, dST, ddT, dktilde,
+                     workspace, stream)
+
+
+def backward_kda(q, k, ktilde, v, beta, r=None, eta=0.1, d0=None, alpha_k=None, S0=None, *,
+                 do=None, dST=None, ddT=None, dktilde=None, workspace=None, stream=None):
+    """Gradients of both phases with a decay per key channel
+    (osdn_backward_kda): as ``backward``, with alpha_k [B, H, T, K] and its
+    gradient under the key "alpha" ([B, H, T, K])."""
+    return _backward(True, q, k, ktilde, v, beta, r, eta, d0, alpha_k, S0, do, dST, ddT,
+                     dktilde, workspace, stream)
+
+
+def _backward(per_channel, q, k, ktilde, v, beta, r, eta, d0, alpha, S0, do, dST, ddT, dktilde,
+              workspace, stream):
     B, H, T, K = k.shape
     V = v.shape[-1]
     io, dev = _io(k), k.device
+    ashape = (B, H, T, K) if per_channel else (B, H, T)
     for name, t, shape, dt in (("q", q, (B, H, T, K), k.dtype),
                                ("ktilde", ktilde, (B, H, T, K), k.dtype),
                                ("v", v, (B, H, T, V), k.dtype),
                                ("beta", beta, (B, H, T), F32), ("r", r, (B, H, T), F32),
-                               ("d0", d0, (B, H, K), F32), ("alpha", alpha, (B, H, T), F32),
+                               ("d0", d0, (B, H, K), F32), ("alpha", alpha, ashape, F32),
                                ("S0", S0, (B, H, V, K), F32), ("do", do, (B, H, T, V), k.dtype),
                                ("dST", dST, (B, H, V, K), F32), ("ddT", ddT, (B, H, K), F32),
                                ("dktilde", dktilde, (B, H, T, K), k.dtype)):
@@ -350,19 +377,59 @@ def backward(q, k, ktilde, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=Non
     if r is not None:
         g["r"] = new(B, H, T)
     if alpha is not None:
-        g["alpha"] = new(B, H, T)
+        g["alpha"] = new(*ashape)
     if d0 is not None:
         g["d0"] = new(B, H, K)
     if S0 is not None:
         g["S0"] = new(B, H, V, K)
     ws = _workspace(workspace, dev)
+    fn, size = ((lib().osdn_backward_kda, backward_kda_workspace_bytes) if per_channel
+                else (lib().osdn_backward, backward_workspace_bytes))
     with _on(dev):
-        ws.ensure(backward_workspace_bytes(B, H, T, K, V))
-        code = lib().osdn_backward(
-            io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v), _ptr(beta), _ptr(r),
-            float(eta), _ptr(d0), _ptr(alpha), _ptr(S0), _ptr(do), _ptr(dST), _ptr(ddT),
-            _ptr(dktilde), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), _ptr(g["beta"]),
-            _ptr(g.get("r")), _ptr(g.get("alpha")), _ptr(g.get("d0")), _ptr(g.get("S0")),
-            _ptr(g["eta"]), ws.ptr, ws.nbytes, _stream(stream, dev))
-    _check(code, "osdn_backward")
+        ws.ensure(size(B, H, T, K, V))
+        code = fn(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde), _ptr(v), _ptr(beta), _ptr(r),
+                  float(eta), _ptr(d0), _ptr(alpha), _ptr(S0), _ptr(do), _ptr(dST), _ptr(ddT),
+                  _ptr(dktilde), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]), _ptr(g["beta"]),
+                  _ptr(g.get("r")), _ptr(g.get("alpha")), _ptr(g.get("d0")), _ptr(g.get("S0")),
+                  _ptr(g["eta"]), ws.ptr, ws.nbytes, _stream(stream, dev))
+    _check(code, "osdn_backward_kda" if per_channel else "osdn_backward")
     return g
+
+
+def chunk_fwd_kda(q, k, ktilde, v, beta, alpha_k=None, S0=None, o=None, ST=None, workspace=None,
+                  stream=None):
+    """Phase 2 with a decay per key channel (osdn_chunk_fwd_kda), alpha_k
+    [B, H, T, K] fp32: returns (o, ST)."""
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    io, dev = _io(k), k.device
+    _expect("q", q, (B, H, T, K), k.dtype, dev)
+    _expect("ktilde", ktilde, (B, H, T, K), k.dtype, dev)
+    _expect("v", v, (B, H, T, V), k.dtype, dev)
+    _expect("beta", beta, (B, H, T), F32, dev)
+    _expect("alpha_k", alpha_k, (B, H, T, K), F32, dev)
+    _expect("S0", S0, (B, H, V, K), F32, dev)
+    if o is None:
+        o = torch.empty(B, H, T, V, dtype=k.dtype, device=dev)
+    if ST is None:
+        ST = torch.empty(B, H, V, K, dtype=F32, device=dev)
+    _expect("o", o, (B, H, T, V), k.dtype, dev)
+    _expect("ST", ST, (B, H, V, K), F32, dev)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        ws.ensure(int(lib().osdn_chunk_fwd_kda_workspace_bytes(io, B, H, T, K, V)))
+        code = lib().osdn_chunk_fwd_kda(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(ktilde),
+                                        _ptr(v), _ptr(beta), _ptr(alpha_k), _ptr(S0), _ptr(o),
+                                        _ptr(ST), ws.ptr, ws.nbytes, _stream(stream, dev))
+    _check(code, "osdn_chunk_fwd_kda")
+    return o, ST
+
+
+def forward_kda(q, k, v, beta, r=None, eta=0.1, d0=None, alpha_k=None, S0=None, workspace=None,
+                stream=None):
+    """Both phases with a decay per key channel in Phase 2: returns
+    (ktilde, dT, o, ST)."""
+    ws = _workspace(workspace, k.device)
+    ktilde, dT = precond_scan(k, beta, r, eta, d0, workspace=ws, stream=stream)
+    o, ST = chunk_fwd_kda(q, k, ktilde, v, beta, alpha_k, S0, workspace=ws, stream=stream)
+    return ktilde, dT, o, ST

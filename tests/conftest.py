@@ -10,3 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line(
+        "markers", "first_gpu_run: a GPU test of code that has not yet passed on a GPU; "
+        "collected after the others, so that a run stopping at its first failure has "
+        "already run every established test")
+
+
+def pytest_collection_modifyitems(config, items):
+    # stable: the established tests keep their order, the new ones follow
+    items.sort(key=lambda item: item.get_closest_marker("first_gpu_run") is not None)

@@ -212,3 +212,54 @@ def test_backward_workspace_size(L):
         want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (3 * K + 2) * 4)
                 + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
         assert L.osdn_backward_workspace_bytes(B, H, T, K, V) == want
+
+
+def kda(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, kt=3 * FAKE, v=4 * FAKE,
+        beta=5 * FAKE, ak=None, S0=None, o=6 * FAKE, ST=None, ws=7 * FAKE, wsb=256):
+    return L.osdn_chunk_fwd_kda(io, B, H, T, K, V, q, k, kt, v, beta, ak, S0, o, ST, ws, wsb,
+                                None)
+
+
+def test_host_validation_chunk_fwd_kda(L):
+    assert L.osdn_chunk_fwd_kda_workspace_bytes(1, 2, 16, 8192, 128, 128) == 256
+    assert kda(L, io=2) == -3
+    assert kda(L, K=32) == -2 and kda(L, V=96) == -2 and kda(L, T=-1) == -2
+    assert kda(L, ws=None) == -5 and kda(L, wsb=255) == -5
+    assert kda(L, q=None) == -1 and kda(L, o=None) == -1 and kda(L, beta=None) == -1
+    assert kda(L, ak=8 * FAKE + 4) == -4
+    assert kda(L, o=FAKE) == -9                   # o aliases q
+    # alpha_k is [B][H][T][K] fp32: 8 tokens x 64 channels = 2048 bytes
+    assert kda(L, ak=8 * FAKE, o=8 * FAKE + 2032) == -9
+    assert kda(L, ak=8 * FAKE, o=8 * FAKE + 2048) != -9
+    assert kda(L, H=0) == 0
+
+
+def test_host_validation_backward_kda(L):
+    def call(**kw):
+        ak = kw.pop("ak", 8 * FAKE)
+        dak = kw.pop("dak", 19 * FAKE)
+        a = {n: (i + 1) * FAKE for i, n in enumerate(
+            ["q", "k", "kt", "v", "beta", "r", "d0", "alpha", "S0", "do", "dST", "ddT", "dkt",
+             "dq", "dk", "dv", "dbeta", "dr", "dalpha", "dd0", "dS0", "deta"])}
+        T, K, V = 8, 64, 64
+        wsb = kw.pop("wsb", L.osdn_backward_kda_workspace_bytes(1, 1, T, K, V))
+        return L.osdn_backward_kda(kw.pop("io", 1), 1, 1, T, K, V, a["q"], a["k"], a["kt"],
+                                   a["v"], a["beta"], a["r"], 0.1, a["d0"], ak, a["S0"], a["do"],
+                                   a["dST"], a["ddT"], a["dkt"], a["dq"], a["dk"], a["dv"],
+                                   a["dbeta"], a["dr"], dak, a["dd0"], a["dS0"], a["deta"],
+                                   40 * FAKE, wsb, None)
+    assert call(io=4) == -3
+    assert call(wsb=L.osdn_backward_workspace_bytes(1, 1, 8, 64, 64)) == -5  # too small here
+    # dalpha_k is [T][K] fp32 (2048 bytes): it overlaps the next 2 KB, not a [T] vector's 32 B
+    assert call(dak=19 * FAKE, ak=19 * FAKE + 1024) == -9
+    assert call(dak=20 * FAKE - 1024) == -9                 # runs into dd0 at 20 * FAKE
+    assert call() != -9 and call() != -2
+
+
+def test_backward_kda_workspace_size(L):
+    r = lambda x: -(-x // 256) * 256
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64)]:
+        BH, ns = B * H, -(-T // 16)
+        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (4 * K + 1) * 4)
+                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
+        assert L.osdn_backward_kda_workspace_bytes(B, H, T, K, V) == want

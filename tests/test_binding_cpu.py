@@ -72,6 +72,17 @@ def test_valid_calls_pass(fake, io, opts):
     assert set(g) == want and g["eta"].shape == (2, 3) and g["S0" if "S0" in g else "q"].numel()
     assert "osdn_decode_step" in fake.calls and "osdn_precond_scan_residual" in fake.calls
     assert "osdn_backward" in fake.calls
+    ak = torch.rand(2, 3, 40, 128)
+    o, ST = ops.chunk_fwd_kda(x["q"], x["k"], kt, x["v"], x["beta"], ak, x["S0"],
+                              workspace=ops.Workspace(device="cpu"))
+    assert o.shape == (2, 3, 40, 64) and ST.shape == (2, 3, 64, 128)
+    ops.forward_kda(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"], ak, x["S0"],
+                    workspace=ops.Workspace(device="cpu"))
+    gk = ops.backward_kda(x["q"], x["k"], kt, x["v"], x["beta"], x["r"], x["eta"], x["d0"], ak,
+                          x["S0"], do=torch.zeros(2, 3, 40, 64, dtype=x["k"].dtype),
+                          workspace=ops.Workspace(device="cpu"))
+    assert gk["alpha"].shape == (2, 3, 40, 128)
+    assert "osdn_chunk_fwd_kda" in fake.calls and "osdn_backward_kda" in fake.calls
 
 
 def test_mistakes_are_refused_before_the_library(fake):
@@ -99,6 +110,12 @@ def test_mistakes_are_refused_before_the_library(fake):
         lambda: ops.backward(x["q"], x["k"], x["k"], x["v"], x["beta"],
                              dST=torch.zeros(2, 3, 64, 32), workspace=ws),           # dST shape
         lambda: ops.backward(x["q"], x["k"], None, x["v"], x["beta"], workspace=ws),  # no ktilde
+        lambda: ops.chunk_fwd_kda(x["q"], x["k"], x["k"], x["v"], x["beta"], x["alpha"],
+                                  workspace=ws),                        # a scalar gate for KDA
+        lambda: ops.backward_kda(x["q"], x["k"], x["k"], x["v"], x["beta"],
+                                 alpha_k=x["alpha"], workspace=ws),     # likewise
+        lambda: ops.backward(x["q"], x["k"], x["k"], x["v"], x["beta"],
+                             alpha=torch.rand(2, 3, 40, 64), workspace=ws),  # per-channel gate
     ]
     for i, call in enumerate(bad):
         n = len(fake.calls)
