@@ -339,6 +339,18 @@ int osdn_backward_kda(int io, int B, int H, int T, int K, int V, const void *q, 
                       float *dr, float *dalpha_k, float *dd0, float *dS0, float *deta,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * osdn_decode_step with a decay per key channel (the recurrent step of
+ * osdn_chunk_fwd_kda): alpha_k in [B][H][K] fp32, or NULL, in place of
+ * alpha; the state row is decayed column by column,
+ *     S <- S Diag(alpha) + beta (v - S Diag(alpha) k) ktilde^T,   o = S q.
+ * Everything else as osdn_decode_step.
+ */
+int osdn_decode_step_kda(int io, int B, int H, int K, int V, const void *q, const void *k,
+                         const void *v, const float *beta, const float *r, float eta,
+                         const float *alpha_k, float *d, float *S, void *o, void *ktilde,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Zero the 256-byte status area at the start of a workspace (async). */
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 

@@ -15,6 +15,11 @@
 //     o_i = alpha sq + u_i <ktilde, q>.
 // The step moves 8 V K bytes of state per sequence and is HBM-bound.
 //
+// With PCH the decay is per key channel (alpha in R^K, the Kimi Delta
+// Attention backbone of section 4 read as GDN's gate made a vector): the
+// row is decayed column by column, S_i <- alpha (.) S_i, before the same
+// update with a scalar gate of 1.
+//
 // One CTA of 256 threads per sequence: every warp forms the sequence's
 // scalars itself (K/32 elements a lane, warp reductions); after one block
 // barrier (all warps have read d) warp 0 writes d and ktilde; the eight
@@ -42,7 +47,7 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(kThreads) decode_kernel(Params p) {
     constexpr int E = K / 32;   // elements of a K-vector per lane
     const int seq = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -68,7 +73,21 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Params p) {
     }
     const float beta = p.beta[seq];
     const float r = p.r ? p.r[seq] : 1.0f;
-    const float alpha = p.alpha ? p.alpha[seq] : 1.0f;
+    const float alpha = (!PCH && p.alpha) ? p.alpha[seq] : 1.0f;
+    float av[E];   // the per-channel decay of this lane's columns
+#pragma unroll
+    for (int e = 0; e < E; ++e) av[e] = 1.0f;
+    if constexpr (PCH) {
+        if (p.alpha) {
+#pragma unroll
+            for (int e = 0; e < E; e += 2) {
+                float t[2];
+                load2(p.alpha + (size_t)seq * K + lane * E + e, t);
+                av[e] = t[0];
+                av[e + 1] = t[1];
+            }
+        }
+    }
     float n = 0.f, a = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -114,6 +133,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Params p) {
                 sv[rr][e] = t[0];
                 sv[rr][e + 1] = t[1];
             }
+            if constexpr (PCH) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) sv[rr][e] *= av[e];
+            }
         }
 #pragma unroll
         for (int rr = 0; rr < kRowsInFlight; ++rr) {
@@ -144,9 +167,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Params p) {
     }
 }
 
-template <typename io_t, int K>
+template <typename io_t, int K, bool PCH = false>
 cudaError_t launch_t(int BH, const Params &p, cudaStream_t stream) {
-    decode_kernel<io_t, K><<<BH, kThreads, 0, stream>>>(p);
+    decode_kernel<io_t, K, PCH><<<BH, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -173,6 +196,31 @@ cudaError_t decode_step_launch(int io, int BH, int K, int V, const void *q, cons
         return K == 64 ? dec::launch_t<__nv_bfloat16, 64>(BH, p, stream)
                        : dec::launch_t<__nv_bfloat16, 128>(BH, p, stream);
     return K == 64 ? dec::launch_t<float, 64>(BH, p, stream) : dec::launch_t<float, 128>(BH, p, stream);
+}
+
+// The same step with a decay per key channel, alpha_k [BH][K] (NULL: none).
+cudaError_t decode_step_kda_launch(int io, int BH, int K, int V, const void *q, const void *k,
+                                   const void *v, const float *beta, const float *r, float eta,
+                                   const float *alpha_k, float *d, float *S, void *o,
+                                   void *ktilde, cudaStream_t stream) {
+    dec::Params p;
+    p.V = V;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.beta = beta;
+    p.r = r;
+    p.alpha = alpha_k;
+    p.eta = eta;
+    p.d = d;
+    p.S = S;
+    p.o = o;
+    p.ktilde = ktilde;
+    if (io == OSDN_BF16)
+        return K == 64 ? dec::launch_t<__nv_bfloat16, 64, true>(BH, p, stream)
+                       : dec::launch_t<__nv_bfloat16, 128, true>(BH, p, stream);
+    return K == 64 ? dec::launch_t<float, 64, true>(BH, p, stream)
+                   : dec::launch_t<float, 128, true>(BH, p, stream);
 }
 
 }  // namespace osdn

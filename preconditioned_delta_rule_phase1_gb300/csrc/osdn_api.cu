@@ -41,6 +41,10 @@ cudaError_t delta_simt_kda_launch(int io, int BH, int T, int K, int V, const voi
                                   const void *k, const void *kt, const void *v,
                                   const float *beta, const float *alpha_k, const float *S0,
                                   void *o, float *ST, cudaStream_t stream);
+cudaError_t decode_step_kda_launch(int io, int BH, int K, int V, const void *q, const void *k,
+                                   const void *v, const float *beta, const float *r, float eta,
+                                   const float *alpha_k, float *d, float *S, void *o,
+                                   void *ktilde, cudaStream_t stream);
 cudaError_t decode_step_launch(int io, int BH, int K, int V, const void *q, const void *k,
                                const void *v, const float *beta, const float *r, float eta,
                                const float *alpha, float *d, float *S, void *o, void *ktilde,
@@ -269,10 +273,16 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 
-int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const void *k,
-                     const void *v, const float *beta, const float *r, float eta,
-                     const float *alpha, float *d, float *S, void *o, void *ktilde,
-                     void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// osdn_decode_step and osdn_decode_step_kda: one validation, one launch.
+// With a per-channel decay alpha is [B][H][K], else [B][H].
+int decode_checked(int io, int B, int H, int K, int V, const void *q, const void *k,
+                   const void *v, const float *beta, const float *r, float eta,
+                   const float *alpha, float *d, float *S, void *o, void *ktilde,
+                   bool per_channel, void *workspace, size_t workspace_bytes, void *stream) {
     if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
     if (!dims_ok(B, H, 0) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
     if (!workspace || workspace_bytes < kStatusBytes) return OSDN_ERR_WORKSPACE;
@@ -285,7 +295,8 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
         return OSDN_ERR_ALIGN;
     const size_t es = io_bytes(io);
     const void *ins[6] = {q, k, v, beta, r, alpha};
-    const size_t insz[6] = {BH * K * es, BH * K * es, BH * V * es, BH * 4, BH * 4, BH * 4};
+    const size_t insz[6] = {BH * K * es, BH * K * es, BH * V * es, BH * 4, BH * 4,
+                            per_channel ? BH * K * 4 : BH * 4};
     const void *outs[4] = {d, S, o, ktilde};
     const size_t outsz[4] = {BH * K * 4, BH * V * K * 4, BH * V * es, BH * K * es};
     for (int a = 0; a < 4; ++a) {
@@ -296,9 +307,32 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
     }
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
-    cudaError_t e = osdn::decode_step_launch(io, (int)BH, K, V, q, k, v, beta, r, eta, alpha, d, S,
-                                             o, ktilde, (cudaStream_t)stream);
+    cudaError_t e = per_channel
+        ? osdn::decode_step_kda_launch(io, (int)BH, K, V, q, k, v, beta, r, eta, alpha, d, S, o,
+                                       ktilde, (cudaStream_t)stream)
+        : osdn::decode_step_launch(io, (int)BH, K, V, q, k, v, beta, r, eta, alpha, d, S, o,
+                                   ktilde, (cudaStream_t)stream);
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const void *k,
+                     const void *v, const float *beta, const float *r, float eta,
+                     const float *alpha, float *d, float *S, void *o, void *ktilde,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_checked(io, B, H, K, V, q, k, v, beta, r, eta, alpha, d, S, o, ktilde, false,
+                          workspace, workspace_bytes, stream);
+}
+
+int osdn_decode_step_kda(int io, int B, int H, int K, int V, const void *q, const void *k,
+                         const void *v, const float *beta, const float *r, float eta,
+                         const float *alpha_k, float *d, float *S, void *o, void *ktilde,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_checked(io, B, H, K, V, q, k, v, beta, r, eta, alpha_k, d, S, o, ktilde, true,
+                          workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

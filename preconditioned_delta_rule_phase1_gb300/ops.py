@@ -54,6 +54,9 @@ _SIGS = {
     "osdn_backward_kda": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 6 +
                           [ctypes.c_float] + [ctypes.c_void_p] * 17 +
                           [ctypes.c_size_t, ctypes.c_void_p]),
+    "osdn_decode_step_kda": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5 +
+                             [ctypes.c_float] + [ctypes.c_void_p] * 6 +
+                             [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_chunk_fwd_kda_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "osdn_chunk_fwd_kda": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
                            [ctypes.c_size_t, ctypes.c_void_p]),
@@ -306,6 +309,17 @@ def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde
     """One recurrent step (osdn_decode_step): updates d [B,H,K] and S [B,H,V,K]
     (fp32) in place for the token q, k [B,H,K], v [B,H,V] (io); returns
     (o, ktilde)."""
+    return _decode(False, q, k, v, beta, d, S, r, eta, alpha, o, ktilde, workspace, stream)
+
+
+def decode_step_kda(q, k, v, beta, d, S, r=None, eta=0.1, alpha_k=None, o=None, ktilde=None,
+                    workspace=None, stream=None):
+    """One recurrent step with a decay per key channel (osdn_decode_step_kda):
+    as ``decode_step``, with alpha_k [B,H,K] fp32."""
+    return _decode(True, q, k, v, beta, d, S, r, eta, alpha_k, o, ktilde, workspace, stream)
+
+
+def _decode(per_channel, q, k, v, beta, d, S, r, eta, alpha, o, ktilde, workspace, stream):
     B, H, K = k.shape
     V = v.shape[-1]
     io, dev = _io(k), k.device
@@ -313,7 +327,7 @@ def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde
     _expect("v", v, (B, H, V), k.dtype, dev)
     _expect("beta", beta, (B, H), F32, dev)
     _expect("r", r, (B, H), F32, dev)
-    _expect("alpha", alpha, (B, H), F32, dev)
+    _expect("alpha", alpha, (B, H, K) if per_channel else (B, H), F32, dev)
     _expect("d", d, (B, H, K), F32, dev)
     _expect("S", S, (B, H, V, K), F32, dev)
     if o is None:
@@ -323,11 +337,12 @@ def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde
     _expect("o", o, (B, H, V), k.dtype, dev)
     _expect("ktilde", ktilde, (B, H, K), k.dtype, dev)
     ws = _workspace(workspace, dev)
+    name = "osdn_decode_step_kda" if per_channel else "osdn_decode_step"
     with _on(dev):
-        code = lib().osdn_decode_step(io, B, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                                      _ptr(r), float(eta), _ptr(alpha), _ptr(d), _ptr(S), _ptr(o),
-                                      _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream, dev))
-    _check(code, "osdn_decode_step")
+        code = getattr(lib(), name)(io, B, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                    _ptr(r), float(eta), _ptr(alpha), _ptr(d), _ptr(S), _ptr(o),
+                                    _ptr(ktilde), ws.ptr, ws.nbytes, _stream(stream, dev))
+    _check(code, name)
     return o, ktilde
 
 

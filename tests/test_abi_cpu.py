@@ -263,3 +263,20 @@ def test_backward_kda_workspace_size(L):
         want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (4 * K + 1) * 4)
                 + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
         assert L.osdn_backward_kda_workspace_bytes(B, H, T, K, V) == want
+
+
+def test_host_validation_decode_step_kda(L):
+    def dk(**kw):
+        a = dict(io=1, B=1, H=1, K=64, V=64, q=FAKE, k=2 * FAKE, v=3 * FAKE, beta=4 * FAKE,
+                 r=None, ak=9 * FAKE, d=5 * FAKE, S=6 * FAKE, o=7 * FAKE, kt=None, ws=8 * FAKE,
+                 wsb=256)
+        a.update(kw)
+        return L.osdn_decode_step_kda(a["io"], a["B"], a["H"], a["K"], a["V"], a["q"], a["k"],
+                                      a["v"], a["beta"], a["r"], 0.1, a["ak"], a["d"], a["S"],
+                                      a["o"], a["kt"], a["ws"], a["wsb"], None)
+    assert dk(io=3) == -3 and dk(K=96) == -2 and dk(ws=None) == -5
+    assert dk(q=None) == -1 and dk(ak=9 * FAKE + 8) == -4
+    # alpha_k is [B][H][K] fp32 (256 bytes here), not one value per sequence
+    assert dk(d=9 * FAKE + 128) == -9
+    assert dk(d=9 * FAKE + 256) != -9
+    assert dk(B=0) == 0

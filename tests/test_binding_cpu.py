@@ -82,7 +82,10 @@ def test_valid_calls_pass(fake, io, opts):
                           x["S0"], do=torch.zeros(2, 3, 40, 64, dtype=x["k"].dtype),
                           workspace=ops.Workspace(device="cpu"))
     assert gk["alpha"].shape == (2, 3, 40, 128)
+    ops.decode_step_kda(sl("q"), sl("k"), sl("v"), sl("beta"), d, S, r=sl("r"), eta=x["eta"],
+                        alpha_k=ak[:, :, 0].contiguous(), workspace=ops.Workspace(device="cpu"))
     assert "osdn_chunk_fwd_kda" in fake.calls and "osdn_backward_kda" in fake.calls
+    assert "osdn_decode_step_kda" in fake.calls
 
 
 def test_mistakes_are_refused_before_the_library(fake):

@@ -133,3 +133,25 @@ def test_backward_deterministic():
     a, b = run_backward(x, cot), run_backward(x, cot)
     for n in a:
         assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("io,K,V", [("f32", 64, 128), ("bf16", 128, 128), ("bf16", 64, 64)])
+def test_decode_steps_match_oracle(io, K, V):
+    # twenty chained per-channel decode steps against the oracle's 20-token forward
+    x = case(io, K, V, 20, 900 + K + V)
+    d = x["d0"].clone().cuda()
+    S = x["S0"].clone().cuda()
+    g = to_cuda(x)
+    outs, kts = [], []
+    for t in range(20):
+        sl = lambda n: g[n][:, :, t].contiguous()
+        o, kt = ops.decode_step_kda(sl("q"), sl("k"), sl("v"), sl("beta"), d, S, r=sl("r"),
+                                    eta=x["eta"], alpha_k=sl("alpha"))
+        outs.append(o)
+        kts.append(kt)
+    torch.cuda.synchronize()
+    kt_ref, dT_ref, o_ref, S_ref = oracle.forward_kda(x["q"], x["k"], x["v"], x["beta"], x["r"],
+                                                      x["eta"], x["d0"], x["alpha"], x["S0"])
+    errs = {"o": rel_err(torch.stack(outs, 2), o_ref), "ktilde": rel_err(torch.stack(kts, 2), kt_ref),
+            "d": rel_err(d, dT_ref), "S": rel_err(S, S_ref)}
+    assert max(errs.values()) <= TOL[io], errs
