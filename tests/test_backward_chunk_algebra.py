@@ -30,13 +30,13 @@ dSigma carried between chunks:
 
 The Phase 1 adjoint then takes dKt (``test_backward_algebra.phase1_adjoint``)
 and the sum must equal the reference for every input.  A dropped decay term
-fails the comparison.
+fails the comparison.  A last test shows that the serial part, dSigma and
+dV, needs only the forward's prepared operands transposed.
 """
 import numpy as np
 import pytest
 
-from oracle import backward
-from tests.test_backward_algebra import by_hand, case, phase1_adjoint, reference, worst
+from tests.test_backward_algebra import case, phase1_adjoint, reference, worst
 
 
 def chunk_backward(q, k, kt, v, beta, alpha, S0, dO, dST, C=64, drop=None):
@@ -172,3 +172,45 @@ def test_a_dropped_decay_term_is_caught():
     ref = reference(x, cot)
     err = worst(chunked(x, cot, 16, drop="decay"), ref, ["alpha"])
     assert err["alpha"] > 1e-3, err
+
+
+def test_reverse_chain_is_the_forward_chain_transposed():
+    # Per chunk the forward maps (V, Sigma) to (O, Sigma') linearly with the
+    # prepared operands of the tensor-core forward,
+    #     O = Ae V + Qe Sigma,   Sigma' = g_C Sigma + W V + M Sigma,
+    # so the state gradient and dV need only those operands, transposed:
+    #     dV = Ae^T dO + W^T dSigma',   dSigma = g_C dSigma' + M^T dSigma' + Qe^T dO.
+    # Checked here against the explicit chunk backward above, chunk by chunk.
+    x, cot = case(100, 8, 16, 211, True)
+    h = 1
+    q, k, v = x["q"][0, h], x["k"][0, h], x["v"][0, h]
+    beta, alpha, S0 = x["beta"][0, h], x["alpha"][0, h], x["S0"][0, h]
+    dO, dST = cot["o"][0, h], cot["ST"][0, h]
+    rng = np.random.default_rng(5)
+    kt = k * (0.5 + rng.random(k.shape))
+    C, T = 32, 100
+    ref = chunk_backward(q, k, kt, v, beta, alpha, S0, dO, dST, C)
+    # forward with the prepared operands, keeping them per chunk
+    ops_ = []
+    for c0 in range(0, T, C):
+        n = min(C, T - c0)
+        sl = slice(c0, c0 + n)
+        Q, Kc, Kt, b = q[sl], k[sl], kt[sl], beta[sl]
+        lg = np.cumsum(np.log(alpha[sl]))
+        g = np.exp(lg)
+        G = np.exp(lg[:, None] - lg[None, :])
+        L = np.tril(b[:, None] * G * (Kc @ Kt.T), -1)
+        A = np.tril(G * (Q @ Kt.T))
+        Xb = np.linalg.inv(np.eye(n) + L) * b[None, :]
+        Kw = Xb @ (g[:, None] * Kc)
+        Dkt = (g[-1] / g)[:, None] * Kt
+        ops_.append(dict(sl=sl, gC=g[-1], W=Dkt.T @ Xb, M=-Dkt.T @ Kw, Ae=A @ Xb,
+                         Qe=g[:, None] * Q - A @ Kw))
+    dSig = dST.T.copy()
+    dv = np.zeros_like(v)
+    for c in reversed(ops_):
+        dOc = dO[c["sl"]]
+        dv[c["sl"]] = c["Ae"].T @ dOc + c["W"].T @ dSig
+        dSig = c["gC"] * dSig + c["M"].T @ dSig + c["Qe"].T @ dOc
+    np.testing.assert_allclose(dv, ref["dv"], rtol=0, atol=1e-12 * np.abs(ref["dv"]).max())
+    np.testing.assert_allclose(dSig.T, ref["dS0"], rtol=0, atol=1e-12 * np.abs(ref["dS0"]).max())
