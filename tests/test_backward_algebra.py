@@ -31,7 +31,10 @@ Phase 1, one sequence at a time, the adjoint lam = dL/dd_t run backwards
     dk_t += g d_t + 2 k (c_t lam + da d_t + dn),  g = dktilde_t (both parts)
     lam = r_t lam + da w_t + g k_t;  dd0 = lam at the start.
 
-A test below drops one term and checks that the comparison catches it.
+A test below drops one term and checks that the comparison catches it.  The
+last test runs the per-channel-decay variant (Diag(alpha_t) in place of
+alpha_t, dalpha_t[j] += dS_bar[i, j] S_{t-1}[i, j]) as the kernels' PCH flag
+does, against the autograd gradients with a [B, H, T, K] decay.
 """
 import numpy as np
 import pytest
@@ -239,3 +242,71 @@ def test_a_dropped_term_is_caught(drop):
     ref = reference(x, cot)
     err = worst(by_hand(x, cot, drop), ref, NAMES)
     assert max(err.values()) > 1e-3, err
+
+
+def phase2_adjoint_per_channel(q, k, kt, v, beta, alpha_k, S0, dO, dST):
+    """The state adjoint with a decay per key channel, as the kernel's PCH
+    variant runs it: Diag(alpha_t) in place of alpha_t, dalpha_t per column."""
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    dq, dkt, dk2 = np.zeros_like(q), np.zeros_like(k), np.zeros_like(k)
+    db2, da = np.zeros((B, H, T)), np.zeros((B, H, T, K))
+    dv, dS0 = np.zeros_like(v), np.zeros((B, H, V, K))
+    for b in range(B):
+        for h in range(H):
+            for i in range(V):
+                S = S0[b, h, i].copy()
+                Sp, es, us = [], [], []
+                for t in range(T):
+                    a = alpha_k[b, h, t]
+                    e = v[b, h, t, i] - (a * S) @ k[b, h, t]
+                    u = beta[b, h, t] * e
+                    Sp.append(S.copy())
+                    es.append(e)
+                    us.append(u)
+                    S = a * S + u * kt[b, h, t]
+                G = dST[b, h, i].copy()
+                for t in reversed(range(T)):
+                    a, bt = alpha_k[b, h, t], beta[b, h, t]
+                    St = a * Sp[t] + us[t] * kt[b, h, t]
+                    G = G + dO[b, h, t, i] * q[b, h, t]
+                    du = G @ kt[b, h, t]
+                    dSb = G - bt * du * k[b, h, t]
+                    dq[b, h, t] += dO[b, h, t, i] * St
+                    dkt[b, h, t] += us[t] * G
+                    dk2[b, h, t] += -bt * du * a * Sp[t]
+                    db2[b, h, t] += du * es[t]
+                    da[b, h, t] += dSb * Sp[t]
+                    dv[b, h, t, i] = bt * du
+                    G = a * dSb
+                dS0[b, h, i] = G
+    return dict(dq=dq, dkt=dkt, dk2=dk2, dbeta2=db2, dalpha=da, dv=dv, dS0=dS0)
+
+
+def test_per_channel_decay_recurrences_match_reference():
+    x, cot = case(23, 8, 8, 121, gated=False)
+    rng = np.random.default_rng(122)
+    B, H, T, K = x["k"].shape
+    x["alpha"] = 0.6 + 0.4 * rng.random((B, H, T, K))
+    ref = reference(x, cot)
+    d0 = x["d0"]
+    kt = np.zeros_like(x["k"])
+    for b in range(B):
+        for h in range(H):
+            d = d0[b, h].copy()
+            for t in range(T):
+                kk = x["k"][b, h, t]
+                kt[b, h, t] = d * kk
+                w = kk ** 2
+                n = w.sum()
+                bt = x["beta"][b, h, t]
+                c = x["eta"] * bt * (1 - bt * (d @ w)) / n if n > 0 else 0.0
+                d = x["r"][b, h, t] * d + c * w
+    p2 = phase2_adjoint_per_channel(x["q"], x["k"], kt, x["v"], x["beta"], x["alpha"], x["S0"],
+                                    cot["o"], cot["ST"])
+    p1 = phase1_adjoint(x["k"], x["beta"], x["r"], x["eta"], d0, p2["dkt"] + cot["kt"],
+                        cot["dT"], p2["dk2"], p2["dbeta2"])
+    got = dict(q=p2["dq"], k=p1["dk"], v=p2["dv"], beta=p1["dbeta"], r=p1["dr"],
+               alpha=p2["dalpha"], d0=p1["dd0"], S0=p2["dS0"], eta=p1["deta"])
+    err = worst(got, ref, list(ref))
+    assert max(err.values()) < 1e-11, err
