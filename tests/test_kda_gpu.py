@@ -81,8 +81,10 @@ def test_equal_channels_match_the_scalar_gate():
     o1, S1 = ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"])
     o2, S2 = ops.chunk_fwd_kda(g["q"], g["k"], kt, g["v"], g["beta"], ak, g["S0"])
     torch.cuda.synchronize()
-    assert rel_err(o2, o1.double().cpu().numpy()) <= 1e-5
-    assert rel_err(S2, S1.double().cpu().numpy()) <= 1e-5
+    # the two kernels round differently (decay before or after the dot
+    # product), so they agree to the fp32 tolerance, not bit for bit
+    assert rel_err(o2, o1.double().cpu().numpy()) <= TOL["f32"]
+    assert rel_err(S2, S1.double().cpu().numpy()) <= TOL["f32"]
 
 
 BWD = [("f32", 64, 64, 50), ("f32", 128, 64, 5), ("bf16", 128, 128, 100), ("bf16", 64, 128, 33)]
