@@ -8,7 +8,8 @@ shares).  The kernels take ktilde as the forward produced it; here it is the
 oracle's Phase 1 output rounded to the I/O type, so that the comparison is
 about the backward alone.  Cases cover both I/O types, every (K, V) pair,
 one and several 16-token sub-chunks with ragged tails, T = 1 and T = 0,
-optional inputs and cotangents left out, a zero key, and determinism.
+optional inputs and cotangents left out, a zero key, and determinism; and
+the full shape the benchmark times, with its last head checked.
 """
 import numpy as np
 import pytest
@@ -138,3 +139,26 @@ def test_empty_sequence():
     assert torch.equal(got["eta"].cpu(), torch.zeros(1, 2))
     for n in ("q", "k", "v", "beta", "r", "alpha"):
         assert got[n].numel() == 0
+
+
+@pytest.mark.first_gpu_run
+def test_full_size_sampled_head():
+    # the shape `bench.py --backward` times (2 x 16 heads x 8192 tokens,
+    # d_k = d_v = 128, bf16, adaptive forgetting), output cotangent given;
+    # the last head (the largest offsets) against the reference gradients --
+    # heads are independent, so the sample is exact
+    w = synth.WORKLOADS["lm1p3b_apf_bf16"]
+    x = synth.make_inputs(w)
+    gen = torch.Generator().manual_seed(1)
+    dO = torch.randn(w.B, w.H, w.T, w.V, generator=gen).to(x["v"].dtype)
+    got = run(x, {"o": dO, "ST": None, "dT": None, "kt": None})
+    head = w.B * w.H - 1
+    xs = synth.slice_heads(x, [head])
+    ref = backward.grads(xs["q"], xs["k"], xs["v"], xs["beta"], xs["r"], xs["eta"], xs["d0"],
+                         xs["alpha"], xs["S0"], do=dO.reshape(-1, w.T, w.V)[head][None, None])
+    assert set(got) == set(ref), (sorted(got), sorted(ref))
+    errs = {}
+    for n, r in ref.items():
+        flat = got[n].reshape(-1, *got[n].shape[2:])[head]   # eta: this head's share
+        errs[n] = rel_err(flat, np.reshape(r, flat.shape))
+    assert max(errs.values()) <= TOL["bf16"], errs
