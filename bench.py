@@ -89,16 +89,16 @@ def precond_segments(BH, T, has_r):
     return (T + L - 1) // L if L < T else 1
 
 
-def launches_per_step(w, x):
+def launches_per_step(w, x, per_channel=False):
     """Kernels one step enqueues, by the library's own rules: the Phase 1
     segment scan (plus its verify kernel when a retention gate splits the
     sequences into time segments) and Phase 2 (for bf16 I/O a preparation
     and a chain launch per slab of at least 64 chunks, at most 64 slabs; one
-    fp32 kernel otherwise)."""
+    fp32 kernel otherwise, and one with a per-channel decay)."""
     BH, T = w.B * w.H, w.T
     nseg = precond_segments(BH, T, x["r"] is not None)
     p1 = 2 if nseg > 1 else 1
-    if w.io != "bf16":
+    if w.io != "bf16" or per_channel:
         return p1 + 1
     nch = (T + 63) // 64
     per = 64
@@ -586,6 +586,56 @@ def run_backward(args, local_rank):
         "clocks": clk, "gpu_launches": 3 * args.steps}), flush=True)
 
 
+def run_kda(args, local_rank):
+    """--kda: both phases with a decay per key channel (osdn_precond_scan +
+    osdn_chunk_fwd_kda) at the workload's shape, the decay drawn in
+    [0.9, 1) per token and channel.  Inputs are larger than L2; one JSON line
+    with the HBM roofline of the pass (the forward's bytes plus the
+    [B, H, T, K] fp32 decay)."""
+    from preconditioned_delta_rule_phase1_gb300 import ops
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    gen = torch.Generator().manual_seed(2)
+    ak = (0.9 + 0.1 * torch.rand(w.B, w.H, w.T, w.K, generator=gen)).to(dev)
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    stream = torch.cuda.current_stream(dev)
+    ws = ops.Workspace(device=dev)
+    step = lambda: ops.forward_kda(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"],
+                                   ak, g["S0"], workspace=ws, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(gpu_smi_id(dev, local_rank))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    assert ws.status(stream) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = phase1_bytes(w, x) + phase2_bytes(w, x) + w.B * w.H * w.T * w.K * 4
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "OSDN fwd tokens/s with a per-channel decay (phase1 + KDA-style phase2)",
+        "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": w.io, "data": "synthetic",
+        "config": {"workload": w.name + "_kda", "B": w.B, "H": w.H, "T": w.T, "d_k": w.K,
+                   "d_v": w.V, "l2": "inputs larger than L2"},
+        "roofline": {"kernel": "precond scan + delta_simt_kernel (per-channel)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "algorithmic_bytes": nbytes,
+                     "peak_source": peak_src, "traffic": None},
+        "clocks": clk,
+        "gpu_launches": args.steps * launches_per_step(w, x, per_channel=True)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -598,6 +648,8 @@ def main():
                     help="time the recurrent decode step instead of the forward pass")
     ap.add_argument("--backward", action="store_true",
                     help="time the gradients of both phases instead of the forward pass")
+    ap.add_argument("--kda", action="store_true",
+                    help="time both phases with a per-channel decay instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -607,6 +659,9 @@ def main():
         return
     if args.backward:
         run_backward(args, local_rank)
+        return
+    if args.kda:
+        run_kda(args, local_rank)
         return
     if world > 1:
         torch.distributed.init_process_group("gloo")
