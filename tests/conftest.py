@@ -17,5 +17,8 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # stable: the established tests keep their order, the new ones follow
-    items.sort(key=lambda item: item.get_closest_marker("first_gpu_run") is not None)
+    # stable sort: the forward pass's parity tests first (the evidence every
+    # other result builds on), then the rest in file order, then the tests
+    # of code that has not yet passed on a GPU
+    items.sort(key=lambda item: (item.get_closest_marker("first_gpu_run") is not None,
+                                 os.path.basename(str(item.fspath)) != "test_parity_gpu.py"))
