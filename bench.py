@@ -412,7 +412,7 @@ def run_ours(args, w, x, rank, world, local_rank):
         "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.io, "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "dtype": w.io, "data": "synthetic (seeded)",
         "config": {"workload": w.name, "B": B, "H": H, "T": T, "d_k": K, "d_v": V,
                    "io": w.io, "apf": w.apf, "gated": w.gated, "eta": w.eta,
                    "l2": "flushed before every timed step (write of 2x L2)",
