@@ -40,13 +40,19 @@ def _t(x, requires_grad=False):
     return t.requires_grad_(requires_grad)
 
 
-def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None):
+def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, ktilde=None):
     """Both phases, token by token, in float64 torch ops (differentiable).
 
     Shapes as in ``oracle.forward``; alpha may also be [B, H, T, K], a decay
     per key channel (``oracle.forward_kda``): S_t = S_{t-1} Diag(alpha_t) +
     beta_t (v_t - S_{t-1} Diag(alpha_t) k_t) ktilde_t^T.  Returns (ktilde, dT,
     o, ST).
+
+    ``ktilde`` [B, H, T, K], if given, is the value Phase 2 uses in place of
+    d_t (.) k_t -- the forward's stored keys, e.g. rounded to the I/O type --
+    while the derivative still flows through d_t (.) k_t (a straight-through
+    value).  The backward kernels take the stored ktilde, so this is the
+    exact derivative of what they differentiate.
     """
     B, H, T, K = k.shape
     V = v.shape[-1]
@@ -60,6 +66,8 @@ def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None):
         a = (d * w).sum(-1)
         bt = beta[:, :, t]
         ktil = d * kt                                       # preconditioner before the step
+        if ktilde is not None:                              # stored value, same derivative
+            ktil = ktil + (ktilde[:, :, t] - ktil).detach()
         safe_n = torch.where(n > 0, n, torch.ones_like(n))
         coef = torch.where(n > 0, eta * bt * (1.0 - bt * a) / safe_n, torch.zeros_like(n))
         rt = r[:, :, t] if r is not None else torch.ones_like(bt)
@@ -79,9 +87,10 @@ def forward_torch(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None):
 
 
 def grads(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, *, do=None, ddT=None,
-          dST=None, dkt=None):
+          dST=None, dkt=None, ktilde=None):
     """Gradients of L = <o, do> + <d_T, ddT> + <S_T, dST> + <ktilde, dkt> with
-    respect to every input (the cotangents that are None count as zero).
+    respect to every input (the cotangents that are None count as zero);
+    ``ktilde`` as in ``forward_torch`` (the stored keys Phase 2 uses).
 
     Returns a dict keyed like the inputs (q, k, v, beta, r, eta, d0, alpha,
     S0); an input given as None has no entry.  eta's entry is a float.
@@ -90,7 +99,7 @@ def grads(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, *, do=No
            "r": _t(r, True), "eta": _t(eta, True), "d0": _t(d0, True), "alpha": _t(alpha, True),
            "S0": _t(S0, True)}
     kt, dT, o, ST = forward_torch(ins["q"], ins["k"], ins["v"], ins["beta"], ins["r"], ins["eta"],
-                                  ins["d0"], ins["alpha"], ins["S0"])
+                                  ins["d0"], ins["alpha"], ins["S0"], _t(ktilde))
     loss = torch.zeros((), dtype=_F)
     for out, cot in ((o, do), (dT, ddT), (ST, dST), (kt, dkt)):
         if cot is not None:

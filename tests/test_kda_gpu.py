@@ -90,9 +90,12 @@ def test_equal_channels_match_the_scalar_gate():
 BWD = [("f32", 64, 64, 50), ("f32", 128, 64, 5), ("bf16", 128, 128, 100), ("bf16", 64, 128, 33)]
 
 
-def run_backward(x, cot):
+def stored_ktilde(x):
     kt, _ = oracle.precond_scan(x["k"], x["beta"], x["r"], x["eta"], x["d0"])
-    kt = torch.from_numpy(np.asarray(kt)).to(x["k"].dtype).contiguous()
+    return torch.from_numpy(np.asarray(kt)).to(x["k"].dtype).contiguous()
+
+
+def run_backward(x, cot, kt):
     g, c = to_cuda(x), to_cuda(cot)
     got = ops.backward_kda(g["q"], g["k"], kt.cuda(), g["v"], g["beta"], g["r"], g["eta"],
                            g["d0"], g["alpha"], g["S0"], do=c["o"], dST=c["ST"], ddT=c["dT"],
@@ -116,10 +119,11 @@ def cotangents(x, io, seed):
 def test_backward_matches_reference(io, K, V, T):
     x = case(io, K, V, T, 600 + T + K)
     cot = cotangents(x, io, 700 + T)
-    got = run_backward(x, cot)
+    kt = stored_ktilde(x)
+    got = run_backward(x, cot, kt)
     ref = backward.grads(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"],
                          x["alpha"], x["S0"], do=cot["o"], ddT=cot["dT"], dST=cot["ST"],
-                         dkt=cot["kt"])
+                         dkt=cot["kt"], ktilde=kt)
     assert set(got) == set(ref)
     errs = {}
     for n, r in ref.items():
@@ -132,7 +136,8 @@ def test_backward_matches_reference(io, K, V, T):
 def test_backward_deterministic():
     x = case("bf16", 128, 64, 45, 81)
     cot = cotangents(x, "bf16", 82)
-    a, b = run_backward(x, cot), run_backward(x, cot)
+    kt = stored_ktilde(x)
+    a, b = run_backward(x, cot, kt), run_backward(x, cot, kt)
     for n in a:
         assert torch.equal(a[n], b[n]), n
 

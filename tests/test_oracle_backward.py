@@ -92,3 +92,28 @@ def test_finite_differences_catch_a_dropped_retention_gate():
         xm["d0"][idx] -= h
         num[idx] = (c_loss(xp, cot) - c_loss(xm, cot)) / (2 * h)
     assert np.abs(wrong["d0"] - num).max() > 1e-3 * max(1.0, np.abs(num).max())
+
+
+def test_stored_ktilde_option():
+    # (1) with the exact ktilde the straight-through value changes nothing;
+    # (2) with a perturbed ktilde the forward is the C oracle's Phase 2 on
+    #     that ktilde (a separate implementation of the recurrence)
+    x = case(True, 64)
+    kt, dT, o, ST = oracle.forward(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"],
+                                   x["alpha"], x["S0"])
+    rng = np.random.default_rng(9)
+    cot = {"do": rng.standard_normal(o.shape), "dST": rng.standard_normal(ST.shape)}
+    plain = backward.grads(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"],
+                           x["alpha"], x["S0"], **cot)
+    same = backward.grads(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"],
+                          x["alpha"], x["S0"], ktilde=kt, **cot)
+    for n in plain:
+        np.testing.assert_allclose(same[n], plain[n], rtol=0,
+                                   atol=1e-12 * max(1.0, np.abs(plain[n]).max()), err_msg=n)
+    kt2 = kt * (1 + 1e-2 * rng.standard_normal(kt.shape))
+    t = {n: backward._t(x[n]) for n in ("q", "k", "v", "beta", "r", "d0", "alpha", "S0")}
+    _, _, o2, S2 = backward.forward_torch(t["q"], t["k"], t["v"], t["beta"], t["r"], x["eta"],
+                                          t["d0"], t["alpha"], t["S0"], backward._t(kt2))
+    o_ref, S_ref = oracle.delta_fwd(x["q"], x["k"], kt2, x["v"], x["beta"], x["alpha"], x["S0"])
+    np.testing.assert_allclose(o2.numpy(), o_ref, rtol=0, atol=1e-12 * np.abs(o_ref).max())
+    np.testing.assert_allclose(S2.numpy(), S_ref, rtol=0, atol=1e-12 * np.abs(S_ref).max())
