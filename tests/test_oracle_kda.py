@@ -155,3 +155,33 @@ def test_autograd_reference_matches_and_differentiates_the_kda_oracle():
             num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
         np.testing.assert_allclose(g[name], num, rtol=0, atol=1e-6 * max(1, np.abs(num).max()),
                                    err_msg=name)
+
+
+def test_golden_one_hot_fixture():
+    # exact rationals from tests/golden/make_kda_one_hot_fixture.py (closed
+    # form, no oracle call)
+    import os
+    from fractions import Fraction
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "kda_one_hot_closed_form.txt")
+    vals = {}
+    for line in open(path):
+        if line.startswith("#") or "=" not in line:
+            continue
+        key, rhs = (s.strip() for s in line.split("=", 1))
+        vals[key] = [float(Fraction(x)) for x in rhs.split()]
+    K, V = int(vals["K"][0]), int(vals["V"][0])
+    cols = [int(c) for c in vals["cols"]]
+    T = len(cols)
+    k = np.zeros((1, 1, T, K))
+    k[0, 0, np.arange(T), cols] = 1.0
+    q = np.array([vals["q_%d" % t] for t in range(T)])[None, None]
+    v = np.array([vals["v_%d" % t] for t in range(T)])[None, None]
+    alpha = np.array([vals["alpha_%d" % t] for t in range(T)])[None, None]
+    beta = np.array(vals["beta"])[None, None]
+    S0 = np.array([vals["S0_%d" % i] for i in range(V)])[None, None]
+    o, ST = oracle.delta_fwd_kda(q, k, k, v, beta, alpha, S0)
+    np.testing.assert_allclose(o[0, 0], np.array([vals["o_%d" % t] for t in range(T)]),
+                               rtol=0, atol=1e-14)
+    np.testing.assert_allclose(ST[0, 0], np.array([vals["ST_%d" % i] for i in range(V)]),
+                               rtol=0, atol=1e-14)
