@@ -18,7 +18,9 @@ Each pin fixes the result by something other than the oracle's own loop:
     c_tj = alpha_tj (1 - beta_t) if token t writes column j, else alpha_tj;
 (4) equal channels give the scalar-gated oracle (itself pinned elsewhere);
 (5) the autograd reference with a per-channel decay equals the C oracle's
-    forward and its gradients equal finite differences of it.
+    forward and its gradients equal finite differences of it;
+(6) a stored fixture of (3) in exact rationals (tests/golden/, written by a
+    closed-form script that calls no oracle).
 
 A decay applied along the value rows instead of the key columns fails (1).
 """
