@@ -77,14 +77,22 @@ def phase2_flops(w):
     return w.B * w.H * w.T * (6 * w.K * w.V + 2 * C * (w.K + w.V))
 
 
-def precond_segments(BH, T, has_r):
+def sm_count():
+    """SMs of the current device; the GB300 count (152) without one."""
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 152
+
+
+def precond_segments(BH, T, has_r, sms=None):
     """Time segments per sequence of the Phase 1 scan, by the library's rule:
     with a retention gate and T > 256, L halves from 1024 while all segments
-    still fit in 8 warps per SM of 152 (and stays >= 256); else one."""
+    still fit in 8 warps per SM (and stays >= 256); else one."""
     if not has_r or T <= 256:
         return 1
+    sms = sm_count() if sms is None else sms
     L = 1024
-    while L > 256 and BH * ((T + L // 2 - 1) // (L // 2)) <= 8 * 152:
+    while L > 256 and BH * ((T + L // 2 - 1) // (L // 2)) <= 8 * sms:
         L //= 2
     return (T + L - 1) // L if L < T else 1
 
@@ -221,6 +229,14 @@ def env_rank():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def workload_config(w, world):
+    """The `config` of a JSON line: the same keys on both arms."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.K, "d_v": w.V,
+            "io": w.io, "apf": w.apf, "gated": w.gated, "eta": w.eta,
+            "l2": "flushed before every timed step (write of 2x L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, w, x, rank, world):
     if rank != 0:
         return
@@ -242,14 +258,83 @@ def run_reference(args, w, x, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.K, "d_v": w.V,
-                   "io": w.io, "sample": sample},
+        "config": workload_config(w, world),
+        "sample": sample,
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
     }
     print(json.dumps(line), flush=True)
+
+
+def parity_sample(w, x, kt, dT, o, ST):
+    """Normwise max relative error of each output on the first and the last
+    sequence of the workload against the fp64 oracle on the same inputs."""
+    import oracle
+    BH = w.B * w.H
+    heads = sorted({0, BH - 1})
+    xs = synth.slice_heads(x, heads)
+    ref = oracle.forward(xs["q"], xs["k"], xs["v"], xs["beta"], xs["r"], xs["eta"], xs["d0"],
+                         xs["alpha"], xs["S0"])
+    errs = {}
+    for name, got, want in zip(("ktilde", "dT", "o", "ST"), (kt, dT, o, ST), ref):
+        flat = got.reshape(-1, *got.shape[2:])[heads].double().cpu().numpy()[None]
+        errs[name] = float(np.max(np.abs(flat - want)) / max(float(np.max(np.abs(want))), 1e-30))
+    return {"heads": heads, "max_rel_err": errs,
+            "tolerance": 1e-4 if w.io == "f32" else 2e-2}
+
+
+def measure_workload(w, dev, stream, steps, warmup, flush):
+    """Device time of both phases on one workload (inputs resident, L2 flushed
+    before every step), their HBM and tensor roofline fractions, and parity
+    of the last step's outputs on two sampled sequences."""
+    from preconditioned_delta_rule_phase1_gb300 import ops
+    x = synth.make_inputs(w)
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    B, H, T, K, V = w.B, w.H, w.T, w.K, w.V
+    ws = ops.Workspace(device=dev)
+    ws.ensure(max(ops.precond_scan_workspace_bytes(B, H, T, K),
+                  ops.chunk_fwd_workspace_bytes(int(w.io == "bf16"), B, H, T, K, V)))
+    kt = torch.empty_like(g["k"])
+    dT = torch.empty(B, H, K, device=dev)
+    o = torch.empty(B, H, T, V, dtype=g["v"].dtype, device=dev)
+    ST = torch.empty(B, H, V, K, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            flush.zero_()
+            if i >= warmup:
+                ev[i - warmup][0].record(stream)
+            ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], kt, dT, ws, stream)
+            if i >= warmup:
+                ev[i - warmup][1].record(stream)
+            ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], o, ST, ws,
+                          stream)
+            if i >= warmup:
+                ev[i - warmup][2].record(stream)
+    torch.cuda.synchronize(dev)
+    st = ws.status(stream)
+    if st != 0:
+        raise RuntimeError("device status on %s: %d" % (w.name, st))
+    t1 = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t2 = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    hbm_peak, bf16_peak, _ = load_peaks()
+    b1, b2 = phase1_bytes(w, x), phase2_bytes(w, x)
+    return {
+        "B": B, "H": H, "T": T, "d_k": K, "d_v": V, "io": w.io,
+        "apf": w.apf, "gated": w.gated, "steps": steps,
+        "phases_ms": {"precond_scan": t1, "chunk_fwd": t2},
+        "tokens_per_s": B * T / ((t1 + t2) * 1e-3),
+        "precond_scan": {"algorithmic_bytes": b1, "achieved_gbs": b1 / (t1 * 1e-3) / 1e9,
+                         "frac_hbm": b1 / (t1 * 1e-3) / 1e9 / hbm_peak},
+        "chunk_fwd": {"algorithmic_bytes": b2, "achieved_gbs": b2 / (t2 * 1e-3) / 1e9,
+                      "frac_hbm": b2 / (t2 * 1e-3) / 1e9 / hbm_peak,
+                      "tflops": phase2_flops(w) / (t2 * 1e-3) / 1e12,
+                      "frac_tensor": phase2_flops(w) / (t2 * 1e-3) / 1e12 / bf16_peak},
+        "parity": parity_sample(w, x, kt, dT, o, ST),
+        "launches_per_step": launches_per_step(w, x),
+    }
 
 
 def run_ours(args, w, x, rank, world, local_rank):
@@ -408,15 +493,21 @@ def run_ours(args, w, x, rank, world, local_rank):
         cpu = {"value": (th / w.H) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": "%d of %d sequences x first %d of %d tokens, %d times (%.1f s)"
                          % (n_seq, B * H, t_len, T, reps, dt)}
+    # the other workloads of the scope (parity cases, not bench lines): device
+    # time per phase, roofline fractions and sampled parity, one GPU only
+    workloads = None
+    if world == 1 and not args.no_workloads:
+        workloads = {}
+        for name in synth.WORKLOAD_ORDER:
+            wl = synth.WORKLOADS[name]
+            n = max(3, min(args.steps, 10))
+            workloads[name] = measure_workload(wl, dev, stream, n, 3, flush)
     line = {
         "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.io, "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "B": B, "H": H, "T": T, "d_k": K, "d_v": V,
-                   "io": w.io, "apf": w.apf, "gated": w.gated, "eta": w.eta,
-                   "l2": "flushed before every timed step (write of 2x L2)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(w, world),
         "phases_ms": {"precond_scan": t1, "chunk_fwd": t2},
         "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
@@ -433,6 +524,7 @@ def run_ours(args, w, x, rank, world, local_rank):
         "gpu_launches": launches_per_step(w, x) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
 
@@ -644,6 +736,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload table of the other configurations")
     ap.add_argument("--decode", action="store_true",
                     help="time the recurrent decode step instead of the forward pass")
     ap.add_argument("--backward", action="store_true",

@@ -178,6 +178,13 @@ int precond_scan_checked(int io, int B, int H, int T, int K, const void *k, cons
         overlap(dT, BH * K * 4, k, kbytes) || overlap(log_ratio, BH * 4, k, kbytes) ||
         overlap(log_ratio, BH * 4, ktilde, kbytes) || overlap(log_ratio, BH * 4, dT, BH * K * 4))
         return OSDN_ERR_ALIAS;
+    {   // the workspace is written by the call: it may overlap nothing else
+        const size_t gb = BH * (size_t)T * 4;
+        const void *all[7] = {k, beta, r, d0, ktilde, dT, log_ratio};
+        const size_t sz[7] = {kbytes, gb, gb, BH * K * 4, kbytes, BH * K * 4, BH * 4};
+        for (int i = 0; i < 7; ++i)
+            if (overlap(workspace, workspace_bytes, all[i], sz[i])) return OSDN_ERR_ALIAS;
+    }
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     void *scratch = static_cast<char *>(workspace) + kStatusBytes;
@@ -255,9 +262,12 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
     const void *ins[7] = {q, k, ktilde, v, beta, alpha, S0};
     const size_t insz[7] = {kb, kb, kb, vb, gb, gb, sb};
     for (int i = 0; i < 7; ++i)
-        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]))
+        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]) ||
+            overlap(workspace, workspace_bytes, ins[i], insz[i]))
             return OSDN_ERR_ALIAS;
-    if (overlap(o, vb, ST, sb)) return OSDN_ERR_ALIAS;
+    if (overlap(o, vb, ST, sb) || overlap(workspace, workspace_bytes, o, vb) ||
+        overlap(workspace, workspace_bytes, ST, sb))
+        return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     cudaError_t e;
@@ -304,7 +314,10 @@ int decode_checked(int io, int B, int H, int K, int V, const void *q, const void
             if (overlap(outs[a], outsz[a], ins[i], insz[i])) return OSDN_ERR_ALIAS;
         for (int b = a + 1; b < 4; ++b)
             if (overlap(outs[a], outsz[a], outs[b], outsz[b])) return OSDN_ERR_ALIAS;
+        if (overlap(workspace, workspace_bytes, outs[a], outsz[a])) return OSDN_ERR_ALIAS;
     }
+    for (int i = 0; i < 6; ++i)
+        if (overlap(workspace, workspace_bytes, ins[i], insz[i])) return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     cudaError_t e = per_channel
@@ -358,9 +371,9 @@ int backward_checked(int io, int B, int H, int T, int K, int V, const void *q, c
     if (BH == 0) return OSDN_OK;
     if (T > 0 && (!q || !k || !ktilde || !v || !beta || !dq || !dk || !dv || !dbeta))
         return OSDN_ERR_NULL;
-    const void *ins[14] = {q, k, ktilde, v, beta, r, d0, alpha, S0, d_o, d_ST, d_dT, d_ktilde,
-                           workspace};
+    const void *ins[13] = {q, k, ktilde, v, beta, r, d0, alpha, S0, d_o, d_ST, d_dT, d_ktilde};
     void *outs[9] = {dq, dk, dv, dbeta, dr, dalpha, dd0, dS0, deta};
+    if (misaligned(workspace)) return OSDN_ERR_ALIGN;
     for (const void *p : ins)
         if (misaligned(p)) return OSDN_ERR_ALIGN;
     for (const void *p : outs)
@@ -376,7 +389,10 @@ int backward_checked(int io, int B, int H, int T, int K, int V, const void *q, c
             if (overlap(outs[a], outsz[a], ins[i], insz[i])) return OSDN_ERR_ALIAS;
         for (int b = a + 1; b < 9; ++b)
             if (overlap(outs[a], outsz[a], outs[b], outsz[b])) return OSDN_ERR_ALIAS;
+        if (overlap(workspace, workspace_bytes, outs[a], outsz[a])) return OSDN_ERR_ALIAS;
     }
+    for (int i = 0; i < 13; ++i)
+        if (overlap(workspace, workspace_bytes, ins[i], insz[i])) return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     cudaStream_t st = (cudaStream_t)stream;
@@ -444,9 +460,12 @@ int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q,
     const void *ins[7] = {q, k, ktilde, v, beta, alpha_k, S0};
     const size_t insz[7] = {kb, kb, kb, vb, gb, ab, sb};
     for (int i = 0; i < 7; ++i)
-        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]))
+        if (overlap(o, vb, ins[i], insz[i]) || overlap(ST, sb, ins[i], insz[i]) ||
+            overlap(workspace, workspace_bytes, ins[i], insz[i]))
             return OSDN_ERR_ALIAS;
-    if (overlap(o, vb, ST, sb)) return OSDN_ERR_ALIAS;
+    if (overlap(o, vb, ST, sb) || overlap(workspace, workspace_bytes, o, vb) ||
+        overlap(workspace, workspace_bytes, ST, sb))
+        return OSDN_ERR_ALIAS;
     int dev = check_device();
     if (dev != OSDN_OK) return dev;
     cudaError_t e;

@@ -32,11 +32,15 @@
 // segment can start from a state estimated by running the scan over the W
 // tokens before it from d = 0 ("warm-up").  Every segment records its
 // estimated start and its end state; a second kernel checks each start
-// against the predecessor's end (exact by induction from d_0) and recomputes
-// any segment whose estimate is off by more than 2^-21 relative, or all
+// against the predecessor's end and recomputes any segment whose estimate is
+// off by more than 2^-21 of the largest entry of that end state, or all
 // segments after a token whose one-step map could expand (||A_t||_2 > 1).
-// The result is therefore the exact recurrence to fp32 rounding on every
-// input; speculation only decides how much runs in parallel.
+// An accepted start therefore differs from the state the sequential scan
+// would carry into the segment by at most 2^-21 of that state's largest
+// entry; the maps contract (that is what the check on ||A_t|| guarantees),
+// so such a difference shrinks through the segment and the differences of
+// the accepted segments add up to at most about nseg * 2^-21 relative, on
+// top of fp32 rounding.  Speculation only decides how much runs in parallel.
 //
 // Residual diagnostic (optional).  Writing ktilde_t into the state scales
 // the token's residual S k_t - v_t by 1 - beta_t <d_t, w_t> (section 3,
@@ -55,7 +59,7 @@ constexpr int C = 16;          // tokens per chunk
 constexpr int NST = 4;         // key chunks in flight per warp
 constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment
 constexpr int kMaxWarps = 4;   // warps (segments) per CTA
-constexpr int kSmCount = 152;  // SMs the segment count is sized for (GB300)
+constexpr int kDefaultSms = 152;  // GB300; used only when no device can be queried
 constexpr float kRelTol = 4.76837158203125e-07f;  // 2^-21
 
 // One warp's staging area.  Key rows are padded by 8 elements so that the
@@ -572,6 +576,18 @@ __global__ void copy_or_fill_kernel(size_t n, const float *__restrict__ src, flo
         dst[i] = src ? src[i] : fill;
 }
 
+// Streaming multiprocessors of the current device (the segment count and
+// the CTA shape are sized for one wave); the GB300 count when there is none.
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();   // clear the error a device-less query leaves behind
+        return kDefaultSms;
+    }
+    return n;
+}
+
 template <typename io_t, int K, bool HAS_R, bool LR>
 static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
@@ -583,7 +599,7 @@ static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     if (e0 != cudaSuccess) return e0;
     // few segments: one per CTA, so that they spread over the SMs
     const long long nwarps = (long long)p.BH * p.nseg;
-    const int wpc = nwarps >= 2LL * kSmCount ? kMaxWarps : 1;
+    const int wpc = nwarps >= 2LL * sm_count() ? kMaxWarps : 1;
     const unsigned grid = (unsigned)((nwarps + wpc - 1) / wpc);
     precond_segment_kernel<io_t, K, HAS_R, LR><<<grid, 32 * wpc, wpc * kStage, stream>>>(p);
     cudaError_t e = cudaGetLastError();
@@ -613,7 +629,8 @@ int precond_segments(int BH, int T, bool has_r, int *L_out) {
     int L = T;
     if (has_r && T > 2 * p1::kWarm) {
         L = 1024;
-        while (L > 2 * p1::kWarm && (long long)BH * cdiv(T, L / 2) <= 8LL * p1::kSmCount)
+        const long long sms = p1::sm_count();
+        while (L > 2 * p1::kWarm && (long long)BH * cdiv(T, L / 2) <= 8LL * sms)
             L >>= 1;
         if (L >= T) L = T;
     }

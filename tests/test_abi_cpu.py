@@ -87,6 +87,8 @@ def test_host_validation_precond_scan(L):
     assert scan(L, k=None) == -1 and scan(L, beta=None) == -1 and scan(L, kt=None) == -1
     assert scan(L, k=FAKE + 4) == -4 and scan(L, d0=FAKE + 8) == -4
     assert scan(L, kt=FAKE) == -9          # ktilde aliases k
+    assert scan(L, ws=FAKE) == -9          # the workspace overlaps k
+    assert scan(L, ws=2 * FAKE - 128) == -9   # ... runs into ktilde
     assert scan(L, B=0) == 0               # empty batch: nothing to do
 
 
@@ -110,6 +112,8 @@ def test_host_validation_chunk_fwd(L):
     assert chunk(L, q=None) == -1 and chunk(L, o=None) == -1
     assert chunk(L, v=4 * FAKE + 2) == -4
     assert chunk(L, o=FAKE) == -9          # o aliases q
+    assert chunk(L, ws=6 * FAKE) == -9     # the workspace overlaps o
+    assert chunk(L, ws=FAKE) == -9         # ... or an input
     assert chunk(L, wsb=0) == -5
     need = L.osdn_chunk_fwd_workspace_bytes(1, 1, 1, 8, 64, 64)
     assert chunk(L, wsb=need - 1) == -5
@@ -162,6 +166,8 @@ def test_host_validation_decode_step(L):
     assert decode(L, k=2 * FAKE + 4) == -4
     assert decode(L, o=FAKE) == -9          # o aliases q
     assert decode(L, S=5 * FAKE) == -9      # S overlaps d
+    assert decode(L, ws=7 * FAKE) == -9     # the workspace overlaps o
+    assert decode(L, ws=2 * FAKE) == -9     # ... or an input
     assert decode(L, H=0) == 0
 
 
@@ -198,6 +204,9 @@ def test_host_validation_backward(L):
     assert bwd(L, outs={"dS0": 11 * FAKE}) == -9        # dS0 aliases the cotangent d_ST
     assert bwd(L, outs={"dr": 17 * FAKE + 16}) == -9    # dr overlaps dbeta (8 tokens, 32 bytes)
     assert bwd(L, outs={"dr": 17 * FAKE + 32}) != -9    # ... and starts right after it
+    assert bwd(L, ws=14 * FAKE) == -9                   # the workspace overlaps dq
+    assert bwd(L, ws=FAKE) == -9                        # ... or an input
+    assert bwd(L, ws=22 * FAKE - 64) == -9              # ... runs into deta
     assert bwd(L, H=0) == 0
 
 
@@ -228,6 +237,8 @@ def test_host_validation_chunk_fwd_kda(L):
     assert kda(L, q=None) == -1 and kda(L, o=None) == -1 and kda(L, beta=None) == -1
     assert kda(L, ak=8 * FAKE + 4) == -4
     assert kda(L, o=FAKE) == -9                   # o aliases q
+    assert kda(L, ws=6 * FAKE) == -9              # the workspace overlaps o
+    assert kda(L, ws=4 * FAKE) == -9              # ... or an input
     # alpha_k is [B][H][T][K] fp32: 8 tokens x 64 channels = 2048 bytes
     assert kda(L, ak=8 * FAKE, o=8 * FAKE + 2032) == -9
     assert kda(L, ak=8 * FAKE, o=8 * FAKE + 2048) != -9

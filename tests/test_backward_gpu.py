@@ -147,7 +147,6 @@ def test_empty_sequence():
         assert got[n].numel() == 0
 
 
-@pytest.mark.first_gpu_run
 def test_full_size_sampled_head():
     # the shape `bench.py --backward` times (2 x 16 heads x 8192 tokens,
     # d_k = d_v = 128, bf16, adaptive forgetting), output cotangent given;

@@ -17,7 +17,7 @@ from preconditioned_delta_rule_phase1_gb300 import build as osdn_build
 from preconditioned_delta_rule_phase1_gb300 import ops, synth
 from tests._util import TOL, rel_err, to_cuda
 
-pytestmark = [pytest.mark.gpu, pytest.mark.first_gpu_run]
+pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module", autouse=True)
