@@ -23,7 +23,9 @@
 // tcgen05 MMAs.  The outputs are staged in shared memory in the tensor maps'
 // box layout, in tiles the kernel no longer needs, and leave by TMA stores.
 // 90 KB of shared memory and 256 TMEM columns: two CTAs share an SM and hide
-// each other's latency.
+// each other's latency.  A decay alpha that is not positive and finite (its
+// log enters the algebra), or a beta that is not finite, is recorded in the
+// status word as OSDN_ERR_DEVICE.
 #include "tc_common.cuh"
 
 namespace osdn {
@@ -274,13 +276,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (warp == 0) {
             // beta (0 past T) and the inclusive cumulative log alpha, two tokens a lane
             float bb[2], lg[2];
+            bool bad = false;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int i = 2 * lane + e;
                 const bool valid = i < nvalid;
                 bb[e] = valid ? p.beta[(size_t)seq * T + t0 + i] : 0.0f;
-                lg[e] = (GATED && valid) ? logf(p.alpha[(size_t)seq * T + t0 + i]) : 0.0f;
+                const float a = (GATED && valid) ? p.alpha[(size_t)seq * T + t0 + i] : 1.0f;
+                // the chunk algebra takes log alpha: a decay must be positive and finite
+                bad |= !isfinite(bb[e]) || !(a > 0.0f) || !isfinite(a);
+                lg[e] = (GATED && valid) ? logf(a) : 0.0f;
             }
+            if (bad) report_status(p.status, OSDN_ERR_DEVICE);
             float sc = lg[0] + lg[1];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {

@@ -55,6 +55,7 @@ constexpr int kThreads = 480;
 constexpr uint32_t kColS = 0;   // S^T (M=K), 64 columns
 constexpr uint32_t kColO = 64;  // O (M=64), two buffers of 64 columns
 constexpr uint32_t kTmemCols = 256;
+constexpr float kSpecTol = 1.52587890625e-05f;   // 2^-16: a speculative start accepted this close
 
 // Shared memory: ring X stages ([W | M] as K-row blocks of 64 columns, then
 // V), ring Y stages ([Ae | Qe] as 64-row blocks of 64 columns, then V), and
@@ -77,6 +78,17 @@ struct Params {
     const float *S0, *gc;
     __nv_bfloat16 *o;
     float *ST;
+    // Speculative time segments (seg_len > 0; grid z = segment): segment z
+    // owns chunks [z L, (z+1) L); for z > 0 it starts from a zero state `warm`
+    // chunks early, records the state it reaches at z L in seg_spec[z] and
+    // writes O only from z L on.  Its end state goes to seg_end[z], the last
+    // segment's to ST.
+    int seg_len, warm, nseg;
+    float *seg_spec, *seg_end;   // [nseg][BH][V][K]
+    // Repair launch: when `check` is given, a CTA first compares its rows of
+    // `check` (a speculative start) with S0 (the exact start) and leaves at
+    // once if they agree to kSpecTol of S0's largest entry.
+    const float *check;
     int *status;
     // Test hook (environment variable OSDN_TEST_STALL_CHAIN): the producer
     // issues nothing, so the waits run out -- after these limits, shortened
@@ -114,7 +126,50 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;
     const int seq = blockIdx.y, v0 = blockIdx.x * BV;
-    const int T = p.T, nch = p.nch, cbase = p.c0, ncs = p.ncs;
+    const int T = p.T, nch = p.nch;
+    // this CTA's chunks, the first whose output it writes, the chunk whose
+    // entering state it records (-1: none), and its start and end states
+    int cbase = p.c0, ncs = p.ncs, emit_from = p.c0, record_c = -1;
+    const float *S0 = p.S0;
+    float *ST = p.ST;
+    float *spec = nullptr;
+    const size_t sstride = (size_t)gridDim.y * p.V * K;   // one [BH][V][K] state
+    if (p.seg_len > 0) {
+        const int z = blockIdx.z, L = p.seg_len;
+        cbase = z == 0 ? 0 : z * L - p.warm;
+        ncs = min(nch, (z + 1) * L) - cbase;
+        emit_from = z * L;
+        record_c = z == 0 ? -1 : z * L;
+        S0 = z == 0 ? p.S0 : nullptr;
+        ST = z == p.nseg - 1 ? p.ST : p.seg_end + z * sstride;
+        spec = z == 0 ? nullptr : p.seg_spec + z * sstride;
+    }
+    if (p.check) {
+        // repair launch: leave if this CTA's rows of the speculative start
+        // agree with the exact start (the predecessor's end) already
+        __shared__ unsigned s_diff, s_mag;
+        if (tid == 0) s_diff = s_mag = 0u;
+        __syncthreads();
+        float diff = 0.0f, mag = 0.0f;
+        for (int i = tid; i < BV * K; i += kThreads) {
+            const size_t at = ((size_t)seq * p.V + v0 + i / K) * K + i % K;
+            const float a = S0[at], b = p.check[at];
+            diff = fmaxf(diff, fabsf(a - b));
+            mag = fmaxf(mag, fabsf(a));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, m));
+            mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, m));
+        }
+        // non-negative floats order like their bit patterns (a NaN compares high)
+        if (lane == 0) {
+            atomicMax(&s_diff, __float_as_uint(diff));
+            atomicMax(&s_mag, __float_as_uint(mag));
+        }
+        __syncthreads();
+        if (__uint_as_float(s_diff) <= kSpecTol * __uint_as_float(s_mag)) return;
+    }
     auto stX = [&](int j) { return smem + LY::oX + (j % NS) * LY::kX; };
     auto stY = [&](int j) { return smem + LY::oY + (j % NS) * LY::kY; };
     // the bf16 copy of the state entering chunk c
@@ -266,7 +321,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::named_bar(3, 128);
             if (ot == 0) ptx::mbar_arrive(&bars.o_free[j & 1]);
             const int t = (cbase + j) * C + trow;
-            if (lane < 16 && t < T) st_global_bf16(p.o + ((size_t)seq * T + t) * p.V + v0, o, 64);
+            if (lane < 16 && t < T && cbase + j >= emit_from)
+                st_global_bf16(p.o + ((size_t)seq * T + t) * p.V + v0, o, 64);
         }
     } else {
         // ======================================================== state
@@ -280,7 +336,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             float sv[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-                sv[e] = (act && p.S0) ? p.S0[((size_t)seq * p.V + v0 + c0 + e) * K + krow] : 0.0f;
+                sv[e] = (act && S0) ? S0[((size_t)seq * p.V + v0 + c0 + e) * K + krow] : 0.0f;
             if (act) st_row_sw128(sS(0), K, krow, c0, sv, 32);
             float lo[16], hi[16];
 #pragma unroll
@@ -311,11 +367,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             float sv[32];
             tmem_ld32(tS, sv);
             if (last) {
-                if (act && p.ST) {
+                if (act && ST) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) p.ST[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
+                    for (int e = 0; e < 32; ++e) ST[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
                 }
                 break;
+            }
+            if (act && cbase + j + 1 == record_c) {   // the state entering the segment's first chunk
+#pragma unroll
+                for (int e = 0; e < 32; ++e) spec[((size_t)seq * p.V + v0 + c0 + e) * K + krow] = sv[e];
             }
             if (GATED) {  // the next chunk's decay, applied before its update
                 float lo[16], hi[16];
@@ -344,13 +404,23 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// What a chain launch does beyond its chunk range: the speculative pass over
+// time segments (grid z = segment), or a repair launch that first checks
+// each CTA's speculative start (see Params).
+struct ChainOpt {
+    int seg_len = 0, warm = 0, nseg = 0;
+    float *seg_spec = nullptr, *seg_end = nullptr;
+    const float *check = nullptr;
+};
+
 // Chunks [c0, c1) of every sequence, from the state S0 (NULL: zeros) to ST
 // (NULL: not written).
 template <int K, bool GATED>
 cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
                            const __nv_bfloat16 *w, const __nv_bfloat16 *m,
                            const __nv_bfloat16 *qe, const __nv_bfloat16 *ae, const float *gc,
-                           const float *S0, void *o, float *ST, int *status, cudaStream_t stream) {
+                           const float *S0, void *o, float *ST, int *status, cudaStream_t stream,
+                           const ChainOpt &opt) {
     const int nch = (T + C - 1) / C, Tp = nch * C;
     CUtensorMap mw, mm, mae, mqe, mv;
     if (!make_map(&mw, w, BH, nch * K, C) || !make_map(&mm, m, BH, nch * K, K) ||
@@ -373,34 +443,67 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
     p.gc = gc;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.ST = ST;
+    p.seg_len = opt.seg_len;
+    p.warm = opt.warm;
+    p.nseg = opt.nseg;
+    p.seg_spec = opt.seg_spec;
+    p.seg_end = opt.seg_end;
+    p.check = opt.check;
     p.status = status;
     p.stall = std::getenv("OSDN_TEST_STALL_CHAIN") != nullptr ? 1 : 0;
     p.bar_limit = p.stall ? 64u : kWaitLimit;
     p.poll_limit = p.stall ? (1u << 14) : (kWaitLimit << 11);
-    dim3 grid(V / BV, BH);
+    dim3 grid(V / BV, BH, opt.seg_len > 0 ? opt.nseg : 1);
     chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
     return cudaGetLastError();
 }
 
+// Time segments of the chain with a decay (the state then forgets its start):
+// as many as keep one wave of chain CTAs (one per SM), with at least
+// kMinSegChunks chunks each; 1 when that leaves a single segment.
+constexpr int kMinSegChunks = 16;
+constexpr int kWarmChunks = 4;   // warm-up of a speculative segment: 256 tokens
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+int chain_segments(int BH, int T, int V) {
+    const long long nch = ((long long)T + C - 1) / C;
+    const long long ctas = (long long)BH * (V / BV);
+    long long n = ctas > 0 ? sm_count() / ctas : 1;
+    n = std::min(n, nch / kMinSegChunks);
+    return (int)std::max(1LL, n);
+}
+
 // Workspace carve-up: the prepared operands (W and M per chunk, K rows each;
-// Qe and Ae per token, chunk-padded; g_C per chunk) and two fp32 states
-// [BH][V][K] that carry S from one slab of chunks to the next.
+// Qe and Ae per token, chunk-padded; g_C per chunk), two fp32 states
+// [BH][V][K] that carry S from one slab of chunks to the next, and, where the
+// chain may run in time segments, each segment's speculative start and end
+// state.
 struct Carve {
     __nv_bfloat16 *w, *m, *qe, *ae;
-    float *gc, *state[2];
+    float *gc, *state[2], *seg_spec, *seg_end;
+    int nseg;
     size_t bytes;
 };
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 Carve carve(void *base, int BH, int T, int K, int V) {
     const size_t nch = (size_t)(T + C - 1) / C, Tp = nch * C;
-    const size_t sz[7] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
+    const int nseg = chain_segments(BH, T, V);
+    const size_t segb = nseg > 1 ? round256((size_t)nseg * BH * V * K * 4) : 0;
+    const size_t sz[9] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
                           round256((size_t)BH * Tp * K * 2), round256((size_t)BH * Tp * C * 2),
                           round256((size_t)BH * nch * 4), round256((size_t)BH * V * K * 4),
-                          round256((size_t)BH * V * K * 4)};
+                          round256((size_t)BH * V * K * 4), segb, segb};
     char *b = static_cast<char *>(base);
-    char *ptrs[7];
+    char *ptrs[9];
     size_t off = 0;
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 9; ++i) {
         ptrs[i] = b ? b + off : nullptr;
         off += sz[i];
     }
@@ -412,6 +515,9 @@ Carve carve(void *base, int BH, int T, int K, int V) {
     c.gc = reinterpret_cast<float *>(ptrs[4]);
     c.state[0] = reinterpret_cast<float *>(ptrs[5]);
     c.state[1] = reinterpret_cast<float *>(ptrs[6]);
+    c.seg_spec = reinterpret_cast<float *>(ptrs[7]);
+    c.seg_end = reinterpret_cast<float *>(ptrs[8]);
+    c.nseg = nseg;
     c.bytes = off;
     return c;
 }
@@ -489,15 +595,45 @@ cudaError_t prep_range(int BH, int T, int K, int c0, int c1, const void *q, cons
 }
 cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void *v, const float *alpha,
                         const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const tc::ChainOpt &opt = tc::ChainOpt()) {
     if (K == 128) {
         if (alpha)
-            return tc::chain_launch_t<128, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
-        return tc::chain_launch_t<128, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+            return tc::chain_launch_t<128, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+        return tc::chain_launch_t<128, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
     }
     if (alpha)
-        return tc::chain_launch_t<64, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
-    return tc::chain_launch_t<64, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream);
+        return tc::chain_launch_t<64, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+    return tc::chain_launch_t<64, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+}
+
+// With a decay the state forgets where it started, so the chain can run in
+// time segments: every segment but the first starts from a zero state a few
+// chunks early (speculative pass, all segments at once); then, in segment
+// order, each segment's recorded start is compared with its predecessor's
+// end and, where they differ by more than 2^-16 of that end's largest entry,
+// the segment is recomputed from that exact end.  Every accepted start is
+// therefore that close to the state the unsegmented chain would carry in.
+cudaError_t chain_segmented(int BH, int T, int K, int V, int nch, const void *v, const float *alpha,
+                            const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
+                            cudaStream_t stream) {
+    const int nseg = w.nseg, L = (nch + nseg - 1) / nseg;
+    const size_t sstride = (size_t)BH * V * K;
+    tc::ChainOpt spec;
+    spec.seg_len = L;
+    spec.warm = tc::kWarmChunks;
+    spec.nseg = (nch + L - 1) / L;
+    spec.seg_spec = w.seg_spec;
+    spec.seg_end = w.seg_end;
+    cudaError_t e = chain_range(BH, T, K, V, 0, nch, v, alpha, w, S0, o, ST, status, stream, spec);
+    for (int i = 1; e == cudaSuccess && i < spec.nseg; ++i) {
+        tc::ChainOpt rep;
+        rep.check = w.seg_spec + i * sstride;
+        const int c0 = i * L, c1 = std::min(nch, c0 + L);
+        float *sout = i == spec.nseg - 1 ? ST : w.seg_end + i * sstride;
+        e = chain_range(BH, T, K, V, c0, c1, v, alpha, w, w.seg_end + (i - 1) * sstride, o, sout,
+                        status, stream, rep);
+    }
+    return e;
 }
 }  // namespace
 
@@ -511,6 +647,11 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
     int per = tc::kSlabChunks;
     while ((nch + per - 1) / per > tc::kMaxSlabs) per *= 2;
     const int nslab = (nch + per - 1) / per;
+    if (alpha && w.nseg > 1) {  // a decay: every chunk prepared, then the chain in time segments
+        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);
+        if (e != cudaSuccess) return e;
+        return chain_segmented(BH, T, K, V, nch, v, alpha, w, S0, o, ST, status, stream);
+    }
     if (nslab <= 1) {  // one slab: preparation, then the chain, on the caller's stream
         cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);
         if (e != cudaSuccess) return e;

@@ -132,16 +132,20 @@ def test_chunk_fwd_workspace_size(L):
     # fp32 I/O and empty sequences need only the status word; bf16 keeps each
     # chunk's prepared operands: W (K x 64) and M (K x K) per chunk, Qe (2K
     # bytes a row) and Ae (128 bytes a row) on the chunk-padded length, g_C
-    # per chunk, and two fp32 states carried between slabs of chunks
+    # per chunk, two fp32 states carried between slabs of chunks, and, where
+    # the chain can run in time segments (as many as keep one chain CTA per
+    # SM of 152, at least 16 chunks each), each segment's start and end state
     assert L.osdn_chunk_fwd_workspace_bytes(0, 2, 3, 100, 128, 64) == 256
     assert L.osdn_chunk_fwd_workspace_bytes(1, 2, 3, 0, 128, 64) == 256
-    for B, H, T, K in [(1, 1, 1, 64), (2, 3, 100, 128), (1, 16, 65536, 128)]:
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (1, 16, 65536, 128, 64),
+                          (1, 16, 65536, 128, 128), (64, 32, 8192, 128, 128), (1, 2, 3217, 64, 64)]:
         BH, Tp, nch = B * H, -(-T // 64) * 64, -(-T // 64)
         r = lambda x: -(-x // 256) * 256
-        V = 64
+        nseg = max(1, min(152 // (BH * V // 64), nch // 16))
+        seg = 2 * r(nseg * BH * V * K * 4) if nseg > 1 else 0
         want = (256 + r(BH * nch * K * 64 * 2) + r(BH * nch * K * K * 2) + r(BH * Tp * K * 2)
-                + r(BH * Tp * 64 * 2) + r(BH * nch * 4) + 2 * r(BH * V * K * 4))
-        assert L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, 64) == want
+                + r(BH * Tp * 64 * 2) + r(BH * nch * 4) + 2 * r(BH * V * K * 4) + seg)
+        assert L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, V) == want, (B, H, T, K, V)
 
 
 def test_no_gpu_means_cuda_error_not_crash(L):

@@ -188,14 +188,37 @@ def test_segmented_scan_many_accepted_segments_fp32():
 
 @pytest.mark.parametrize("nfull", [128, 256 + 64])
 def test_phase2_slabs_with_ragged_last_slab(nfull):
-    # nfull chunks of 64 tokens and a ragged one: the bf16 Phase 2 runs them
-    # as slabs of 64 chunks and a last one of 1 chunk, preparing later slabs
-    # while earlier ones run and carrying the state between slabs; decay, S0
-    # and S_T all cross the slab seams
+    # nfull chunks of 64 tokens and a ragged one: without a decay the bf16
+    # Phase 2 runs them as slabs of 64 chunks and a last one of 1 chunk,
+    # preparing later slabs while earlier ones run and carrying the state
+    # between slabs; S0 and S_T cross the slab seams
     T = 64 * nfull + 37
-    x = synth.make_random(1, 2, T, 64, 64, io="bf16", apf=True, gated=True, s0=True, d0=True,
+    x = synth.make_random(1, 2, T, 64, 64, io="bf16", apf=True, gated=False, s0=True, d0=True,
                           seed=21)
     check_all(x, "bf16", None, "slabs T=%d" % T)
+
+
+@pytest.mark.parametrize("case", ["accepted", "all_repaired", "one_repaired", "ragged",
+                                  "wide_rows"])
+def test_phase2_time_segments_with_decay(case):
+    # With a decay the bf16 chain runs in time segments (here 3 of 16 chunks):
+    # every segment but the first starts from a zero state 4 chunks early, and
+    # a start that does not match its predecessor's end is recomputed.
+    # accepted: the synthetic decay forgets the warm-up's guess; all_repaired:
+    # a decay of 0.9999 does not, every later segment is recomputed;
+    # one_repaired: no decay over the first segment's last 4 chunks, so only
+    # the second segment's start is off; ragged: a ragged last chunk and
+    # segment; wide_rows: K = V = 128 (two CTAs of 64 value rows a sequence,
+    # each deciding for its own rows)
+    K = V = 128 if case == "wide_rows" else 64
+    T = 64 * 51 + 17 if case == "ragged" else 64 * 48
+    x = synth.make_random(1, 2, T, K, V, io="bf16", apf=True, gated=True, s0=True, d0=True,
+                          seed=41)
+    if case == "all_repaired":
+        x["alpha"] = torch.full_like(x["alpha"], 0.9999)
+    if case == "one_repaired":
+        x["alpha"][:, :, 64 * 12:64 * 16] = 1.0
+    check_all(x, "bf16", None, "segments %s" % case)
 
 
 def test_concurrent_calls_share_the_library_streams():
@@ -226,3 +249,25 @@ def test_concurrent_calls_share_the_library_streams():
     for i in range(2):
         for a, b in zip(out[i], ref[i]):
             assert torch.equal(a, b), "thread %d" % i
+
+
+@pytest.mark.parametrize("bad", ["alpha_zero", "alpha_negative", "beta_nan"])
+def test_invalid_gates_reported_by_the_device(bad):
+    # the bf16 chunk pass takes log alpha: a decay that is not positive (or a
+    # beta that is not finite) is recorded in the status word as
+    # OSDN_ERR_DEVICE; nothing faults and the next call is clean
+    x = synth.make_random(1, 2, 200, 64, 64, io="bf16", apf=True, gated=True, seed=51)
+    g = to_cuda(x)
+    if bad == "alpha_zero":
+        g["alpha"][0, 1, 70] = 0.0
+    if bad == "alpha_negative":
+        g["alpha"][0, 0, 3] = -0.5
+    if bad == "beta_nan":
+        g["beta"][0, 1, 199] = float("nan")
+    ws = ops.Workspace()
+    kt, _ = ops.precond_scan(g["k"], g["beta"].nan_to_num(0.5), g["r"], g["eta"])
+    ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == -8, ops.status_string(ws.status())
+    ws2 = ops.Workspace()
+    run_gpu(x, ws2)
