@@ -55,7 +55,11 @@
  *  the call in flight (calls that use one workspace concurrently on
  *  different streams race on it).  Zero the first 256 bytes once before the
  *  first call (osdn_workspace_init does that on a stream); the status word is
- *  sticky until the caller zeroes it again.
+ *  sticky until the caller zeroes it again.  The header's second word is a
+ *  test word: while it is nonzero, the bf16 osdn_chunk_fwd's state recurrence
+ *  loads nothing and shortens its bounded waits, so that they run out and the
+ *  status word reads OSDN_ERR_TIMEOUT -- the way the timeout path is
+ *  exercised without a fault.  Keep it zero otherwise.
  */
 #ifndef OSDN_H
 #define OSDN_H
@@ -71,13 +75,15 @@ typedef enum { OSDN_F32 = 0, OSDN_BF16 = 1 } osdn_dtype;
 typedef enum {
     OSDN_OK = 0,
     OSDN_ERR_NULL = -1,      /* a required pointer is NULL                     */
-    OSDN_ERR_DIMS = -2,      /* negative size, B*H > 65535, or K / V not in {64, 128} */
+    OSDN_ERR_DIMS = -2,      /* negative size, B*H > 2^24, or K / V not in {64, 128} */
     OSDN_ERR_DTYPE = -3,     /* io is not OSDN_F32 / OSDN_BF16                 */
     OSDN_ERR_ALIGN = -4,     /* a pointer is not 16-byte aligned               */
     OSDN_ERR_WORKSPACE = -5, /* workspace NULL or smaller than required        */
     OSDN_ERR_CUDA = -6,      /* the CUDA runtime rejected a launch or query    */
     OSDN_ERR_TIMEOUT = -7,   /* device: a bounded wait ran out (status word)   */
-    OSDN_ERR_DEVICE = -8,    /* device: an internal consistency check failed   */
+    OSDN_ERR_DEVICE = -8,    /* device: an input checked on the device is invalid
+                                (osdn_chunk_fwd, bf16: a decay alpha that is not
+                                positive and finite, or a beta that is not finite) */
     OSDN_ERR_ALIAS = -9,     /* an output overlaps an input it must not alias  */
     OSDN_ERR_ARCH = -10,     /* the current device is not sm_103 (GB300)       */
     OSDN_ERR_SCRATCH = -11   /* osdn_precond_scan_noalloc: shape needs more

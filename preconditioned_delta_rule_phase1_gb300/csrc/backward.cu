@@ -123,7 +123,7 @@ __device__ __forceinline__ float decayed_pred(const float (&S)[NC], const float 
 // ---------------------------------------------------------------- kernel 1
 template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(kBwdRows * 32)
-state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
+state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
                      const io_t *__restrict__ k, const io_t *__restrict__ kt,
                      const io_t *__restrict__ v, const float *__restrict__ beta,
                      const float *__restrict__ alpha, const float *__restrict__ S0,
@@ -140,7 +140,8 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x, nrb = gridDim.x;
     const int i = rb * kBwdRows + warp;               // this warp's value row
-    const size_t seq = blockIdx.y;
+    const size_t seq = grid_seq();
+    if (seq >= (size_t)BH) return;
     const int c0 = lane * NC;
     const size_t tok0 = seq * (size_t)T;               // first token of the sequence
     float *Spw = Sp + warp * kBwdSub * K;
@@ -269,12 +270,13 @@ state_adjoint_kernel(int T, int V, int nsub, const io_t *__restrict__ q,
 // ---------------------------------------------------------------- kernel 2
 template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(256)
-partial_sum_kernel(int T, int nrb, const float *__restrict__ part,
+partial_sum_kernel(int BH, int T, int nrb, const float *__restrict__ part,
                    const io_t *__restrict__ dkt_ext, io_t *__restrict__ dq,
                    float *__restrict__ dalpha, float *__restrict__ dkt_tot,
                    float *__restrict__ dk2, float *__restrict__ db2) {
     constexpr int P = bwd_part_width(K, PCH);
-    const size_t seq = blockIdx.y;
+    const size_t seq = grid_seq();
+    if (seq >= (size_t)BH) return;
     const int tb = blockIdx.x * kSumTok;
     for (int x = threadIdx.x; x < kSumTok * P; x += blockDim.x) {
         const int tt = x / P, col = x % P;
@@ -474,13 +476,13 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
     auto *k1 = state_adjoint_kernel<io_t, K, PCH>;
     cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
     if (e != cudaSuccess) return e;
-    k1<<<dim3(nrb, BH), kBwdRows * 32, smem, stream>>>(
-        T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
+    k1<<<seq_grid(nrb, BH), kBwdRows * 32, smem, stream>>>(
+        BH, T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
         static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
         static_cast<const io_t *>(dO), dST, static_cast<io_t *>(dv), dS0, s.ck2, s.part);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    partial_sum_kernel<io_t, K, PCH><<<dim3(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
-        T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
+    partial_sum_kernel<io_t, K, PCH><<<seq_grid(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
+        BH, T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
         s.dkt_tot, s.dk2, s.db2);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     precond_adjoint_kernel<io_t, K><<<(BH + kBwdSeqs - 1) / kBwdSeqs, kBwdSeqs * 32, 0, stream>>>(

@@ -13,6 +13,7 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
                                 cudaStream_t stream);
 size_t precond_scratch_bytes(int BH, int T, int K);
 size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r);
+int precond_segments(int BH, int T, bool has_r, int *L_out);
 size_t precond_noalloc_capacity();
 cudaError_t precond_scan_noalloc_launch(int io, int BH, int T, int K, const void *k,
                                         const float *beta, const float *r, float eta,
@@ -57,9 +58,11 @@ constexpr size_t kStatusBytes = 256;
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// Sequences map to the second grid dimension, so B*H is capped at its limit.
+// At most 2^24 sequences: the kernels spread them over two grid dimensions,
+// and the Phase 1 scan numbers its speculative segments in a 32-bit index.
+constexpr size_t kMaxSeqs = size_t(1) << 24;
 bool dims_ok(int B, int H, int T) {
-    return B >= 0 && H >= 0 && T >= 0 && (size_t)B * (size_t)H <= 65535;
+    return B >= 0 && H >= 0 && T >= 0 && (size_t)B * (size_t)H <= kMaxSeqs;
 }
 bool width_ok(int x) { return x == 64 || x == 128; }
 // The tensor-core Phase 2 addresses each chunk's rows of its prepared
@@ -96,7 +99,7 @@ const char *osdn_status_string(int code) {
     switch (code) {
     case OSDN_OK: return "ok";
     case OSDN_ERR_NULL: return "a required pointer is NULL";
-    case OSDN_ERR_DIMS: return "bad dimensions (negative size, B*H over 65535, or K/V not 64 or 128)";
+    case OSDN_ERR_DIMS: return "bad dimensions (negative size, B*H over 2^24, or K/V not 64 or 128)";
     case OSDN_ERR_DTYPE: return "unsupported io dtype";
     case OSDN_ERR_ALIGN: return "pointer not 16-byte aligned";
     case OSDN_ERR_WORKSPACE: return "workspace NULL or too small";
@@ -169,6 +172,8 @@ int precond_scan_checked(int io, int B, int H, int T, int K, const void *k, cons
     if (workspace_bytes < osdn_precond_scan_workspace_bytes(B, H, T, K)) return OSDN_ERR_WORKSPACE;
     const size_t BH = (size_t)B * H;
     if (BH == 0) return OSDN_OK;
+    if (BH * (size_t)osdn::precond_segments((int)BH, T, r != nullptr, nullptr) > 0x7fffffffu)
+        return OSDN_ERR_DIMS;   // one warp per segment, numbered in 32 bits
     if (T > 0 && (!k || !beta || !ktilde)) return OSDN_ERR_NULL;
     if (misaligned(k) || misaligned(beta) || misaligned(r) || misaligned(d0) ||
         misaligned(ktilde) || misaligned(dT) || misaligned(log_ratio) || misaligned(workspace))
@@ -221,6 +226,8 @@ int osdn_precond_scan_noalloc(int io, int B, int H, int T, int K, const void *k,
     if (!dims_ok(B, H, T) || !width_ok(K)) return OSDN_ERR_DIMS;
     const size_t BH = (size_t)B * H;
     if (BH == 0) return OSDN_OK;
+    if (BH * (size_t)osdn::precond_segments((int)BH, T, r != nullptr, nullptr) > 0x7fffffffu)
+        return OSDN_ERR_DIMS;
     if (T > 0 && (!k || !beta || !ktilde)) return OSDN_ERR_NULL;
     if (misaligned(k) || misaligned(beta) || misaligned(r) || misaligned(d0) ||
         misaligned(ktilde) || misaligned(dT))

@@ -30,6 +30,22 @@ inline cudaError_t smem_attr_once(const void *func, int bytes,
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// Sequences are spread over grid y and z (y fastest), so that B*H is not
+// bounded by the 65,535 limit of a single grid dimension: seq_grid(x, BH, w)
+// covers BH sequences with w extra z-slices per sequence group, grid_seq()
+// recovers a CTA's sequence (CTAs past BH leave at once).
+constexpr unsigned kGridYMax = 65535;
+inline dim3 seq_grid(unsigned x, size_t BH, unsigned zmul = 1) {
+    const unsigned y = (unsigned)(BH < kGridYMax ? BH : kGridYMax);
+    const unsigned nz = (unsigned)((BH + y - 1) / y);
+    return dim3(x, y, nz * zmul);
+}
+__device__ __forceinline__ size_t grid_seq(unsigned nz = 0) {
+    // nz: the sequence groups (gridDim.z without further z-slices when 0)
+    const unsigned z = nz ? blockIdx.z % nz : blockIdx.z;
+    return blockIdx.y + (size_t)gridDim.y * z;
+}
+
 // Record the first problem a kernel meets in the workspace status word and
 // keep it: later reports never overwrite an earlier one.
 __device__ __forceinline__ void report_status(int *status, int code) {

@@ -39,7 +39,7 @@ constexpr int kPrepBlock = 288;      // + the control warp
 constexpr uint32_t kPrepCols = 256;  // TMEM columns
 
 struct PrepParams {
-    int T, nch, c0;   // sequence length, its chunks, first chunk of this launch
+    int BH, T, nch, c0;   // sequences, sequence length, its chunks, first chunk of this launch
     const float *beta, *alpha;
     float *gc;
     int *status;
@@ -178,7 +178,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = p.c0 + blockIdx.x, seq = blockIdx.y, nch = p.nch;
+    if (grid_seq() >= (size_t)p.BH) return;
+    const int j = p.c0 + blockIdx.x, seq = (int)grid_seq(), nch = p.nch;
     const int T = p.T, t0 = j * C;
     const int nvalid = min(C, T - t0);
     uint8_t *sKQ = smem + LY::oKQ, *sKt = smem + LY::oKt, *sA = smem + LY::oA;
@@ -483,7 +484,8 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
     p.alpha = alpha;
     p.gc = gc;
     p.status = status;
-    dim3 grid(c1 - c0, BH);
+    p.BH = BH;
+    const dim3 grid = seq_grid(c1 - c0, BH);
     chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();
 }

@@ -26,7 +26,7 @@ constexpr int kStage = 16;  // tokens staged per pass (static smem stays < 48 KB
 
 template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(128)
-delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restrict__ k,
+delta_simt_kernel(int BH, int T, int V, const io_t *__restrict__ q, const io_t *__restrict__ k,
                   const io_t *__restrict__ ktilde, const io_t *__restrict__ v,
                   const float *__restrict__ beta, const float *__restrict__ alpha,
                   const float *__restrict__ S0, io_t *__restrict__ o, float *__restrict__ ST) {
@@ -42,7 +42,8 @@ delta_simt_kernel(int T, int V, const io_t *__restrict__ q, const io_t *__restri
     const int tid = threadIdx.x;
     const int row = tid >> 2, p = tid & 3;
     const int row0 = blockIdx.x * kRows;
-    const size_t seq = blockIdx.y;
+    const size_t seq = grid_seq();
+    if (seq >= (size_t)BH) return;
     const size_t kbase = seq * (size_t)T * K, vbase = seq * (size_t)T * V;
 
     float S[KP];
@@ -142,9 +143,9 @@ static cudaError_t launch_delta_simt(int BH, int T, int V, const void *q, const 
                                      const void *kt, const void *v, const float *beta,
                                      const float *alpha, const float *S0, void *o, float *ST,
                                      cudaStream_t stream) {
-    dim3 grid(V / kRows, BH);
+    const dim3 grid = seq_grid(V / kRows, BH);
     delta_simt_kernel<io_t, K, PCH><<<grid, 128, 0, stream>>>(
-        T, V, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
+        BH, T, V, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
         static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
         static_cast<io_t *>(o), ST);
     return cudaGetLastError();

@@ -74,7 +74,8 @@ struct Lay {
 };
 
 struct Params {
-    int T, V, nch, c0, ncs;   // sequence length, V, its chunks; this launch: chunks [c0, c0 + ncs)
+    int BH, T, V, nch, c0, ncs;   // sequences, length, V, its chunks; this launch: chunks [c0, c0 + ncs)
+    int nz;                       // z-slices of the grid that hold sequences (segments: the rest)
     const float *S0, *gc;
     __nv_bfloat16 *o;
     float *ST;
@@ -90,11 +91,9 @@ struct Params {
     // once if they agree to kSpecTol of S0's largest entry.
     const float *check;
     int *status;
-    // Test hook (environment variable OSDN_TEST_STALL_CHAIN): the producer
-    // issues nothing, so the waits run out -- after these limits, shortened
-    // for the test -- and the kernel ends with OSDN_ERR_TIMEOUT.
-    int stall;
-    uint32_t bar_limit, poll_limit;
+    // Test word (the second word of the workspace header, status[1]): when it
+    // is nonzero the producer issues nothing and the waits are shortened, so
+    // that they run out and the kernel ends with OSDN_ERR_TIMEOUT.
 };
 
 // Barriers.  The bf16 state copy entering chunk c sits in buffer c % NSB:
@@ -125,17 +124,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;
-    const int seq = blockIdx.y, v0 = blockIdx.x * BV;
+    if (grid_seq(p.nz) >= (size_t)p.BH) return;
+    const int seq = (int)grid_seq(p.nz), v0 = blockIdx.x * BV;
     const int T = p.T, nch = p.nch;
+    const int stall = p.status ? *reinterpret_cast<volatile int *>(p.status + 1) : 0;
+    const uint32_t bar_limit = stall ? 64u : kWaitLimit;
+    const uint32_t poll_limit = stall ? (1u << 14) : (kWaitLimit << 11);
     // this CTA's chunks, the first whose output it writes, the chunk whose
     // entering state it records (-1: none), and its start and end states
     int cbase = p.c0, ncs = p.ncs, emit_from = p.c0, record_c = -1;
     const float *S0 = p.S0;
     float *ST = p.ST;
     float *spec = nullptr;
-    const size_t sstride = (size_t)gridDim.y * p.V * K;   // one [BH][V][K] state
+    const size_t sstride = (size_t)p.BH * p.V * K;   // one [BH][V][K] state
     if (p.seg_len > 0) {
-        const int z = blockIdx.z, L = p.seg_len;
+        const int z = blockIdx.z / p.nz, L = p.seg_len;
         cbase = z == 0 ? 0 : z * L - p.warm;
         ncs = min(nch, (z + 1) * L) - cbase;
         emit_from = z * L;
@@ -213,10 +216,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             ptx::prefetch_tmap(&tm_qe);
             ptx::prefetch_tmap(&tm_v);
             int lastX = -1, lastY = -1;
-            for (int j = 0; j < (p.stall ? 0 : ncs); ++j) {
+            for (int j = 0; j < (stall ? 0 : ncs); ++j) {
                 // rows of global chunk cbase + j in (Qe, Ae, V) and (W, M)
                 const int t0 = (cbase + j) * C, r0 = (cbase + j) * K;
-                if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st, p.bar_limit)) break;
+                if (j >= NS && !wait_bar(&bars.emptyX[j % NS], ((j / NS) - 1) & 1, &s_abort, st, bar_limit)) break;
                 uint8_t *x = stX(j);
                 ptx::mbar_arrive_expect_tx(&bars.fullX[j % NS], LY::kX);
 #pragma unroll
@@ -229,7 +232,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 }
                 ptx::tma_load_3d(x + LY::oVx, &tm_v, &bars.fullX[j % NS], v0, t0, seq);
                 lastX = j;
-                if (j >= NS && !wait_bar(&bars.emptyY[j % NS], ((j / NS) - 1) & 1, &s_abort, st, p.bar_limit)) break;
+                if (j >= NS && !wait_bar(&bars.emptyY[j % NS], ((j / NS) - 1) & 1, &s_abort, st, bar_limit)) break;
                 uint8_t *y = stY(j);
                 ptx::mbar_arrive_expect_tx(&bars.fullY[j % NS], LY::kY);
                 ptx::tma_load_3d(y, &tm_ae, &bars.fullY[j % NS], 0, t0, seq);
@@ -255,8 +258,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             for (int j = 0; j < ncs; ++j) {
                 // S^T += [W | M] [V; S^T]; releases ring X.  W V as soon as the
                 // accumulator has been read, M S^T once the bf16 copy is in place.
-                if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st, p.poll_limit) ||
-                    !wait_poll(&bars.s_tmem, j & 1, &s_abort, st, p.poll_limit))
+                if (!wait_poll(&bars.fullX[j % NS], (j / NS) & 1, &s_abort, st, poll_limit) ||
+                    !wait_poll(&bars.s_tmem, j & 1, &s_abort, st, poll_limit))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t x = ptx::smem_u32(stX(j));
@@ -265,7 +268,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 #pragma unroll
                 for (int ks = 0; ks < C / 16; ++ks)
                     ptx::umma_bf16(tmem + kColS, da + koff(K, ks), dV + mnoff(ks), id_s, 1);
-                if (!wait_poll(&bars.s_ready, j & 1, &s_abort, st, p.poll_limit)) break;
+                if (!wait_poll(&bars.s_ready, j & 1, &s_abort, st, poll_limit)) break;
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
@@ -285,9 +288,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             const uint32_t id_o = ptx::idesc_bf16(64, BV, 0, 1);
             for (int c = 0; c < ncs; ++c) {
                 // O = [Ae | Qe] [V; S^T] of chunk c, behind chunk c's state product
-                if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st, p.poll_limit) ||
-                    !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st, p.poll_limit) ||
-                    (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st, p.poll_limit)))
+                if (!wait_poll(&bars.fullY[c % NS], (c / NS) & 1, &s_abort, st, poll_limit) ||
+                    !wait_poll(&bars.s_issued[c % NSB], (c / NSB) & 1, &s_abort, st, poll_limit) ||
+                    (c >= 2 && !wait_poll(&bars.o_free[c & 1], ((c >> 1) - 1) & 1, &s_abort, st, poll_limit)))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t y = ptx::smem_u32(stY(c));
@@ -313,7 +316,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         const int ot = tid - 96;
         const int trow = 16 * q4 + lane;   // M=64 accumulator: lanes 0-15 of each quarter
         for (int j = 0; j < ncs; ++j) {
-            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st, p.bar_limit), 3, 128)) break;
+            if (!vote_all(wait_bar(&bars.o_full[j & 1], (j >> 1) & 1, &s_abort, st, bar_limit), 3, 128)) break;
             ptx::tc_fence_after();
             float o[64];
             tmem_ld64(tmem + lane_off + kColO + 64 * (j & 1), o);
@@ -360,8 +363,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             // the copy entering chunk j+1 overwrites the one chunk j-2's output read
             const int n = j + 1;
             const bool okw = (last || n < NSB ||
-                              wait_poll(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st, p.poll_limit)) &&
-                             wait_poll(&bars.s_full, j & 1, &s_abort, st, p.poll_limit);
+                              wait_poll(&bars.o_read[n % NSB], ((n / NSB) - 1) & 1, &s_abort, st, poll_limit)) &&
+                             wait_poll(&bars.s_full, j & 1, &s_abort, st, poll_limit);
             if (!vote_all(okw, 1, 256)) break;
             ptx::tc_fence_after();
             float sv[32];
@@ -450,10 +453,9 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
     p.seg_end = opt.seg_end;
     p.check = opt.check;
     p.status = status;
-    p.stall = std::getenv("OSDN_TEST_STALL_CHAIN") != nullptr ? 1 : 0;
-    p.bar_limit = p.stall ? 64u : kWaitLimit;
-    p.poll_limit = p.stall ? (1u << 14) : (kWaitLimit << 11);
-    dim3 grid(V / BV, BH, opt.seg_len > 0 ? opt.nseg : 1);
+    p.BH = BH;
+    const dim3 grid = seq_grid(V / BV, BH, opt.seg_len > 0 ? opt.nseg : 1);
+    p.nz = (int)((BH + grid.y - 1) / grid.y);
     chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
     return cudaGetLastError();
 }
@@ -646,6 +648,10 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
     const int nch = (T + tc::C - 1) / tc::C;
     int per = tc::kSlabChunks;
     while ((nch + per - 1) / per > tc::kMaxSlabs) per *= 2;
+    // a sequence of one slab is still split in two when the chain leaves at
+    // least half the SMs to the preparation of its second half
+    if (nch <= per && nch >= 32 && (long long)BH * (V / tc::BV) * 2 <= tc::sm_count())
+        per = (nch + 1) / 2;
     const int nslab = (nch + per - 1) / per;
     if (alpha && w.nseg > 1) {  // a decay: every chunk prepared, then the chain in time segments
         cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);

@@ -118,7 +118,7 @@ def test_host_validation_chunk_fwd(L):
     need = L.osdn_chunk_fwd_workspace_bytes(1, 1, 1, 8, 64, 64)
     assert chunk(L, wsb=need - 1) == -5
     assert chunk(L, H=0) == 0
-    assert chunk(L, B=256, H=256) == -2    # more sequences than the grid holds
+    assert chunk(L, B=4096, H=4097) == -2  # more than 2^24 sequences
     # the tensor-core path's 32-bit chunk-row coordinates cap T; fp32 I/O has no cap
     cap = (0x7fffffff // 128) * 64
     assert chunk(L, T=cap + 1, wsb=1 << 62) == -2
@@ -194,7 +194,7 @@ def bwd(L, io=1, B=1, H=1, T=8, K=64, V=64, ins=None, outs=None, ws=40 * FAKE, w
 def test_host_validation_backward(L):
     assert bwd(L, io=5) == -3
     assert bwd(L, K=96) == -2 and bwd(L, V=32) == -2 and bwd(L, T=-3) == -2
-    assert bwd(L, B=256, H=256) == -2
+    assert bwd(L, B=4096, H=4097) == -2
     assert bwd(L, ws=None) == -5 and bwd(L, wsb=16) == -5
     need = L.osdn_backward_workspace_bytes(1, 1, 8, 64, 64)
     assert bwd(L, wsb=need - 1) == -5

@@ -271,3 +271,17 @@ def test_invalid_gates_reported_by_the_device(bad):
     assert ws.status() == -8, ops.status_string(ws.status())
     ws2 = ops.Workspace()
     run_gpu(x, ws2)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_more_sequences_than_one_grid_dimension_holds(io):
+    # 65,537 sequences: the kernels spread sequences over two grid dimensions,
+    # so the first, the 65,535th and the last one are all computed
+    x = synth.make_random(1, 65537, 70, 64, 64, io=io, apf=True, gated=(io == "bf16"), s0=True,
+                          seed=61)
+    kt, dT, o, ST = run_gpu(x)
+    heads = [0, 65534, 65535, 65536]
+    okt, odT, oo, oST = oracle_forward(x, heads)
+    tol = TOL[io]
+    for name, got, want in (("ktilde", kt, okt), ("dT", dT, odT), ("o", o, oo), ("ST", ST, oST)):
+        assert rel_err(pick(got, heads), want) <= tol, name

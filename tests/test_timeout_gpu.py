@@ -1,7 +1,6 @@
 """The timeout path of the tensor-core Phase 2 on the GPU, without a fault:
-the library's test hook (environment variable OSDN_TEST_STALL_CHAIN) makes
-the state-recurrence kernel load nothing, so a bounded wait on a barrier that
-nothing completes runs out.  The call must end, leave OSDN_ERR_TIMEOUT in the
+the workspace header's test word makes the state-recurrence kernel load
+nothing, so a bounded wait on a barrier that nothing completes runs out.  The call must end, leave OSDN_ERR_TIMEOUT in the
 workspace status word, and leave the device usable: the same call without
 the hook then matches the oracle."""
 import pytest
@@ -25,16 +24,16 @@ def _lib():
 
 
 @pytest.mark.parametrize("gated", [False, True])
-def test_stalled_chain_reports_timeout_and_device_stays_usable(monkeypatch, gated):
+def test_stalled_chain_reports_timeout_and_device_stays_usable(gated):
     x = synth.make_random(1, 2, 200, 64, 64, io="bf16", apf=True, gated=gated, s0=True, seed=71)
     g = to_cuda(x)
     kt, dT = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"])
-    monkeypatch.setenv("OSDN_TEST_STALL_CHAIN", "1")
     ws = ops.Workspace()
+    ws.ensure(ops.chunk_fwd_workspace_bytes(1, 1, 2, 200, 64, 64))
+    ws.buf[4:8].view(torch.int32).fill_(1)    # the header's test word
     ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], workspace=ws)
     torch.cuda.synchronize()
     assert ws.status() == OSDN_ERR_TIMEOUT
-    monkeypatch.delenv("OSDN_TEST_STALL_CHAIN")
     ws2 = ops.Workspace()
     o, ST = ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], workspace=ws2)
     torch.cuda.synchronize()
