@@ -30,17 +30,19 @@
 //
 // Time segments.  With a retention gate the map d -> d_{t+1} contracts, so a
 // segment can start from a state estimated by running the scan over the W
-// tokens before it from d = 0 ("warm-up").  Every segment records its
-// estimated start and its end state; a second kernel checks each start
-// against the predecessor's end and recomputes any segment whose estimate is
-// off by more than 2^-21 of the largest entry of that end state, or all
+// tokens before it from d = 0 ("warm-up", 128 tokens).  Every segment
+// records its estimated start and its end state; a
+// second kernel checks each start against the predecessor's end and
+// recomputes any segment whose estimate is off by more than a bound relative
+// to the largest entry of that end state (2^-21 for fp32 I/O; 2^-13 for bf16
+// I/O, a sixteenth of the rounding its ktilde is stored with), or all
 // segments after a token whose one-step map could expand (||A_t||_2 > 1).
 // An accepted start therefore differs from the state the sequential scan
-// would carry into the segment by at most 2^-21 of that state's largest
-// entry; the maps contract (that is what the check on ||A_t|| guarantees),
-// so such a difference shrinks through the segment and the differences of
-// the accepted segments add up to at most about nseg * 2^-21 relative, on
-// top of fp32 rounding.  Speculation only decides how much runs in parallel.
+// would carry into the segment by at most that bound; the maps contract
+// (that is what the check on ||A_t|| guarantees), so such a difference
+// shrinks through the segment and the differences of the accepted segments
+// add up to at most about nseg times the bound, on top of fp32 rounding.
+// Speculation only decides how much runs in parallel.
 //
 // Residual diagnostic (optional).  Writing ktilde_t into the state scales
 // the token's residual S k_t - v_t by 1 - beta_t <d_t, w_t> (section 3,
@@ -57,10 +59,22 @@ namespace p1 {
 
 constexpr int C = 16;          // tokens per chunk
 constexpr int NST = 4;         // key chunks in flight per warp
-constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment
+constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment (fp32 I/O)
+constexpr int kMinSeg = 256;   // shortest segment
 constexpr int kMaxWarps = 4;   // warps (segments) per CTA
 constexpr int kDefaultSms = 152;  // GB300; used only when no device can be queried
 constexpr float kRelTol = 4.76837158203125e-07f;  // 2^-21
+
+// The acceptance bound of a speculative start, relative to the largest entry
+// of the predecessor's end state: 2^-21 for fp32 I/O; for bf16 I/O, whose
+// ktilde carries a rounding of 2^-9 anyway, 2^-13 (a sixteenth of that), so
+// that a retention too slow to forget the guess to fp32 precision in the
+// warm-up does not force a repair the output could not tell from it.
+template <typename io_t>
+struct Spec {
+    static constexpr int warm = kWarm;
+    static constexpr float tol = sizeof(io_t) == 2 ? 1.220703125e-04f : kRelTol;
+};
 
 // One warp's staging area.  Key rows are padded by 8 elements so that the
 // Gram fragment loads (rows g and g+8, two columns per lane) hit 32 banks.
@@ -101,6 +115,28 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid
                  : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void mbar_init_cta(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
+                 "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_parity(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 template <int N>
 __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -426,6 +462,282 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
     __syncwarp();
 }
 
+// ---------------------------------------------------------------------------
+// A whole sequence on one CTA, for scans that run in a single segment (no
+// retention gate, or too few tokens to segment).  The state then has no
+// other parallelism, so the chunk's work is split to shorten its serial
+// path:
+//   chain warps 0 .. K/32-1   lane l of warp w owns column 32 w + l of d;
+//                             per chunk: the partial p_t = <d, w_t> over its
+//                             columns, one cross-warp sum, e = X b (a 16 x 16
+//                             mat-vec, computed by every chain warp alike),
+//                             then its column's 16 steps and ktilde stores;
+//   solver warps K/32 .. +3   take every fourth chunk, ahead of the chain:
+//                             the Gram, n_t and the coupling rows (as in the
+//                             warp scan above), then X = (I + N)^-1 of the
+//                             coupling matrix N by column substitution, handed
+//                             over in shared memory.
+// With b_t = c_t - c_t beta_t rho_t p_t the coefficients of the chunk are
+// e = X b, the same numbers the warp scan's substitution forms on its chain.
+constexpr int kSolvers = 4;
+constexpr int kSolverStages = 3;   // key chunks in flight per solver warp
+constexpr int kChainStages = 4;    // key chunks in flight per chain warp
+
+template <typename io_t, int K>
+struct CtaSmem {
+    static constexpr int KP = K + 8;
+    static constexpr int NW = K / 32;
+    alignas(16) io_t skeys[kSolvers][kSolverStages][C][KP];   // solver key rings
+    alignas(16) float sgb[kSolvers][kSolverStages][C];
+    alignas(16) float sgr[kSolvers][kSolverStages][C];
+    alignas(16) float sG[kSolvers][C][20];                    // Gram and n_t (column 16)
+    alignas(16) float sN[kSolvers][C][C + 4];                 // coupling rows, then X
+    alignas(16) float sNy[kSolvers][C][C + 4];                // coupling rows without c (LR)
+    alignas(16) float4 sS[kSolvers][C];                       // (c_t, c_t b_t rho_t, r_t, b_t rho_t)
+    alignas(16) io_t ckeys[NW][kChainStages][C][32];          // chain key rings: own columns
+    alignas(16) float part[2][NW][C];                         // per-warp partial p_t
+    alignas(16) float sR[kSolvers][C];                        // r_t (1 past T)
+    alignas(16) float be[NW][2][C];                           // per chain warp: b, then e
+    uint64_t xr[kSolvers], xc[kSolvers];                      // X ready / consumed
+    int abort_flag;
+};
+
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         int *status) {
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        if (mbar_try_wait_parity(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort_flag) return false;
+    }
+    report_status(status, OSDN_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
+template <typename io_t, int K, bool HAS_R, bool LR>
+__global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(Params p) {
+    using SM = CtaSmem<io_t, K>;
+    constexpr int NW = K / 32;
+    constexpr int EPP = 16 / (int)sizeof(io_t);   // elements per 16-byte piece
+    constexpr int PR = K / EPP;                   // pieces per key row
+    constexpr int KS = K / 8;                     // Gram k-steps
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SM &sm = *reinterpret_cast<SM *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seq = blockIdx.x, T = p.T, nc = (T + C - 1) / C;
+    const io_t *kseq = static_cast<const io_t *>(p.k) + (size_t)seq * T * K;
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSolvers; ++i) {
+            mbar_init_cta(&sm.xr[i], 1);
+            mbar_init_cta(&sm.xc[i], NW);
+        }
+        sm.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp >= NW) {
+        // ================================================= solver warp
+        const int sv = warp - NW;
+        const int g = lane >> 2, q = lane & 3, t = lane & (C - 1);
+        const float *bseq = p.beta + (size_t)seq * T;
+        const float *rseq = HAS_R ? p.r + (size_t)seq * T : nullptr;
+        const int nmine = nc > sv ? (nc - sv + kSolvers - 1) / kSolvers : 0;
+        auto issue = [&](int m) {
+            if (m < nmine) {
+                const int s = m % kSolverStages, t0 = (sv + m * kSolvers) * C;
+#pragma unroll
+                for (int i = lane; i < C * PR; i += 32) {
+                    const int tt = i / PR, pc = i % PR;
+                    const bool valid = t0 + tt < T;
+                    const io_t *src = valid ? kseq + (size_t)(t0 + tt) * K + pc * EPP : kseq;
+                    cp_async16(&sm.skeys[sv][s][tt][pc * EPP], src, valid);
+                }
+                const bool valid = t0 + t < T && (HAS_R || lane < C);
+                const float *src = lane < C ? bseq : rseq;
+                float *dst = lane < C ? &sm.sgb[sv][s][t] : &sm.sgr[sv][s][t];
+                cp_async4(dst, valid ? src + t0 + t : bseq, valid);
+            }
+            cp_commit();
+        };
+#pragma unroll
+        for (int m = 0; m < kSolverStages - 1; ++m) issue(m);
+        GramPass<io_t, K> gp;
+        CoefPass<HAS_R, LR> cf;
+        bool unused = false;
+        for (int m = 0; m < nmine; ++m) {
+            issue(m + kSolverStages - 1);
+            cp_wait<kSolverStages - 1>();
+            __syncwarp();
+            const int s = m % kSolverStages, t0 = (sv + m * kSolvers) * C, nv = min(C, T - t0);
+            gp.start();
+#pragma unroll
+            for (int s8 = 0; s8 < KS; ++s8) gp.step(sm.skeys[sv][s], g, q, s8);
+            // the chain has consumed this solver's previous X
+            bool ok = true;
+            if (m >= 1) ok = cta_wait(&sm.xc[sv], (m - 1) & 1, abort_flag, p.status);
+            if (!__all_sync(kFullMask, ok)) break;
+            gp.finish(sm.sG[sv], g, q);
+            __syncwarp();
+            cf.start(sm.sgb[sv][s], sm.sgr[sv][s], sm.sG[sv], t, nv, p.eta, unused);
+#pragma unroll
+            for (int u = C - 1; u >= 0; --u) cf.step(t, u);
+            cf.finish();
+            if (lane < C) {
+#pragma unroll
+                for (int u = 0; u < C; ++u) {
+                    sm.sN[sv][t][u] = cf.coef[u];
+                    if (LR) sm.sNy[sv][t][u] = cf.coefy[u];
+                }
+                sm.sS[sv][t] = make_float4(cf.ct, cf.cbr, t < nv ? cf.rt : 1.0f, cf.by);
+                sm.sR[sv][t] = t < nv ? cf.rt : 1.0f;
+            }
+            __syncwarp();
+            // X = (I + N)^-1, lane u < 16 forming column u; rows of N read
+            // before the column overwrites them (every lane reads row i
+            // while the lanes' x_i of earlier rows are in registers)
+            float x[C];
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                float part4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k4 = 0; k4 < i; k4 += 4) {
+                    const float4 n4 = *reinterpret_cast<const float4 *>(&sm.sN[sv][i][k4]);
+                    const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k4 + e < i) part4[e] = fmaf(nn[e], x[k4 + e], part4[e]);
+                }
+                x[i] = ((i == t) ? 1.0f : 0.0f) - ((part4[0] + part4[1]) + (part4[2] + part4[3]));
+            }
+            __syncwarp();
+            if (lane < C) {
+#pragma unroll
+                for (int i = 0; i < C; ++i) sm.sN[sv][i][t] = x[i];   // X[i][t]
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(&sm.xr[sv]);
+        }
+        cp_wait<0>();
+        __syncwarp();
+    } else {
+        // ================================================= chain warp
+        const int w = warp, col = 32 * w + lane;
+        io_t *ktseq = static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K;
+        // this warp's 32 columns of a chunk's 16 keys, staged by cp.async:
+        // 4-byte pieces, lane l copying piece l of every row (bf16: 16 lanes
+        // cover the 64-byte row, fp32: 32 lanes the 128-byte row)
+        constexpr int PW = 32 * (int)sizeof(io_t) / 4;   // 4-byte pieces per row
+        auto issue = [&](int j) {
+            if (j < nc) {
+                const int s = j % kChainStages, t0 = j * C;
+#pragma unroll
+                for (int i = lane; i < C * PW; i += 32) {
+                    const int tt = i / PW, pc = i % PW;
+                    const bool valid = t0 + tt < T;
+                    const io_t *src = valid ? kseq + (size_t)(t0 + tt) * K + 32 * w + pc * (4 / (int)sizeof(io_t)) : kseq;
+                    cp_async4(reinterpret_cast<uint8_t *>(&sm.ckeys[w][s][tt][0]) + 4 * pc, src, valid);
+                }
+            }
+            cp_commit();
+        };
+#pragma unroll
+        for (int j = 0; j < kChainStages - 1; ++j) issue(j);
+        float d = p.d0 ? p.d0[(size_t)seq * K + col] : 1.0f;
+        float lr = 0.0f;
+        for (int j = 0; j < nc; ++j) {
+            issue(j + kChainStages - 1);
+            cp_wait<kChainStages - 1>();
+            __syncwarp();
+            const int s = j % kChainStages, sv = j % kSolvers, t0 = j * C, nv = min(C, T - t0);
+            float kk[C], ww[C], v[C];
+#pragma unroll
+            for (int u = 0; u < C; ++u) {
+                kk[u] = to_f32(sm.ckeys[w][s][u][lane]);
+                ww[u] = kk[u] * kk[u];
+                v[u] = d * ww[u];
+            }
+            // p_t over this warp's columns: lanes 2t and 2t+1 end with it
+#pragma unroll
+            for (int off = 16, n = 8; off >= 2; off >>= 1, n >>= 1) {
+                const bool hi = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    const float keep = hi ? v[i + n] : v[i];
+                    const float send = hi ? v[i] : v[i + n];
+                    v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
+                }
+            }
+            v[0] += __shfl_xor_sync(kFullMask, v[0], 1);
+            if ((lane & 1) == 0) sm.part[j & 1][w][lane >> 1] = v[0];
+            const bool ok = cta_wait(&sm.xr[sv], (j / kSolvers) & 1, abort_flag, p.status);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * NW) : "memory");
+            if (!__all_sync(kFullMask, ok) || *abort_flag) break;
+            // e = X b: lane t < 16 forms b_t, every lane reads all of b and
+            // its row of X as float4 (this warp's own copy of b and e)
+            const int t = lane & (C - 1);
+            const float4 cs = sm.sS[sv][t];
+            float pt = 0.0f;
+#pragma unroll
+            for (int ww2 = 0; ww2 < NW; ++ww2) pt += sm.part[j & 1][ww2][t];
+            if (lane < C) sm.be[w][0][t] = cs.x - cs.y * pt;
+            __syncwarp();
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u4 = 0; u4 < C; u4 += 4) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(&sm.sN[sv][t][u4]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(&sm.be[w][0][u4]);
+                acc4[0] = fmaf(x4.x, b4.x, acc4[0]);
+                acc4[1] = fmaf(x4.y, b4.y, acc4[1]);
+                acc4[2] = fmaf(x4.z, b4.z, acc4[2]);
+                acc4[3] = fmaf(x4.w, b4.w, acc4[3]);
+            }
+            const float et = t < nv ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
+            if (lane < C) sm.be[w][1][t] = et;
+            __syncwarp();
+            if (LR) {   // the residual factor y_t = 1 - b_t rho_t p_t - sum_u Ny_tu e_u
+                float y4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u4 = 0; u4 < C; u4 += 4) {
+                    const float4 n4 = *reinterpret_cast<const float4 *>(&sm.sNy[sv][t][u4]);
+                    const float4 e4 = *reinterpret_cast<const float4 *>(&sm.be[w][1][u4]);
+                    y4[0] = fmaf(n4.x, e4.x, y4[0]);
+                    y4[1] = fmaf(n4.y, e4.y, y4[1]);
+                    y4[2] = fmaf(n4.z, e4.z, y4[2]);
+                    y4[3] = fmaf(n4.w, e4.w, y4[3]);
+                }
+                const float y = 1.0f - cs.w * pt - ((y4[0] + y4[1]) + (y4[2] + y4[3]));
+                if (w == 0 && lane < C && t < nv) lr += logf(y * y);
+            }
+            // this column through the chunk
+            io_t *kst = ktseq + (size_t)t0 * K + col;
+#pragma unroll
+            for (int u4 = 0; u4 < C; u4 += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(&sm.be[w][1][u4]);
+                const float4 r4 = HAS_R ? *reinterpret_cast<const float4 *>(&sm.sR[sv][u4])
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float ev[4] = {e4.x, e4.y, e4.z, e4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = u4 + e;
+                    if (u < nv) from_f32(kst[(size_t)u * K], d * kk[u]);
+                    d = fmaf(ev[e], ww[u], HAS_R ? rv[e] * d : d);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(&sm.xc[sv]);
+        }
+        cp_wait<0>();
+        __syncwarp();
+        if (p.dT) p.dT[(size_t)seq * K + col] = d;
+        if (LR && w == 0) {
+            lr = warp_sum(lr);
+            if (lane == 0) p.logratio[seq] = lr;
+        }
+    }
+}
+
 // One warp per (segment, sequence): warp id = segment + nseg * sequence.
 template <typename io_t, int K, bool HAS_R, bool LR>
 __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params p) {
@@ -451,7 +763,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params 
     } else {
 #pragma unroll
         for (int e = 0; e < EP; ++e) d[e] = make_float2(0.0f, 0.0f);   // the warm-up forgets this
-        tb = tseg - kWarm;
+        tb = tseg - Spec<io_t>::warm;
     }
     bool expand = false;
     float lr = 0.0f;   // warm-up tokens (< tseg) add nothing
@@ -523,7 +835,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p
             for (int m = 0; m < kB; ++m) {
                 float diff, mag;
                 warp_diff<EP>(prev[m], cur[m], diff, mag);
-                if (lane == 0 && b0 + m < p.nseg && !(diff <= kRelTol * mag))
+                if (lane == 0 && b0 + m < p.nseg && !(diff <= Spec<io_t>::tol * mag))
                     atomicMin(&first_bad, b0 + m);
             }
         }
@@ -538,7 +850,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_verify_kernel(Params p
         ld_pairs<EP>(p.ws_start + (base + i) * K + E * lane, cur);
         float diff, mag;
         warp_diff<EP>(prev_end, cur, diff, mag);
-        const bool ok = !all_suspect && diff <= kRelTol * mag;
+        const bool ok = !all_suspect && diff <= Spec<io_t>::tol * mag;
         float2 dd[EP];
         if (ok) {
             ld_pairs<EP>(p.ws_end + (base + i) * K + E * lane, dd);
@@ -591,7 +903,16 @@ static int sm_count() {
 template <typename io_t, int K, bool HAS_R, bool LR>
 static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
-    static std::atomic<unsigned long long> attr_seg{0}, attr_ver{0};
+    static std::atomic<unsigned long long> attr_seg{0}, attr_ver{0}, attr_cta{0};
+    if (p.nseg == 1 && p.BH <= 2 * sm_count()) {
+        // one segment a sequence and few sequences: a CTA per sequence
+        constexpr int kCta = (int)sizeof(CtaSmem<io_t, K>);
+        cudaError_t e = smem_attr_once((const void *)precond_cta_kernel<io_t, K, HAS_R, LR>, kCta,
+                                       attr_cta);
+        if (e != cudaSuccess) return e;
+        precond_cta_kernel<io_t, K, HAS_R, LR><<<p.BH, 32 * (K / 32 + kSolvers), kCta, stream>>>(p);
+        return cudaGetLastError();
+    }
     cudaError_t e0 = smem_attr_once((const void *)precond_segment_kernel<io_t, K, HAS_R, LR>,
                                     kMaxWarps * kStage, attr_seg);
     if (e0 == cudaSuccess)
@@ -627,10 +948,10 @@ int precond_segments(int BH, int T, bool has_r, int *L_out) {
     // ceil(a / b) in 64 bits: T may be within a segment of INT_MAX
     auto cdiv = [](long long a, long long b) { return (a + b - 1) / b; };
     int L = T;
-    if (has_r && T > 2 * p1::kWarm) {
+    if (has_r && T > p1::kMinSeg) {
         L = 1024;
         const long long sms = p1::sm_count();
-        while (L > 2 * p1::kWarm && (long long)BH * cdiv(T, L / 2) <= 8LL * sms)
+        while (L > p1::kMinSeg && (long long)BH * cdiv(T, L / 2) <= 8LL * sms)
             L >>= 1;
         if (L >= T) L = T;
     }
