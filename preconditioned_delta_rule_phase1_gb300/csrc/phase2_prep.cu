@@ -23,7 +23,9 @@
 // tcgen05 MMAs.  The outputs are staged in shared memory in the tensor maps'
 // box layout, in tiles the kernel no longer needs, and leave by TMA stores.
 // 90 KB of shared memory and 256 TMEM columns: two CTAs share an SM and hide
-// each other's latency.  A decay alpha that is not positive and finite (its
+// each other's latency.  The load warp also prefetches into L2 the K, Q and
+// Kt tiles of the CTA one wave (two CTAs per SM) later in launch order, so
+// that its loads find them there.  A decay alpha that is not positive and finite (its
 // log enters the algebra), or a beta that is not finite, is recorded in the
 // status word as OSDN_ERR_DEVICE.
 #include "tc_common.cuh"
@@ -40,6 +42,7 @@ constexpr uint32_t kPrepCols = 256;  // TMEM columns
 
 struct PrepParams {
     int BH, T, nch, c0;   // sequences, sequence length, its chunks, first chunk of this launch
+    int ahead;            // CTAs resident at once: the CTA that many later gets its inputs into L2
     const float *beta, *alpha;
     float *gc;
     int *status;
@@ -219,6 +222,24 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ptx::tma_load_3d(sKQ + cb * 16384, &tm_k, &bar_full, cb * 64, t0, seq);
                 ptx::tma_load_3d(sKQ + cb * 16384 + 8192, &tm_q, &bar_full, cb * 64, t0, seq);
                 ptx::tma_load_3d(sKt + cb * 8192, &tm_kt, &bar_full, cb * 64, t0, seq);
+            }
+            {   // the inputs of the CTA about one wave later, into L2
+                const size_t gx = gridDim.x, gy = gridDim.y;
+                const size_t me = blockIdx.x + gx * (blockIdx.y + gy * (size_t)blockIdx.z);
+                const size_t later = me + (size_t)p.ahead;
+                if (later < gx * gy * gridDim.z) {
+                    const size_t yz = later / gx;
+                    const int c2 = p.c0 + (int)(later % gx);
+                    const int seq2 = (int)(yz % gy + gy * (yz / gy));
+                    if (seq2 < p.BH) {
+#pragma unroll
+                        for (int cb = 0; cb < K / 64; ++cb) {
+                            ptx::tma_prefetch_3d(&tm_k, cb * 64, c2 * C, seq2);
+                            ptx::tma_prefetch_3d(&tm_q, cb * 64, c2 * C, seq2);
+                            ptx::tma_prefetch_3d(&tm_kt, cb * 64, c2 * C, seq2);
+                        }
+                    }
+                }
             }
             uint64_t *last = &bar_full;   // completes once everything issued so far has
             const uint32_t aKQ = ptx::smem_u32(sKQ), aKt = ptx::smem_u32(sKt);
@@ -485,6 +506,7 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
     p.gc = gc;
     p.status = status;
     p.BH = BH;
+    p.ahead = 2 * sm_count();   // two CTAs per SM
     const dim3 grid = seq_grid(c1 - c0, BH);
     chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();

@@ -46,6 +46,16 @@ cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *
                               __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe,
                               __nv_bfloat16 *ae, float *gc, int *status, cudaStream_t stream);
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
 namespace {
 
 constexpr int BV = 64;          // columns of V (rows of S) per CTA
@@ -465,15 +475,6 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
 // kMinSegChunks chunks each; 1 when that leaves a single segment.
 constexpr int kMinSegChunks = 16;
 constexpr int kWarmChunks = 4;   // warm-up of a speculative segment: 256 tokens
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        return 152;
-    }
-    return n;
-}
 int chain_segments(int BH, int T, int V) {
     const long long nch = ((long long)T + C - 1) / C;
     const long long ctas = (long long)BH * (V / BV);

@@ -198,6 +198,8 @@ bool tensor_map_encoder_ready();
 // [BH][rows][width] bf16 in global memory, boxes of 64 columns x 64 rows,
 // 128-byte swizzle; rows past `rows` read as zero.
 bool make_map(CUtensorMap *m, const void *ptr, int BH, int rows, int width);
+// Streaming multiprocessors of the current device (152 if the query fails).
+int sm_count();
 
 }  // namespace tc
 }  // namespace osdn
