@@ -70,6 +70,19 @@ def phase2_bytes(w, x):
     return b
 
 
+def fused_bytes(w, x):
+    """The fused pass's own I/O: q, k, v, beta (and r, alpha) in, o out, plus
+    the per-sequence d and S -- no ktilde."""
+    BH, T, K, V, e = w.B * w.H, w.T, w.K, w.V, io_bytes(w)
+    b = BH * T * ((2 * K + 2 * V) * e + 4)
+    b += BH * T * 4 if x["r"] is not None else 0
+    b += BH * T * 4 if x["alpha"] is not None else 0
+    b += BH * K * 4 + BH * V * K * 4                  # write d_T, S_T
+    b += BH * K * 4 if x["d0"] is not None else 0
+    b += BH * V * K * 4 if x["S0"] is not None else 0
+    return b
+
+
 def phase2_flops(w):
     # per token-head: K S^T, Q S^T, U^T Ktilde (2KV each) plus the chunk-local
     # Gram, scores, solve and intra-chunk output (2 C (K + V)), C = 64
@@ -97,21 +110,42 @@ def precond_segments(BH, T, has_r, sms=None):
     return (T + L - 1) // L if L < T else 1
 
 
-def launches_per_step(w, x, per_channel=False):
+def chain_segments(BH, T, V, sms=None):
+    """Time segments of the bf16 Phase 2 chain with a decay, by the library's
+    rule: as many as keep one wave of chain CTAs (BH * V/64 of them per
+    segment), each of at least 16 chunks."""
+    sms = sm_count() if sms is None else sms
+    nch = (T + 63) // 64
+    ctas = BH * (V // 64)
+    n = sms // ctas if ctas > 0 else 1
+    return max(1, min(n, nch // 16))
+
+
+def launches_per_step(w, x, per_channel=False, sms=None):
     """Kernels one step enqueues, by the library's own rules: the Phase 1
     segment scan (plus its verify kernel when a retention gate splits the
-    sequences into time segments) and Phase 2 (for bf16 I/O a preparation
-    and a chain launch per slab of at least 64 chunks, at most 64 slabs; one
-    fp32 kernel otherwise, and one with a per-channel decay)."""
-    BH, T = w.B * w.H, w.T
-    nseg = precond_segments(BH, T, x["r"] is not None)
+    sequences into time segments) and Phase 2.  For bf16 I/O Phase 2 is a
+    preparation and a chain launch per slab (slabs of at least 64 chunks, at
+    most 64 of them; a sequence of 32 to 64 chunks in two slabs when the
+    chain leaves half the SMs free), or, with a decay and time segments, one
+    preparation launch, the speculative chain launch and one repair launch
+    per later segment; fp32 I/O and a per-channel decay run one kernel."""
+    BH, T, V = w.B * w.H, w.T, w.V
+    sms = sm_count() if sms is None else sms
+    nseg = precond_segments(BH, T, x["r"] is not None, sms)
     p1 = 2 if nseg > 1 else 1
     if w.io != "bf16" or per_channel:
         return p1 + 1
     nch = (T + 63) // 64
+    cseg = chain_segments(BH, T, V, sms)
+    if x["alpha"] is not None and cseg > 1:
+        L = (nch + cseg - 1) // cseg
+        return p1 + 1 + (nch + L - 1) // L
     per = 64
     while (nch + per - 1) // per > 64:
         per *= 2
+    if 32 <= nch <= per and BH * (V // 64) * 2 <= sms:
+        per = (nch + 1) // 2
     nslab = max(1, (nch + per - 1) // per)
     return p1 + 2 * nslab
 
@@ -319,6 +353,23 @@ def measure_workload(w, dev, stream, steps, warmup, flush):
         raise RuntimeError("device status on %s: %d" % (w.name, st))
     t1 = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     t2 = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    parity = parity_sample(w, x, kt, dT, o, ST)
+    # the same step through the one-call forward pass (ktilde kept on chip)
+    wsf = ops.Workspace(device=dev)
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            flush.zero_()
+            if i >= warmup:
+                evf[i - warmup][0].record(stream)
+            ops.forward_fused(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"],
+                              g["alpha"], g["S0"], o, dT, ST, wsf, stream)
+            if i >= warmup:
+                evf[i - warmup][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if wsf.status(stream) != 0:
+        raise RuntimeError("device status on %s (fused): %d" % (w.name, wsf.status(stream)))
+    tf = statistics.mean(e[0].elapsed_time(e[1]) for e in evf)
     hbm_peak, bf16_peak, _ = load_peaks()
     b1, b2 = phase1_bytes(w, x), phase2_bytes(w, x)
     return {
@@ -332,8 +383,10 @@ def measure_workload(w, dev, stream, steps, warmup, flush):
                       "frac_hbm": b2 / (t2 * 1e-3) / 1e9 / hbm_peak,
                       "tflops": phase2_flops(w) / (t2 * 1e-3) / 1e12,
                       "frac_tensor": phase2_flops(w) / (t2 * 1e-3) / 1e12 / bf16_peak},
-        "parity": parity_sample(w, x, kt, dT, o, ST),
+        "parity": parity,
         "launches_per_step": launches_per_step(w, x),
+        "fused": {"ms": tf, "tokens_per_s": B * T / (tf * 1e-3),
+                  "frac_hbm": fused_bytes(w, x) / (tf * 1e-3) / 1e9 / hbm_peak},
     }
 
 
@@ -678,6 +731,62 @@ def run_backward(args, local_rank):
         "clocks": clk, "gpu_launches": 3 * args.steps}), flush=True)
 
 
+def run_fused(args, local_rank):
+    """--fused: both phases through the one-call forward pass (osdn_forward),
+    which keeps ktilde on chip: the scan stores e_t and a checkpoint of d
+    every 64 tokens, the chunk preparation rebuilds ktilde from them.  L2 is
+    flushed before every timed step, as for the two-call line; one JSON line
+    with the pass's HBM roofline over its own I/O (no ktilde)."""
+    from preconditioned_delta_rule_phase1_gb300 import ops
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    g = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+    B, H, T, K, V = w.B, w.H, w.T, w.K, w.V
+    stream = torch.cuda.current_stream(dev)
+    ws = ops.Workspace(device=dev)
+    dT = torch.empty(B, H, K, device=dev)
+    o = torch.empty(B, H, T, V, dtype=g["v"].dtype, device=dev)
+    ST = torch.empty(B, H, V, K, device=dev)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8,
+                        device=dev)
+    step = lambda: ops.forward_fused(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"],
+                                     g["alpha"], g["S0"], o, dT, ST, ws, stream)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(gpu_smi_id(dev, local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    st = ws.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after timed steps: %d" % st)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    nbytes = fused_bytes(w, x)
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "OSDN fwd tokens/s, both phases in one call (ktilde kept on chip)",
+        "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": w.io, "data": "synthetic (seeded)",
+        "config": dict(workload_config(w, 1), path="osdn_forward"),
+        "roofline": {"kernel": "osdn_forward", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "algorithmic_bytes": nbytes, "peak_source": peak_src, "traffic": None},
+        "clocks": clk, "gpu_launches": args.steps * launches_per_step(w, x)}), flush=True)
+
+
 def run_kda(args, local_rank):
     """--kda: both phases with a decay per key channel (osdn_precond_scan +
     osdn_chunk_fwd_kda) at the workload's shape, the decay drawn in
@@ -744,6 +853,8 @@ def main():
                     help="time the gradients of both phases instead of the forward pass")
     ap.add_argument("--kda", action="store_true",
                     help="time both phases with a per-channel decay instead")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the one-call forward pass (ktilde kept on chip) instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -756,6 +867,9 @@ def main():
         return
     if args.kda:
         run_kda(args, local_rank)
+        return
+    if args.fused:
+        run_fused(args, local_rank)
         return
     if world > 1:
         torch.distributed.init_process_group("gloo")

@@ -212,18 +212,24 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
  *   ST           out [B][H][V][K] fp32, or NULL (not written)
  * io == OSDN_BF16 runs on the tensor cores (bf16 operands, fp32
  * accumulation, state carried in fp32); io == OSDN_F32 runs in fp32 FFMA.
- * For sequences longer than 64 chunks of 64 tokens the bf16 path overlaps
- * the preparation of later chunks with the state recurrence of earlier ones
- * on two library-owned streams per device (created on first use, forked from
- * and joined back to `stream` with events); the library serialises the
- * enqueue of such calls.
+ * For sequences longer than 64 chunks of 64 tokens (or of 32 to 64 chunks
+ * when the state recurrence leaves at least half the SMs free) the bf16
+ * path overlaps the preparation of later chunks with the state recurrence of
+ * earlier ones on two library-owned streams per device (created on first
+ * use, forked from and joined back to `stream` with events); the library
+ * serialises the enqueue of such calls.  With a decay alpha and few
+ * sequences the recurrence instead runs in speculative time segments: each
+ * segment starts from a zero state four chunks early, and a segment whose
+ * start differs from its predecessor's end by more than 2^-16 of that end's
+ * largest entry (per block of 64 value rows) is recomputed from that end, so
+ * the speculation changes the result by no more than that bound.
  * With T == 0 the call writes ST = S0 and nothing else.  With io ==
  * OSDN_BF16, T may be at most 1,073,741,760 (the chunk rows of the prepared
  * operands are addressed with 32-bit TMA coordinates); a longer sequence
  * returns OSDN_ERR_DIMS (split it and chain the state through S0 / ST).
- * Test hook: with the environment variable OSDN_TEST_STALL_CHAIN set, the
- * bf16 path's state-recurrence kernel loads nothing, so its bounded waits
- * run out (after limits shortened to milliseconds) and the call leaves
+ * Test hook: while the workspace header's test word is nonzero, the bf16
+ * path's state-recurrence kernel loads nothing, so its bounded waits run out
+ * (after limits shortened to milliseconds) and the call leaves
  * OSDN_ERR_TIMEOUT in the status word with o and ST unwritten; the device
  * stays usable.  It exists to test the timeout path.
  */
@@ -231,6 +237,46 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
                    const void *ktilde, const void *v, const float *beta, const float *alpha,
                    const float *S0, void *o, float *ST, void *workspace, size_t workspace_bytes,
                    void *stream);
+
+/*
+ * Bytes of workspace osdn_forward needs for this shape (>= 256).  bf16: the
+ * preconditioner scan's segment scratch, the scan's checkpoints (4 B*H*T for
+ * e_t and 4 B*H*ceil(T/64)*K for d at every 64th token) and the tensor-core
+ * Phase 2 workspace of osdn_chunk_fwd, each rounded up to 256 bytes.  fp32:
+ * the scan's scratch and ktilde (4 B*H*T*K).
+ */
+size_t osdn_forward_workspace_bytes(int io, int B, int H, int T, int K, int V);
+
+/*
+ * Both phases in one call, with the preconditioned keys kept off global
+ * memory (section 2.2: the two phases; the preconditioner scan's cost is the
+ * throughput overhead section 4.3 reports).  The results are those of
+ * osdn_precond_scan followed by osdn_chunk_fwd on the same inputs, except
+ * that ktilde is not returned:
+ *   q, k    in [B][H][T][K] io          v   in [B][H][T][V] io
+ *   beta    in [B][H][T] fp32;  r, alpha in [B][H][T] fp32 or NULL (1)
+ *   eta     the step size;  d0 in [B][H][K] fp32 or NULL (ones)
+ *   S0      in [B][H][V][K] fp32 or NULL (zeros)
+ *   o       out [B][H][T][V] io;  dT out [B][H][K] fp32 or NULL;
+ *   ST      out [B][H][V][K] fp32 or NULL
+ * io == OSDN_BF16: the scan writes, instead of ktilde, its coefficient e_t
+ * (d_{t+1} = r_t d_t + e_t k_t^2) for every token and d at every 64-token
+ * boundary -- 12 bytes a token-head at K = 128 where ktilde takes 256 -- and
+ * Phase 2's chunk preparation rebuilds each chunk's ktilde in shared memory
+ * from them (rho d_c + P W, one small tensor-core product).  The rebuilt
+ * preconditioner differs from the scan's own by about 2^-16 relative, well
+ * inside the rounding of bf16 ktilde, so o and S_T agree with the two-call
+ * path to within the bf16 tolerance, not bit for bit.
+ * io == OSDN_F32: the two phases run as osdn_precond_scan + osdn_chunk_fwd,
+ * with ktilde held in the workspace.
+ * Outputs must not overlap inputs, each other or the workspace
+ * (OSDN_ERR_ALIAS).  The limits, the status word and the errors are those
+ * of the two calls.
+ */
+int osdn_forward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                 const void *v, const float *beta, const float *r, float eta, const float *d0,
+                 const float *alpha, const float *S0, void *o, float *dT, float *ST,
+                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * One recurrent step (T = 1) of both phases, in place: the inference form of

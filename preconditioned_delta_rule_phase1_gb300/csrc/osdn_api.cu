@@ -12,6 +12,15 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
                                 float *dT, float *logratio, void *scratch, int *status,
                                 cudaStream_t stream);
 size_t precond_scratch_bytes(int BH, int T, int K);
+cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *k,
+                                      const float *beta, const float *r, float eta,
+                                      const float *d0, float *dT, float *ecoef, float *dchk,
+                                      void *scratch, int *status, cudaStream_t stream);
+cudaError_t delta_tc_fused_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                                  const void *v, const float *beta, const float *r,
+                                  const float *ecoef, const float *dchk, const float *alpha,
+                                  const float *S0, void *o, float *ST, void *scratch, int *status,
+                                  cudaStream_t stream);
 size_t precond_scratch_bytes_for(int BH, int T, int K, bool has_r);
 int precond_segments(int BH, int T, bool has_r, int *L_out);
 size_t precond_noalloc_capacity();
@@ -89,6 +98,46 @@ int check_device() {
     return OSDN_OK;
 }
 
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// osdn_forward's workspace after the status word: the scan's segment scratch,
+// then (bf16) e_t, the 64-token checkpoints of d and Phase 2's workspace, or
+// (fp32) ktilde.
+struct FwdCarve {
+    void *p1;
+    float *ecoef, *dchk;
+    void *kt, *p2;
+    size_t bytes;
+};
+FwdCarve fwd_carve(void *base, int io, int BH, int T, int K, int V) {
+    const size_t nch = ((size_t)T + 63) / 64;
+    size_t sz[4];
+    sz[0] = round256(osdn::precond_scratch_bytes(BH, T, K));
+    if (io == OSDN_BF16) {
+        sz[1] = round256((size_t)BH * T * 4);
+        sz[2] = round256((size_t)BH * nch * K * 4);
+        sz[3] = round256(osdn::delta_tc_scratch_bytes(BH, T, K, V));
+    } else {
+        sz[1] = round256((size_t)BH * T * K * 4);
+        sz[2] = sz[3] = 0;
+    }
+    char *b = static_cast<char *>(base);
+    char *at[4];
+    size_t off = 0;
+    for (int i = 0; i < 4; ++i) {
+        at[i] = b ? b + off : nullptr;
+        off += sz[i];
+    }
+    FwdCarve c;
+    c.p1 = at[0];
+    c.ecoef = io == OSDN_BF16 ? reinterpret_cast<float *>(at[1]) : nullptr;
+    c.dchk = io == OSDN_BF16 ? reinterpret_cast<float *>(at[2]) : nullptr;
+    c.kt = io == OSDN_BF16 ? nullptr : at[1];
+    c.p2 = io == OSDN_BF16 ? at[3] : nullptr;
+    c.bytes = off;
+    return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,6 +172,13 @@ size_t osdn_chunk_fwd_workspace_bytes(int io, int B, int H, int T, int K, int V)
     if (io != OSDN_BF16 || T == 0 || T > kMaxTcTokens) return kStatusBytes;
     // the tensor-core path keeps each chunk's prepared operands in the workspace
     return kStatusBytes + osdn::delta_tc_scratch_bytes(B * H, T, K, V);
+}
+
+size_t osdn_forward_workspace_bytes(int io, int B, int H, int T, int K, int V) {
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V) || T == 0) return kStatusBytes;
+    if (io != OSDN_BF16 && io != OSDN_F32) return kStatusBytes;
+    const FwdCarve c = fwd_carve(nullptr, io, B * H, T, K, V);
+    return kStatusBytes + c.bytes;
 }
 
 size_t osdn_backward_workspace_bytes(int B, int H, int T, int K, int V) {
@@ -287,6 +343,65 @@ int osdn_chunk_fwd(int io, int B, int H, int T, int K, int V, const void *q, con
     else  // fp32 I/O: fp32 FFMA (tensor-core operand rounding would not meet fp32 accuracy)
         e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha, S0, o, ST,
                                     (cudaStream_t)stream);
+    return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+}
+
+int osdn_forward(int io, int B, int H, int T, int K, int V, const void *q, const void *k,
+                 const void *v, const float *beta, const float *r, float eta, const float *d0,
+                 const float *alpha, const float *S0, void *o, float *dT, float *ST,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+    if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (io == OSDN_BF16 && T > kMaxTcTokens) return OSDN_ERR_DIMS;
+    if (!workspace) return OSDN_ERR_WORKSPACE;
+    if (workspace_bytes < osdn_forward_workspace_bytes(io, B, H, T, K, V)) return OSDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH == 0) return OSDN_OK;
+    if (BH * (size_t)osdn::precond_segments((int)BH, T, r != nullptr, nullptr) > 0x7fffffffu)
+        return OSDN_ERR_DIMS;   // one warp per scan segment, numbered in 32 bits
+    if (T > 0 && (!q || !k || !v || !beta || !o)) return OSDN_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(beta) || misaligned(r) ||
+        misaligned(d0) || misaligned(alpha) || misaligned(S0) || misaligned(o) ||
+        misaligned(dT) || misaligned(ST) || misaligned(workspace))
+        return OSDN_ERR_ALIGN;
+    const size_t es = io_bytes(io);
+    const size_t kb = BH * (size_t)T * K * es, vb = BH * (size_t)T * V * es;
+    const size_t sb = BH * (size_t)V * K * 4, gb = BH * (size_t)T * 4, db = BH * (size_t)K * 4;
+    const void *ins[8] = {q, k, v, beta, r, alpha, d0, S0};
+    const size_t insz[8] = {kb, kb, vb, gb, gb, gb, db, sb};
+    const void *outs[4] = {o, dT, ST, workspace};
+    const size_t outsz[4] = {vb, db, sb, workspace_bytes};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 8; ++j)
+            if (overlap(outs[i], outsz[i], ins[j], insz[j])) return OSDN_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], outsz[i], outs[j], outsz[j])) return OSDN_ERR_ALIAS;
+    }
+    int dev = check_device();
+    if (dev != OSDN_OK) return dev;
+    cudaStream_t st = (cudaStream_t)stream;
+    int *status = static_cast<int *>(workspace);
+    cudaError_t e;
+    if (T == 0) {   // d_T = d_0 and S_T = S_0
+        e = osdn::precond_scan_launch(io, (int)BH, 0, K, k, beta, r, eta, d0, nullptr, dT, nullptr,
+                                      nullptr, status, st);
+        if (e == cudaSuccess) e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, st);
+        return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
+    }
+    const FwdCarve c = fwd_carve(static_cast<char *>(workspace) + kStatusBytes, io, (int)BH, T, K, V);
+    if (io == OSDN_BF16) {
+        e = osdn::precond_checkpoint_launch(io, (int)BH, T, K, k, beta, r, eta, d0, dT, c.ecoef,
+                                            c.dchk, c.p1, status, st);
+        if (e == cudaSuccess)
+            e = osdn::delta_tc_fused_launch((int)BH, T, K, V, q, k, v, beta, r, c.ecoef, c.dchk,
+                                            alpha, S0, o, ST, c.p2, status, st);
+    } else {
+        e = osdn::precond_scan_launch(io, (int)BH, T, K, k, beta, r, eta, d0, c.kt, dT, nullptr,
+                                      c.p1, status, st);
+        if (e == cudaSuccess)
+            e = osdn::delta_simt_launch(io, (int)BH, T, K, V, q, k, c.kt, v, beta, alpha, S0, o, ST,
+                                        st);
+    }
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }
 

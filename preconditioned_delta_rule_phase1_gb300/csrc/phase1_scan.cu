@@ -44,6 +44,14 @@
 // add up to at most about nseg times the bound, on top of fp32 rounding.
 // Speculation only decides how much runs in parallel.
 //
+// Checkpoint mode (the fused forward pass).  Instead of (or besides)
+// ktilde, the scan can write the coefficient e_t of every token and d at
+// every 64-token boundary.  From those a later kernel rebuilds the
+// preconditioner of any token of a 64-token chunk without a scan:
+//     d_t = rho_t d_c + sum_{u<t} pi_ut e_u w_u   (rho, pi within the chunk)
+// -- one small matrix product, which is how the fused forward's chunk
+// preparation forms ktilde on chip.
+//
 // Residual diagnostic (optional).  Writing ktilde_t into the state scales
 // the token's residual S k_t - v_t by 1 - beta_t <d_t, w_t> (section 3,
 // theorem 5.2: f_t(S_t) / f_t(S_{t-1}) = (1 - beta_t <d_t, w_t>)^2), and the
@@ -93,8 +101,10 @@ struct Params {
     const void *k;
     const float *beta, *r, *d0;
     float eta;
-    void *ktilde;
+    void *ktilde;               // or NULL (checkpoint mode without ktilde)
     float *dT;
+    float *ecoef;               // [BH][T] e_t, or NULL
+    float *dchk;                // [BH][ceil(T/64)][K] d at tokens 0, 64, 128, ..., or NULL
     float *ws_start, *ws_end;   // [BH][nseg][K]
     int *ws_flag;               // [BH][nseg]
     float *ws_lr;               // [BH][nseg] residual log-ratio of each segment
@@ -334,10 +344,11 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
     const int g = lane >> 2, q = lane & 3;   // mma fragment coordinates
     const int t = lane & (C - 1);            // the token this lane solves for
     const io_t *kseq = static_cast<const io_t *>(p.k) + (size_t)seq * p.T * K;
-    io_t *ktseq = static_cast<io_t *>(p.ktilde) + (size_t)seq * p.T * K;
+    io_t *ktseq = p.ktilde ? static_cast<io_t *>(p.ktilde) + (size_t)seq * p.T * K : nullptr;
     const float *bseq = p.beta + (size_t)seq * p.T;
     const float *rseq = HAS_R ? p.r + (size_t)seq * p.T : nullptr;
     const int nc = (te - tb + C - 1) / C;
+    const size_t nchk = (size_t)(p.T + 63) / 64;   // checkpoints per sequence
 
     auto issue = [&](int j) {
         if (j < nc) {
@@ -432,12 +443,15 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
         if (lane < C) {
             const float et = t < nv ? acc : 0.0f, rt = t < nv ? cf.rt : 1.0f;
             st.sER[t] = make_float4(et, et, rt, rt);
+            if (p.ecoef && t < nv && t0 >= tseg) p.ecoef[(size_t)seq * p.T + t0 + t] = et;
         }
+        if (p.dchk && (t0 & 63) == 0 && t0 >= tseg)   // d entering a 64-token chunk
+            st_pairs<EP>(p.dchk + ((size_t)seq * nchk + (t0 >> 6)) * K + E * lane, d);
         __syncwarp();
 
         // ---- chain: this lane's columns through the chunk; emit ktilde ----------
-        const int nst = t0 >= tseg ? nv : 0;   // tokens of this chunk to emit
-        io_t *kst = ktseq + (size_t)t0 * K + E * lane;
+        const int nst = (t0 >= tseg && ktseq) ? nv : 0;   // tokens of this chunk to emit
+        io_t *kst = ktseq ? ktseq + (size_t)t0 * K + E * lane : nullptr;
 #pragma unroll
         for (int u = 0; u < C; ++u) {
             const float4 er = st.sER[u];
@@ -624,7 +638,8 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
     } else {
         // ================================================= chain warp
         const int w = warp, col = 32 * w + lane;
-        io_t *ktseq = static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K;
+        io_t *ktseq = p.ktilde ? static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K : nullptr;
+        const size_t nchk = (size_t)(T + 63) / 64;   // checkpoints per sequence
         // this warp's 32 columns of a chunk's 16 keys, staged by cp.async:
         // 4-byte pieces, lane l copying piece l of every row (bf16: 16 lanes
         // cover the 64-byte row, fp32: 32 lanes the 128-byte row)
@@ -695,6 +710,9 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
             }
             const float et = t < nv ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
             if (lane < C) sm.be[w][1][t] = et;
+            if (p.ecoef && w == 0 && lane < C && t < nv) p.ecoef[(size_t)seq * T + t0 + t] = et;
+            if (p.dchk && (t0 & 63) == 0)   // d entering a 64-token chunk
+                p.dchk[((size_t)seq * nchk + (t0 >> 6)) * K + col] = d;
             __syncwarp();
             if (LR) {   // the residual factor y_t = 1 - b_t rho_t p_t - sum_u Ny_tu e_u
                 float y4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -711,7 +729,7 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
                 if (w == 0 && lane < C && t < nv) lr += logf(y * y);
             }
             // this column through the chunk
-            io_t *kst = ktseq + (size_t)t0 * K + col;
+            io_t *kst = ktseq ? ktseq + (size_t)t0 * K + col : nullptr;
 #pragma unroll
             for (int u4 = 0; u4 < C; u4 += 4) {
                 const float4 e4 = *reinterpret_cast<const float4 *>(&sm.be[w][1][u4]);
@@ -721,7 +739,7 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int u = u4 + e;
-                    if (u < nv) from_f32(kst[(size_t)u * K], d * kk[u]);
+                    if (kst && u < nv) from_f32(kst[(size_t)u * K], d * kk[u]);
                     d = fmaf(ev[e], ww[u], HAS_R ? rv[e] * d : d);
                 }
             }
@@ -974,10 +992,10 @@ size_t precond_scratch_bytes(int BH, int T, int K) {
     return segment_scratch_bytes((size_t)BH * nseg, K);
 }
 
-cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
-                                const float *r, float eta, const float *d0, void *ktilde,
-                                float *dT, float *logratio, void *scratch, int *status,
-                                cudaStream_t stream) {
+static cudaError_t scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
+                               const float *r, float eta, const float *d0, void *ktilde,
+                               float *dT, float *logratio, float *ecoef, float *dchk,
+                               void *scratch, int *status, cudaStream_t stream) {
     if (T == 0) {   // d_T = d_0; an empty product of residual ratios is 1
         if (logratio) {
             p1::copy_or_fill_kernel<<<(unsigned)((BH + 255) / 256), 256, 0, stream>>>(
@@ -1001,6 +1019,8 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
     p.eta = eta;
     p.ktilde = ktilde;
     p.dT = dT;
+    p.ecoef = ecoef;
+    p.dchk = dchk;
     p.logratio = logratio;
     p.status = status;
     float *f = static_cast<float *>(scratch);
@@ -1014,6 +1034,24 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
         return K == 64 ? p1::launch<__nv_bfloat16, 64>(p, stream)
                        : p1::launch<__nv_bfloat16, 128>(p, stream);
     return K == 64 ? p1::launch<float, 64>(p, stream) : p1::launch<float, 128>(p, stream);
+}
+
+cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
+                                const float *r, float eta, const float *d0, void *ktilde,
+                                float *dT, float *logratio, void *scratch, int *status,
+                                cudaStream_t stream) {
+    return scan_launch(io, BH, T, K, k, beta, r, eta, d0, ktilde, dT, logratio, nullptr, nullptr,
+                       scratch, status, stream);
+}
+
+// Checkpoint mode: e_t of every token ([BH][T]) and d entering every 64-token
+// chunk ([BH][ceil(T/64)][K]) instead of ktilde; d_T as usual.
+cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *k,
+                                      const float *beta, const float *r, float eta,
+                                      const float *d0, float *dT, float *ecoef, float *dchk,
+                                      void *scratch, int *status, cudaStream_t stream) {
+    return scan_launch(io, BH, T, K, k, beta, r, eta, d0, nullptr, dT, nullptr, ecoef, dchk,
+                       scratch, status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -25,7 +25,19 @@
 // 90 KB of shared memory and 256 TMEM columns: two CTAs share an SM and hide
 // each other's latency.  The load warp also prefetches into L2 the K, Q and
 // Kt tiles of the CTA one wave (two CTAs per SM) later in launch order, so
-// that its loads find them there.  A decay alpha that is not positive and finite (its
+// that its loads find them there.
+//
+// Fused forward pass (template flag FUSED): Kt is not read but rebuilt from
+// the preconditioner scan's checkpoints -- d_c, the preconditioner entering
+// the chunk, and e_t of every token (d_{t+1} = r_t d_t + e_t w_t, w = k . k):
+//   Kt = (rho d_c^T + P W) . K,   P_tu = pi_ut e_u (u < t),   W_u = w_u,
+// with rho_t = prod_{v<t} r_v and pi_ut = prod_{u<v<t} r_v inside the chunk.
+// P W runs on the tensor cores with P and W each split into a bf16 high
+// part and a bf16 remainder (three products: hi.hi + hi.lo + lo.hi), so the
+// rebuilt preconditioner carries about 2^-16 relative error instead of the
+// 2^-9 of one bf16 product.  The four tiles use space that is dead at that
+// point: W over L, its remainder over Xb / Xb diag(g), P over A, its
+// remainder over Kt.  A decay alpha that is not positive and finite (its
 // log enters the algebra), or a beta that is not finite, is recorded in the
 // status word as OSDN_ERR_DEVICE.
 #include "tc_common.cuh"
@@ -44,6 +56,9 @@ struct PrepParams {
     int BH, T, nch, c0;   // sequences, sequence length, its chunks, first chunk of this launch
     int ahead;            // CTAs resident at once: the CTA that many later gets its inputs into L2
     const float *beta, *alpha;
+    const float *r;       // fused: retention r_t [BH][T], or NULL (r = 1)
+    const float *ecoef;   // fused: e_t [BH][T]
+    const float *dchk;    // fused: d entering each chunk [BH][nch][K]
     float *gc;
     int *status;
 };
@@ -163,7 +178,7 @@ __device__ void solve_unit_lower(float *sL, int pt) {
     ptx::named_bar(1, kPrepThreads);
 }
 
-template <int K, bool GATED>
+template <int K, bool GATED, bool FUSED>
 __global__ void __launch_bounds__(kPrepBlock, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_w,
@@ -176,8 +191,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     __shared__ uint64_t bar_full, bar_g, bar_x2, bar_p1, bar_x3, bar_p2;
+    __shared__ uint64_t bar_f0, bar_f1, bar_kt;   // fused: W, P staged; P W done; Kt built
     __shared__ uint32_t tmem_base_sh;
     __shared__ float sBeta[C], sLg[C], sD[C];
+    // fused: e_t, r_t, and sPre[b][t] = prod_{16 b <= v < t} r_v (1 for t <= 16 b):
+    // sPre[0] is rho, sPre[b] for b > 0 the r products from column block b on
+    __shared__ float sE[FUSED ? C : 1], sR[FUSED ? C : 1], sPre[FUSED ? 4 : 1][FUSED ? C : 1];
+    __shared__ __align__(16) float sD0[FUSED ? K : 1];
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,7 +219,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     };
 
     if (tid == kPrepThreads) {
-        uint64_t *all[] = {&bar_full, &bar_g, &bar_x2, &bar_p1, &bar_x3, &bar_p2};
+        uint64_t *all[] = {&bar_full, &bar_g, &bar_x2, &bar_p1, &bar_x3, &bar_p2,
+                           &bar_f0, &bar_f1, &bar_kt};
         for (uint64_t *b : all) ptx::mbar_init(b, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -216,12 +237,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (warp == 8) {
         // ============================================ TMA + MMA (one thread)
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&bar_full, 3 * C * K * 2);
+            ptx::mbar_arrive_expect_tx(&bar_full, (FUSED ? 2 : 3) * C * K * 2);
 #pragma unroll
             for (int cb = 0; cb < K / 64; ++cb) {
                 ptx::tma_load_3d(sKQ + cb * 16384, &tm_k, &bar_full, cb * 64, t0, seq);
                 ptx::tma_load_3d(sKQ + cb * 16384 + 8192, &tm_q, &bar_full, cb * 64, t0, seq);
-                ptx::tma_load_3d(sKt + cb * 8192, &tm_kt, &bar_full, cb * 64, t0, seq);
+                if (!FUSED) ptx::tma_load_3d(sKt + cb * 8192, &tm_kt, &bar_full, cb * 64, t0, seq);
             }
             {   // the inputs of the CTA about one wave later, into L2
                 const size_t gx = gridDim.x, gy = gridDim.y;
@@ -236,7 +257,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         for (int cb = 0; cb < K / 64; ++cb) {
                             ptx::tma_prefetch_3d(&tm_k, cb * 64, c2 * C, seq2);
                             ptx::tma_prefetch_3d(&tm_q, cb * 64, c2 * C, seq2);
-                            ptx::tma_prefetch_3d(&tm_kt, cb * 64, c2 * C, seq2);
+                            if (!FUSED) ptx::tma_prefetch_3d(&tm_kt, cb * 64, c2 * C, seq2);
                         }
                     }
                 }
@@ -245,6 +266,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const uint32_t aKQ = ptx::smem_u32(sKQ), aKt = ptx::smem_u32(sKt);
             const uint32_t aA = ptx::smem_u32(sA), aXb = ptx::smem_u32(sXb), aXg = ptx::smem_u32(sXg);
             bool ok = wait_poll(&bar_full, 0, &s_abort, st);
+            if (FUSED) {
+                ok = ok && wait_poll(&bar_f0, 0, &s_abort, st);
+                if (ok) {  // P W = Ph Wh + Ph Wl + Pl Wh (M=64, N=K), MN-major W tiles
+                    ptx::tc_fence_after();
+                    const uint32_t idk = ptx::idesc_bf16(64, K, 0, 1);
+                    const uint64_t dPh = dk0(aA), dPl = dk0(aKt);
+                    const uint64_t dWh = dmn0(ptx::smem_u32(smem + LY::oL), 8192);
+                    const uint64_t dWl = dmn0(aXb, 8192);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks) {
+                        ptx::umma_bf16(tmem, dPh + koff(C, ks), dWh + mnoff(ks), idk, ks > 0);
+                        ptx::umma_bf16(tmem, dPh + koff(C, ks), dWl + mnoff(ks), idk, 1);
+                        ptx::umma_bf16(tmem, dPl + koff(C, ks), dWh + mnoff(ks), idk, 1);
+                    }
+                    ptx::umma_commit(&bar_f1);
+                    last = &bar_f1;
+                }
+                ok = ok && wait_poll(&bar_kt, 0, &s_abort, st);
+            }
             if (ok) {  // [K;Q] Kt^T (M=128): Gram rows 0-63, scores rows 64-127
                 ptx::tc_fence_after();
                 const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
@@ -322,6 +362,40 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             sLg[2 * lane] = excl + lg[0];
             sLg[2 * lane + 1] = excl + lg[0] + lg[1];
         }
+        if (FUSED && warp == 1) {
+            // e_t and r_t, two tokens a lane (e = 0 and r = 1 past T), and the
+            // exclusive products of r from token 0, 16, 32 and 48 on, by
+            // product scans (no division: r may be 0)
+            float ee[2], rr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = 2 * lane + e;
+                const bool valid = i < nvalid;
+                ee[e] = valid ? p.ecoef[(size_t)seq * T + t0 + i] : 0.0f;
+                rr[e] = (valid && p.r) ? p.r[(size_t)seq * T + t0 + i] : 1.0f;
+            }
+            sE[2 * lane] = ee[0];
+            sE[2 * lane + 1] = ee[1];
+            sR[2 * lane] = rr[0];
+            sR[2 * lane + 1] = rr[1];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float r0 = 2 * lane >= 16 * b ? rr[0] : 1.0f;
+                const float r1 = 2 * lane + 1 >= 16 * b ? rr[1] : 1.0f;
+                float pr = r0 * r1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(kFullMask, pr, off);
+                    if (lane >= off) pr *= y;
+                }
+                float excl = __shfl_up_sync(kFullMask, pr, 1);
+                if (lane == 0) excl = 1.0f;
+                sPre[b][2 * lane] = excl;
+                sPre[b][2 * lane + 1] = excl * r0;
+            }
+        }
+        if (FUSED && pt >= 64 && pt < 64 + K)   // the preconditioner entering the chunk
+            sD0[pt - 64] = p.dchk[((size_t)seq * nch + j) * K + (pt - 64)];
         ptx::named_bar(1, kPrepThreads);
         if (GATED && pt < C) {
             // tokens past T add nothing to the log, so sLg[C-1] is the chunk's total
@@ -330,8 +404,84 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (pt == 0) p.gc[(size_t)seq * nch + j] = __expf(lgC);
         }
 
+        bool fok = true;
+        if (FUSED) {
+            // ---- P = pi . e (strictly lower): high part over A, remainder over Kt
+            {
+                const int t = pt >> 2, blk = pt & 3, s0 = 16 * blk;
+                float ph[16], pl[16];
+                // pi_st = prod_{s<v<t} r_v, walked down from s = s0 + 15, where
+                // it is the product of r over [s0 + 16, t)
+                float pi = blk < 3 ? sPre[blk + 1][t] : 1.0f;
+#pragma unroll
+                for (int e = 15; e >= 0; --e) {
+                    const int s = s0 + e;
+                    float val = 0.0f;
+                    if (s < t) {
+                        val = pi * sE[s];
+                        pi *= sR[s];
+                    }
+                    ph[e] = __bfloat162float(__float2bfloat16_rn(val));
+                    pl[e] = val - ph[e];
+                }
+                st_row_sw128(sA, C, t, s0, ph, 16);
+                st_row_sw128(sKt, C, t, s0, pl, 16);
+            }
+            // ---- W = K . K once the keys have landed: high part over L, remainder over Xb
+            fok = vote_all(wait_poll(&bar_full, 0, &s_abort, st), 1, kPrepThreads);
+            if (fok) {
+                constexpr int PIECES = C * K * 2 / 16;   // 16-byte pieces of the K rows
+                uint8_t *sWh = smem + LY::oL, *sWl = sXb;
+                for (int i = pt; i < PIECES; i += kPrepThreads) {
+                    const int cb = i >> 9, o = (i & 511) * 16;   // 512 pieces per 64-row block
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sKQ + cb * 16384 + o);
+                    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&in[e]));
+                        const float wx = x.x * x.x, wy = x.y * x.y;   // exact: bf16 squared fits fp32
+                        hi[e] = pack_bf16x2(wx, wy);
+                        const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi[e]));
+                        lo[e] = pack_bf16x2(wx - h.x, wy - h.y);
+                    }
+                    *reinterpret_cast<uint4 *>(sWh + cb * 8192 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(sWl + cb * 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(1, kPrepThreads);
+                if (pt == 0) ptx::mbar_arrive(&bar_f0);
+            }
+            // ---- Kt = (rho d_c + P W) . K, over P's remainder (its product has completed)
+            fok = fok && vote_all(wait_poll(&bar_f1, 0, &s_abort, st), 1, kPrepThreads);
+            if (fok) {
+                ptx::tc_fence_after();
+                const int mrow = 16 * (warp & 3) + lane;
+                const uint32_t loff = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+                const int h = warp >> 2;
+                float v[NH];
+                tmem_ldn<NH>(tmem + loff + h * NH, v);
+                if (lane < 16) {
+                    const float rho = sPre[0][mrow];
+#pragma unroll
+                    for (int c = 0; c < NH; c += 16) {
+                        float kv[16];
+                        ld_row_sw128(sKQ, 128, mrow, h * NH + c, kv, 16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            kv[e] *= fmaf(rho, sD0[h * NH + c + e], v[c + e]);
+                        st_row_sw128(sKt, C, mrow, h * NH + c, kv, 16);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::named_bar(1, kPrepThreads);
+                if (pt == 0) ptx::mbar_arrive(&bar_kt);
+            }
+        }
+
         // ---- Gram / scores: L (fp32) and A (bf16); then Kt <- D Kt
-        bool ok = vote_all(wait_poll(&bar_g, 0, &s_abort, st), 1, kPrepThreads);
+        bool ok = fok && vote_all(wait_poll(&bar_g, 0, &s_abort, st), 1, kPrepThreads);
         if (ok) {
             ptx::tc_fence_after();
             float g[32];
@@ -480,21 +630,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (warp == 8) ptx::tmem_dealloc(tmem, kPrepCols);
 }
 
-template <int K, bool GATED>
+template <int K, bool GATED, bool FUSED>
 cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const void *k,
-                          const void *kt, const float *beta, const float *alpha, __nv_bfloat16 *w,
-                          __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc,
-                          int *status, cudaStream_t stream) {
+                          const void *kt, const float *beta, const float *alpha, const Fused &fz,
+                          __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae,
+                          float *gc, int *status, cudaStream_t stream) {
     const int nch = (T + C - 1) / C, Tp = nch * C;
     CUtensorMap mk, mq, mkt, mw, mm, mqe, mae;
-    if (!make_map(&mk, k, BH, T, K) || !make_map(&mq, q, BH, T, K) || !make_map(&mkt, kt, BH, T, K) ||
+    if (!make_map(&mk, k, BH, T, K) || !make_map(&mq, q, BH, T, K) ||
+        !make_map(&mkt, FUSED ? k : kt, BH, T, K) ||   // fused: Kt is built, not loaded
         !make_map(&mw, w, BH, nch * K, C) || !make_map(&mm, m, BH, nch * K, K) ||
         !make_map(&mqe, qe, BH, Tp, K) || !make_map(&mae, ae, BH, Tp, C))
         return cudaErrorInvalidValue;
     constexpr int smem = PrepLay<K>::kAlloc;
     static std::atomic<unsigned long long> attr_done{0};
     {
-        cudaError_t e = smem_attr_once((const void *)chunk_prep_kernel<K, GATED>, smem, attr_done);
+        cudaError_t e = smem_attr_once((const void *)chunk_prep_kernel<K, GATED, FUSED>, smem, attr_done);
         if (e != cudaSuccess) return e;
     }
     PrepParams p;
@@ -503,30 +654,45 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
     p.c0 = c0;
     p.beta = beta;
     p.alpha = alpha;
+    p.r = fz.r;
+    p.ecoef = fz.ecoef;
+    p.dchk = fz.dchk;
     p.gc = gc;
     p.status = status;
     p.BH = BH;
     p.ahead = 2 * sm_count();   // two CTAs per SM
     const dim3 grid = seq_grid(c1 - c0, BH);
-    chunk_prep_kernel<K, GATED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
+    chunk_prep_kernel<K, GATED, FUSED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t prep_launch_k(int BH, int T, int c0, int c1, const void *q, const void *k,
+                          const void *kt, const float *beta, const float *alpha, const Fused &fz,
+                          __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae,
+                          float *gc, int *status, cudaStream_t stream) {
+    if (fz.ecoef) {
+        if (alpha)
+            return prep_launch_t<K, true, true>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<K, false, true>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+    }
+    if (alpha)
+        return prep_launch_t<K, true, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+    return prep_launch_t<K, false, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
 }
 
 }  // namespace
 
-// Chunks [c0, c1) of every sequence.
+// Chunks [c0, c1) of every sequence.  With fz.ecoef given (the fused forward
+// pass) Kt is rebuilt from the preconditioner's checkpoints instead of read.
 cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
                               const void *kt, const float *beta, const float *alpha,
-                              __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe,
-                              __nv_bfloat16 *ae, float *gc, int *status, cudaStream_t stream) {
-    if (K == 128) {
-        if (alpha)
-            return prep_launch_t<128, true>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
-        return prep_launch_t<128, false>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
-    }
-    if (alpha)
-        return prep_launch_t<64, true>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
-    return prep_launch_t<64, false>(BH, T, c0, c1, q, k, kt, beta, alpha, w, m, qe, ae, gc, status, stream);
+                              const Fused &fz, __nv_bfloat16 *w, __nv_bfloat16 *m,
+                              __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc, int *status,
+                              cudaStream_t stream) {
+    if (K == 128)
+        return prep_launch_k<128>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+    return prep_launch_k<64>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
 }
 
 }  // namespace tc

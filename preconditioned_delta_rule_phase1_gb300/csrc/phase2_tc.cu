@@ -43,8 +43,9 @@ namespace tc {
 
 cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
                               const void *kt, const float *beta, const float *alpha,
-                              __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe,
-                              __nv_bfloat16 *ae, float *gc, int *status, cudaStream_t stream);
+                              const Fused &fz, __nv_bfloat16 *w, __nv_bfloat16 *m,
+                              __nv_bfloat16 *qe, __nv_bfloat16 *ae, float *gc, int *status,
+                              cudaStream_t stream);
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -591,10 +592,10 @@ size_t delta_tc_scratch_bytes(int BH, int T, int K, int V) {
 
 namespace {
 cudaError_t prep_range(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
-                       const void *kt, const float *beta, const float *alpha, const tc::Carve &w,
-                       int *status, cudaStream_t stream) {
-    return tc::chunk_prep_launch(BH, T, K, c0, c1, q, k, kt, beta, alpha, w.w, w.m, w.qe, w.ae, w.gc,
-                                 status, stream);
+                       const void *kt, const float *beta, const float *alpha, const tc::Fused &fz,
+                       const tc::Carve &w, int *status, cudaStream_t stream) {
+    return tc::chunk_prep_launch(BH, T, K, c0, c1, q, k, kt, beta, alpha, fz, w.w, w.m, w.qe, w.ae,
+                                 w.gc, status, stream);
 }
 cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void *v, const float *alpha,
                         const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
@@ -640,10 +641,11 @@ cudaError_t chain_segmented(int BH, int T, int K, int V, int nch, const void *v,
 }
 }  // namespace
 
-cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
-                            const void *kt, const void *v, const float *beta, const float *alpha,
-                            const float *S0, void *o, float *ST, void *scratch, int *status,
-                            cudaStream_t stream) {
+namespace {
+cudaError_t delta_tc_impl(int BH, int T, int K, int V, const void *q, const void *k,
+                          const void *kt, const void *v, const float *beta, const float *alpha,
+                          const tc::Fused &fz, const float *S0, void *o, float *ST, void *scratch,
+                          int *status, cudaStream_t stream) {
     if (!tc::tensor_map_encoder_ready()) return cudaErrorNotSupported;
     const tc::Carve w = tc::carve(scratch, BH, T, K, V);
     const int nch = (T + tc::C - 1) / tc::C;
@@ -655,12 +657,12 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
         per = (nch + 1) / 2;
     const int nslab = (nch + per - 1) / per;
     if (alpha && w.nseg > 1) {  // a decay: every chunk prepared, then the chain in time segments
-        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);
+        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, fz, w, status, stream);
         if (e != cudaSuccess) return e;
         return chain_segmented(BH, T, K, V, nch, v, alpha, w, S0, o, ST, status, stream);
     }
     if (nslab <= 1) {  // one slab: preparation, then the chain, on the caller's stream
-        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, w, status, stream);
+        cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, fz, w, status, stream);
         if (e != cudaSuccess) return e;
         return chain_range(BH, T, K, V, 0, nch, v, alpha, w, S0, o, ST, status, stream);
     }
@@ -676,11 +678,11 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
     if ((e = cudaStreamWaitEvent(ov->chain, ev[0], 0)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ov->prep, ev[0], 0)) != cudaSuccess) return e;
     // slab 0 prepared ahead of the chain; slabs 1.. prepared behind it
-    if ((e = prep_range(BH, T, K, 0, per, q, k, kt, beta, alpha, w, status, ov->chain)) != cudaSuccess)
+    if ((e = prep_range(BH, T, K, 0, per, q, k, kt, beta, alpha, fz, w, status, ov->chain)) != cudaSuccess)
         return e;
     for (int s = 1; s < nslab; ++s) {
         const int c0 = s * per, c1 = std::min(nch, c0 + per);
-        if ((e = prep_range(BH, T, K, c0, c1, q, k, kt, beta, alpha, w, status, ov->prep)) != cudaSuccess)
+        if ((e = prep_range(BH, T, K, c0, c1, q, k, kt, beta, alpha, fz, w, status, ov->prep)) != cudaSuccess)
             return e;
         if ((e = cudaEventRecord(ev[1 + s], ov->prep)) != cudaSuccess) return e;
     }
@@ -697,6 +699,31 @@ cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const vo
     // itself waited for the last preparation slab)
     if ((e = cudaEventRecord(ev[1], ov->chain)) != cudaSuccess) return e;
     return cudaStreamWaitEvent(stream, ev[1], 0);
+}
+}  // namespace
+
+cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                            const void *kt, const void *v, const float *beta, const float *alpha,
+                            const float *S0, void *o, float *ST, void *scratch, int *status,
+                            cudaStream_t stream) {
+    return delta_tc_impl(BH, T, K, V, q, k, kt, v, beta, alpha, tc::Fused(), S0, o, ST, scratch,
+                         status, stream);
+}
+
+// The fused forward pass's Phase 2: Kt is rebuilt chunk by chunk from the
+// preconditioner scan's checkpoints (e_t of every token, d entering every
+// chunk) and never read from or written to global memory.
+cudaError_t delta_tc_fused_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                                  const void *v, const float *beta, const float *r,
+                                  const float *ecoef, const float *dchk, const float *alpha,
+                                  const float *S0, void *o, float *ST, void *scratch, int *status,
+                                  cudaStream_t stream) {
+    tc::Fused fz;
+    fz.r = r;
+    fz.ecoef = ecoef;
+    fz.dchk = dchk;
+    return delta_tc_impl(BH, T, K, V, q, k, nullptr, v, beta, alpha, fz, S0, o, ST, scratch, status,
+                         stream);
 }
 
 }  // namespace osdn

@@ -58,6 +58,9 @@ _SIGS = {
                              [ctypes.c_float] + [ctypes.c_void_p] * 6 +
                              [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_chunk_fwd_kda_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "osdn_forward_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "osdn_forward": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 5 + [ctypes.c_float] +
+                     [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p]),
     "osdn_chunk_fwd_kda": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.c_void_p] * 10 +
                            [ctypes.c_size_t, ctypes.c_void_p]),
 }
@@ -196,6 +199,10 @@ def chunk_fwd_workspace_bytes(io, B, H, T, K, V) -> int:
     return int(lib().osdn_chunk_fwd_workspace_bytes(io, B, H, T, K, V))
 
 
+def forward_workspace_bytes(io, B, H, T, K, V) -> int:
+    return int(lib().osdn_forward_workspace_bytes(io, B, H, T, K, V))
+
+
 def backward_workspace_bytes(B, H, T, K, V) -> int:
     return int(lib().osdn_backward_workspace_bytes(B, H, T, K, V))
 
@@ -302,6 +309,39 @@ def forward(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, worksp
     ktilde, dT = precond_scan(k, beta, r, eta, d0, workspace=ws, stream=stream)
     o, ST = chunk_fwd(q, k, ktilde, v, beta, alpha, S0, workspace=ws, stream=stream)
     return ktilde, dT, o, ST
+
+
+def forward_fused(q, k, v, beta, r=None, eta=0.1, d0=None, alpha=None, S0=None, o=None, dT=None,
+                  ST=None, workspace=None, stream=None):
+    """Both phases in one call (osdn_forward), ktilde kept off global memory
+    for bf16 I/O: returns (dT, o, ST)."""
+    B, H, T, K = k.shape
+    V = v.shape[-1]
+    io, dev = _io(k), k.device
+    _expect("q", q, (B, H, T, K), k.dtype, dev)
+    _expect("v", v, (B, H, T, V), k.dtype, dev)
+    _expect("beta", beta, (B, H, T), F32, dev)
+    _expect("r", r, (B, H, T), F32, dev)
+    _expect("d0", d0, (B, H, K), F32, dev)
+    _expect("alpha", alpha, (B, H, T), F32, dev)
+    _expect("S0", S0, (B, H, V, K), F32, dev)
+    if o is None:
+        o = torch.empty(B, H, T, V, dtype=k.dtype, device=dev)
+    if dT is None:
+        dT = torch.empty(B, H, K, dtype=F32, device=dev)
+    if ST is None:
+        ST = torch.empty(B, H, V, K, dtype=F32, device=dev)
+    _expect("o", o, (B, H, T, V), k.dtype, dev)
+    _expect("dT", dT, (B, H, K), F32, dev)
+    _expect("ST", ST, (B, H, V, K), F32, dev)
+    ws = _workspace(workspace, dev)
+    with _on(dev):
+        ws.ensure(forward_workspace_bytes(io, B, H, T, K, V))
+        code = lib().osdn_forward(io, B, H, T, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(r),
+                                  float(eta), _ptr(d0), _ptr(alpha), _ptr(S0), _ptr(o), _ptr(dT),
+                                  _ptr(ST), ws.ptr, ws.nbytes, _stream(stream, dev))
+    _check(code, "osdn_forward")
+    return dT, o, ST
 
 
 def decode_step(q, k, v, beta, d, S, r=None, eta=0.1, alpha=None, o=None, ktilde=None,

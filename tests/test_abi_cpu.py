@@ -65,6 +65,20 @@ def test_bench_segment_rule_matches_the_library(L, B, H, T, K):
     assert ops.precond_scan_workspace_bytes(B, H, T, K) == want
 
 
+def test_bench_launch_count_rule():
+    # bench.py's gpu_launches claim, from a copy of the library's schedule at
+    # 152 SMs; the ncu launch lists of the 1.3B and long gated workloads show
+    # 6 and 7 of the library's kernels per step
+    import bench
+    from preconditioned_delta_rule_phase1_gb300 import synth
+    want = {"tiny_f32": 2, "lm340m_bf16": 3, "recall_apf_bf16": 6, "lm1p3b_apf_bf16": 6,
+            "long_gated_apf_bf16": 7}
+    for name, n in want.items():
+        w = synth.WORKLOADS[name]
+        x = {"r": 1 if w.apf else None, "alpha": 1 if w.gated else None}
+        assert bench.launches_per_step(w, x, sms=152) == n, name
+
+
 FAKE = 0x10000  # never dereferenced: every case below fails validation first
 
 
@@ -148,12 +162,58 @@ def test_chunk_fwd_workspace_size(L):
         assert L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, V) == want, (B, H, T, K, V)
 
 
+def fwd(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, v=3 * FAKE, beta=4 * FAKE,
+        r=None, d0=None, alpha=None, S0=None, o=5 * FAKE, dT=None, ST=None, ws=6 * FAKE, wsb=None):
+    if wsb is None:   # exactly what the shape needs
+        wsb = L.osdn_forward_workspace_bytes(io, B, H, T, K, V)
+    return L.osdn_forward(io, B, H, T, K, V, q, k, v, beta, r, 0.1, d0, alpha, S0, o, dT, ST, ws,
+                          wsb, None)
+
+
+def test_host_validation_forward(L):
+    assert fwd(L, io=2) == -3
+    assert fwd(L, K=96) == -2 and fwd(L, V=32) == -2 and fwd(L, T=-1) == -2
+    assert fwd(L, B=4096, H=4097) == -2      # more than 2^24 sequences
+    assert fwd(L, ws=None) == -5 and fwd(L, wsb=8) == -5
+    need = L.osdn_forward_workspace_bytes(1, 1, 1, 8, 64, 64)
+    assert fwd(L, wsb=need - 1) == -5
+    assert fwd(L, q=None) == -1 and fwd(L, k=None) == -1 and fwd(L, v=None) == -1
+    assert fwd(L, beta=None) == -1 and fwd(L, o=None) == -1
+    assert fwd(L, v=3 * FAKE + 2) == -4 and fwd(L, dT=7 * FAKE + 4) == -4
+    assert fwd(L, o=FAKE) == -9              # o aliases q
+    assert fwd(L, dT=2 * FAKE) == -9         # d_T aliases k
+    assert fwd(L, ST=5 * FAKE) == -9         # S_T aliases o
+    assert fwd(L, ws=FAKE) == -9             # the workspace overlaps q
+    assert fwd(L, ws=5 * FAKE - 64) == -9    # ... runs into o
+    assert fwd(L, H=0) == 0                  # empty batch: nothing to do
+    cap = (0x7fffffff // 128) * 64           # the tensor-core Phase 2's cap on T
+    assert fwd(L, T=cap + 1, wsb=1 << 62) == -2
+    assert fwd(L, io=0, T=cap + 1, wsb=1 << 62) != -2
+
+
+def test_forward_workspace_size(L):
+    # bf16: the scan's segment scratch, e_t (4 bytes a token), d at every 64th
+    # token (4 K bytes), then osdn_chunk_fwd's workspace; fp32: the scan's
+    # scratch and ktilde in fp32; each part rounded up to 256 bytes
+    r = lambda x: -(-x // 256) * 256
+    assert L.osdn_forward_workspace_bytes(1, 2, 3, 0, 128, 64) == 256
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (2, 16, 8192, 128, 128),
+                          (1, 16, 65536, 128, 128), (1, 2, 3217, 64, 64)]:
+        BH = B * H
+        p1 = L.osdn_precond_scan_workspace_bytes(B, H, T, K) - 256
+        p2 = L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, V) - 256
+        want = 256 + r(p1) + r(BH * T * 4) + r(BH * (-(-T // 64)) * K * 4) + r(p2)
+        assert L.osdn_forward_workspace_bytes(1, B, H, T, K, V) == want, (B, H, T, K, V)
+        assert L.osdn_forward_workspace_bytes(0, B, H, T, K, V) == 256 + r(p1) + r(BH * T * K * 4)
+
+
 def test_no_gpu_means_cuda_error_not_crash(L):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert scan(L) in (-6, -10)
     assert chunk(L) in (-6, -10)
+    assert fwd(L) in (-6, -10)
 
 
 def decode(L, io=1, B=1, H=1, K=64, V=64, q=FAKE, k=2 * FAKE, v=3 * FAKE, beta=4 * FAKE, r=None,
