@@ -129,16 +129,17 @@ def launches_per_step(w, x, per_channel=False, sms=None):
     most 64 of them; a sequence of 32 to 64 chunks in two slabs when the
     chain leaves half the SMs free), or, with a decay and time segments, one
     preparation launch, the speculative chain launch and one repair launch
-    per later segment; fp32 I/O and a per-channel decay run one kernel."""
+    per later segment (a per-channel decay takes the same schedule); fp32 I/O
+    runs one kernel."""
     BH, T, V = w.B * w.H, w.T, w.V
     sms = sm_count() if sms is None else sms
     nseg = precond_segments(BH, T, x["r"] is not None, sms)
     p1 = 2 if nseg > 1 else 1
-    if w.io != "bf16" or per_channel:
+    if w.io != "bf16":
         return p1 + 1
     nch = (T + 63) // 64
     cseg = chain_segments(BH, T, V, sms)
-    if x["alpha"] is not None and cseg > 1:
+    if (x["alpha"] is not None or per_channel) and cseg > 1:
         L = (nch + cseg - 1) // cseg
         return p1 + 1 + (nch + L - 1) // L
     per = 64
@@ -829,7 +830,7 @@ def run_kda(args, local_rank):
         "higher_is_better": True, "dtype": w.io, "data": "synthetic",
         "config": {"workload": w.name + "_kda", "B": w.B, "H": w.H, "T": w.T, "d_k": w.K,
                    "d_v": w.V, "l2": "inputs larger than L2"},
-        "roofline": {"kernel": "precond scan + delta_simt_kernel (per-channel)", "bound": "hbm",
+        "roofline": {"kernel": "osdn_precond_scan + osdn_chunk_fwd_kda", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "algorithmic_bytes": nbytes,
                      "peak_source": peak_src, "traffic": None},

@@ -364,9 +364,19 @@ int osdn_backward(int io, int B, int H, int T, int K, int V, const void *q, cons
  *   alpha_k      in [B][H][T][K] fp32, or NULL (no decay)
  *   S0           in [B][H][V][K] fp32, or NULL (zeros)
  *   o            out [B][H][T][V] io;  ST out [B][H][V][K] fp32, or NULL
- * Both I/O types run the token recurrence in fp32 FFMA, one CTA per 32
- * value rows.  With T == 0 the call writes ST = S0.  Outputs must not
- * overlap inputs (OSDN_ERR_ALIAS).
+ * io == OSDN_BF16 runs on the tensor cores, like osdn_chunk_fwd: with
+ * Gam the within-chunk product of alpha per channel, the chunk Gram and
+ * scores take (Gam . k) . (ktilde / Gam), evaluated against a reference
+ * point per 16-token block so that no factor leaves the fp32 range; the
+ * state rows decay by their own channel's product.  There every entry of
+ * alpha_k must lie in [2^-6, 2^6]; one outside it (or not finite) is
+ * recorded as OSDN_ERR_DEVICE in the status word and the outputs are then
+ * undefined.  The workspace holds the prepared operands of every chunk and
+ * each chunk's per-channel decay product (osdn_chunk_fwd_kda_workspace_bytes);
+ * T is limited as for osdn_chunk_fwd.  io == OSDN_F32 runs the token
+ * recurrence in fp32 FFMA, one CTA per 32 value rows, with any decay, and
+ * needs only the 256-byte status header.  With T == 0 the call writes
+ * ST = S0.  Outputs must not overlap inputs (OSDN_ERR_ALIAS).
  */
 size_t osdn_chunk_fwd_kda_workspace_bytes(int io, int B, int H, int T, int K, int V);
 int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,

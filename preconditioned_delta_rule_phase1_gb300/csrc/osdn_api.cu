@@ -35,6 +35,11 @@ cudaError_t delta_simt_launch(int io, int BH, int T, int K, int V, const void *q
                               const float *alpha, const float *S0, void *o, float *ST,
                               cudaStream_t stream);
 size_t delta_tc_scratch_bytes(int BH, int T, int K, int V);
+size_t delta_tc_kda_scratch_bytes(int BH, int T, int K, int V);
+cudaError_t delta_tc_kda_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                                const void *kt, const void *v, const float *beta,
+                                const float *alpha_k, const float *S0, void *o, float *ST,
+                                void *scratch, int *status, cudaStream_t stream);
 cudaError_t delta_tc_launch(int BH, int T, int K, int V, const void *q, const void *k,
                             const void *kt, const void *v, const float *beta, const float *alpha,
                             const float *S0, void *o, float *ST, void *scratch, int *status,
@@ -192,8 +197,11 @@ size_t osdn_backward_kda_workspace_bytes(int B, int H, int T, int K, int V) {
 }
 
 size_t osdn_chunk_fwd_kda_workspace_bytes(int io, int B, int H, int T, int K, int V) {
-    (void)io; (void)B; (void)H; (void)T; (void)K; (void)V;
-    return kStatusBytes;   // the fp32 FFMA recurrence needs no scratch
+    if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return kStatusBytes;
+    // fp32 I/O runs the FFMA recurrence, which needs no scratch; bf16 keeps
+    // each chunk's prepared operands and its per-channel decay product
+    if (io != OSDN_BF16 || T == 0 || T > kMaxTcTokens) return kStatusBytes;
+    return kStatusBytes + osdn::delta_tc_kda_scratch_bytes(B * H, T, K, V);
 }
 
 int osdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
@@ -566,6 +574,7 @@ int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q,
                        void *workspace, size_t workspace_bytes, void *stream) {
     if (io != OSDN_F32 && io != OSDN_BF16) return OSDN_ERR_DTYPE;
     if (!dims_ok(B, H, T) || !width_ok(K) || !width_ok(V)) return OSDN_ERR_DIMS;
+    if (io == OSDN_BF16 && T > kMaxTcTokens) return OSDN_ERR_DIMS;
     if (!workspace || workspace_bytes < osdn_chunk_fwd_kda_workspace_bytes(io, B, H, T, K, V))
         return OSDN_ERR_WORKSPACE;
     const size_t BH = (size_t)B * H;
@@ -593,6 +602,14 @@ int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q,
     cudaError_t e;
     if (T == 0)
         e = osdn::fill_state_launch(ST ? sb / 4 : 0, S0, 0.0f, ST, (cudaStream_t)stream);
+    else if (io == OSDN_BF16 && alpha_k)  // tensor cores, the decay folded in per channel
+        e = osdn::delta_tc_kda_launch((int)BH, T, K, V, q, k, ktilde, v, beta, alpha_k, S0, o, ST,
+                                      static_cast<char *>(workspace) + kStatusBytes,
+                                      static_cast<int *>(workspace), (cudaStream_t)stream);
+    else if (io == OSDN_BF16)  // no decay: the scalar-gate tensor-core path without a gate
+        e = osdn::delta_tc_launch((int)BH, T, K, V, q, k, ktilde, v, beta, nullptr, S0, o, ST,
+                                  static_cast<char *>(workspace) + kStatusBytes,
+                                  static_cast<int *>(workspace), (cudaStream_t)stream);
     else
         e = osdn::delta_simt_kda_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, alpha_k, S0,
                                         o, ST, (cudaStream_t)stream);

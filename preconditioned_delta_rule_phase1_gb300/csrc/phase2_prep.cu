@@ -37,7 +37,24 @@
 // rebuilt preconditioner carries about 2^-16 relative error instead of the
 // 2^-9 of one bf16 product.  The four tiles use space that is dead at that
 // point: W over L, its remainder over Xb / Xb diag(g), P over A, its
-// remainder over Kt.  A decay alpha that is not positive and finite (its
+// remainder over Kt.
+//
+// Decay per key channel (template flag PCH; S_t = S_{t-1} Diag(alpha_t) +
+// ..., alpha_t a K-vector): with Gam_t the within-chunk inclusive product of
+// alpha_t (per channel), the Gram and the scores become
+//   (Gam_t . k_t) . (kt_s / Gam_s)   and   (Gam_t . q_t) . (kt_s / Gam_s),
+// the decay can no longer be factored out of the dot products, and 1/Gam
+// would overflow under strong decay.  So each 16-token block b of rows takes
+// a reference point m = 16 b - 1 (the token before the block): rows are
+// scaled by Gam_t / Gam_m <= 1 and the columns of a copy of Kt by Gam_m /
+// Gam_s (<= 1 before the block, at most the product of 16 decays' inverses
+// inside it; 0 past it), and four M=128 products, one per reference, fill
+// the 256 TMEM columns; row t reads its block's.  Two copies of Kt at a time
+// live in the dead L and Xb tiles.  Then K rows are rescaled to Gam . K (for
+// Kw), Kt to (Gam_C / Gam_s) . kt (for W and M), Q to Gam . Q inside the Qe
+// epilogue, and the chunk's Gam_C goes to the workspace per channel.  The
+// decay must lie in [2^-6, 2^6] (every factor then stays inside the fp32 and
+// bf16 range); anything else is recorded as OSDN_ERR_DEVICE.  A decay alpha that is not positive and finite (its
 // log enters the algebra), or a beta that is not finite, is recorded in the
 // status word as OSDN_ERR_DEVICE.
 #include "tc_common.cuh"
@@ -51,6 +68,19 @@ constexpr int kLP = 68;              // fp32 pitch of the solver tile
 constexpr int kPrepThreads = 256;    // compute warps 0-7
 constexpr int kPrepBlock = 288;      // + the control warp
 constexpr uint32_t kPrepCols = 256;  // TMEM columns
+constexpr float kMinDecay = 0.015625f, kMaxDecay = 64.0f;   // per-channel decay range (2^-6, 2^6)
+
+// Byte offset of element (r, c) in a 128B-swizzled tile whose 64-column
+// blocks hold `rows` rows of 128 bytes (the layout st_row_sw128 writes).
+__device__ __forceinline__ int sw_off(int rows, int r, int c) {
+    return (c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
+}
+__device__ __forceinline__ float ld_bf(const uint8_t *tile, int off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
+}
+__device__ __forceinline__ void st_bf(uint8_t *tile, int off, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(v);
+}
 
 struct PrepParams {
     int BH, T, nch, c0;   // sequences, sequence length, its chunks, first chunk of this launch
@@ -59,7 +89,8 @@ struct PrepParams {
     const float *r;       // fused: retention r_t [BH][T], or NULL (r = 1)
     const float *ecoef;   // fused: e_t [BH][T]
     const float *dchk;    // fused: d entering each chunk [BH][nch][K]
-    float *gc;
+    const float *alpha_k; // per-channel decay [BH][T][K] (PCH)
+    float *gc;            // g_C per chunk [BH][nch], or per channel [BH][nch][K] (PCH)
     int *status;
 };
 
@@ -178,7 +209,7 @@ __device__ void solve_unit_lower(float *sL, int pt) {
     ptx::named_bar(1, kPrepThreads);
 }
 
-template <int K, bool GATED, bool FUSED>
+template <int K, bool GATED, bool FUSED, bool PCH>
 __global__ void __launch_bounds__(kPrepBlock, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_w,
@@ -192,6 +223,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t *smem = align1024(smem_raw);
     __shared__ uint64_t bar_full, bar_g, bar_x2, bar_p1, bar_x3, bar_p2;
     __shared__ uint64_t bar_f0, bar_f1, bar_kt;   // fused: W, P staged; P W done; Kt built
+    // per-channel decay: Kt copies 0 and 1 staged, their products done, copies 2, 3 staged
+    __shared__ uint64_t bar_c01, bar_r0, bar_r1, bar_c2, bar_c3;
+    // per-channel decay: log Gam at the four reference points (0 for block 0)
+    // and at the chunk's end, and the per-group partial sums of log alpha
+    __shared__ float sLref[PCH ? 4 : 1][PCH ? K : 1], sLamC[PCH ? K : 1];
+    __shared__ float sGrp[PCH ? 256 / K : 1][PCH ? K : 1];
     __shared__ uint32_t tmem_base_sh;
     __shared__ float sBeta[C], sLg[C], sD[C];
     // fused: e_t, r_t, and sPre[b][t] = prod_{16 b <= v < t} r_v (1 for t <= 16 b):
@@ -220,7 +257,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     if (tid == kPrepThreads) {
         uint64_t *all[] = {&bar_full, &bar_g, &bar_x2, &bar_p1, &bar_x3, &bar_p2,
-                           &bar_f0, &bar_f1, &bar_kt};
+                           &bar_f0, &bar_f1, &bar_kt, &bar_c01, &bar_r0, &bar_r1, &bar_c2, &bar_c3};
         for (uint64_t *b : all) ptx::mbar_init(b, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -285,7 +322,26 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 ok = ok && wait_poll(&bar_kt, 0, &s_abort, st);
             }
-            if (ok) {  // [K;Q] Kt^T (M=128): Gram rows 0-63, scores rows 64-127
+            if (ok && PCH) {  // one [K;Q] Kt_b^T product per reference point b (columns 64 b..)
+                const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
+                const uint64_t da = dk0(aKQ);
+                const uint64_t dbuf[2] = {dk0(ptx::smem_u32(smem + LY::oL)), dk0(aXb)};
+                uint64_t *staged[4] = {&bar_c01, &bar_c01, &bar_c2, &bar_c3};
+                uint64_t *done[4] = {&bar_r0, &bar_r1, &bar_g, &bar_g};
+                for (int b = 0; b < 4 && ok; ++b) {
+                    if (b != 1) ok = wait_poll(staged[b], 0, &s_abort, st);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < K / 16; ++ks)
+                        ptx::umma_bf16(tmem + 64 * b, da + koff(128, ks), dbuf[b & 1] + koff(C, ks), id,
+                                       ks > 0);
+                    if (b != 2) {
+                        ptx::umma_commit(done[b]);
+                        last = done[b];
+                    }
+                }
+            } else if (ok) {  // [K;Q] Kt^T (M=128): Gram rows 0-63, scores rows 64-127
                 ptx::tc_fence_after();
                 const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
                 const uint64_t da = dk0(aKQ), db = dk0(aKt);
@@ -405,6 +461,95 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
 
         bool fok = true;
+        if (PCH) {
+            // ---- log Gam per channel: thread (f, grp) sums log alpha over its tokens
+            constexpr int QT = kPrepThreads / K, TPT = C / QT;
+            const int f = pt % K, grp = pt / K;
+            float lam[TPT];
+            {
+                float run = 0.0f;
+                bool bad = false;
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int t = grp * TPT + i;
+                    float a = t < nvalid ? p.alpha_k[((size_t)seq * T + t0 + t) * K + f] : 1.0f;
+                    if (!(a >= kMinDecay && a <= kMaxDecay)) {   // NaN fails too
+                        bad = true;
+                        a = 1.0f;
+                    }
+                    run += logf(a);
+                    lam[i] = run;
+                }
+                if (bad) report_status(p.status, OSDN_ERR_DEVICE);
+                sGrp[grp][f] = run;
+            }
+            ptx::named_bar(1, kPrepThreads);
+            {
+                float off = 0.0f;
+                for (int g2 = 0; g2 < grp; ++g2) off += sGrp[g2][f];
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    lam[i] += off;
+                    const int t = grp * TPT + i;
+                    if ((t & 15) == 15 && t < C - 1) sLref[(t >> 4) + 1][f] = lam[i];
+                    if (t == C - 1) {   // tokens past T add nothing: this is the chunk's Gam_C
+                        sLamC[f] = lam[i];
+                        p.gc[((size_t)seq * nch + j) * K + f] = expf(lam[i]);
+                    }
+                }
+                if (grp == 0) sLref[0][f] = 0.0f;
+            }
+            ptx::named_bar(1, kPrepThreads);
+            // ---- once the tiles have landed: [K;Q] rows relative to their block's
+            // reference, then the reference copies of Kt, two at a time
+            fok = vote_all(wait_poll(&bar_full, 0, &s_abort, st), 1, kPrepThreads);
+            uint8_t *bufs[2] = {smem + LY::oL, sXb};
+            auto copy_kt = [&](int b) {
+                uint8_t *buf = bufs[b & 1];
+                const float ref = sLref[b][f];
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int s_ = grp * TPT + i, off = sw_off(C, s_, f);
+                    const float v = s_ < 16 * (b + 1) ? ld_bf(sKt, off) * expf(ref - lam[i]) : 0.0f;
+                    st_bf(buf, off, v);
+                }
+            };
+            if (fok) {
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int t = grp * TPT + i;
+                    const float fac = expf(lam[i] - sLref[t >> 4][f]);
+                    const int ok_ = sw_off(128, t, f), oq = sw_off(128, C + t, f);
+                    st_bf(sKQ, ok_, ld_bf(sKQ, ok_) * fac);
+                    st_bf(sKQ, oq, ld_bf(sKQ, oq) * fac);
+                }
+                copy_kt(0);
+                copy_kt(1);
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(1, kPrepThreads);
+                if (pt == 0) ptx::mbar_arrive(&bar_c01);
+            }
+            fok = fok && vote_all(wait_poll(&bar_r0, 0, &s_abort, st), 1, kPrepThreads);
+            if (fok) {   // reference 0's product has read its buffer
+                copy_kt(2);
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(1, kPrepThreads);
+                if (pt == 0) ptx::mbar_arrive(&bar_c2);
+            }
+            fok = fok && vote_all(wait_poll(&bar_r1, 0, &s_abort, st), 1, kPrepThreads);
+            if (fok) {
+                copy_kt(3);
+                // Kt itself to (Gam_C / Gam_s) . kt for W and M (no product reads it raw)
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int off = sw_off(C, grp * TPT + i, f);
+                    st_bf(sKt, off, ld_bf(sKt, off) * expf(sLamC[f] - lam[i]));
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(1, kPrepThreads);
+                if (pt == 0) ptx::mbar_arrive(&bar_c3);
+            }
+        }
         if (FUSED) {
             // ---- P = pi . e (strictly lower): high part over A, remainder over Kt
             {
@@ -485,7 +630,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (ok) {
             ptx::tc_fence_after();
             float g[32];
-            tmem_ld32(tmem + lane_off + 32 * half, g);
+            if (PCH) {  // lanes 0-15 of the warp read block b0's reference, 16-31 block b0+1's
+                const int b0 = 2 * (q4 & 1);
+                float g1[32];
+                tmem_ld32(tmem + lane_off + 64 * b0 + 32 * half, g);
+                tmem_ld32(tmem + lane_off + 64 * (b0 + 1) + 32 * half, g1);
+                if (lane >= 16) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) g[jj] = g1[jj];
+                }
+            } else {
+                tmem_ld32(tmem + lane_off + 32 * half, g);
+            }
             const int grow = 32 * q4 + lane;
             if (grow < C) {  // L = tril(diag(beta) (G . K Kt^T), -1)
                 const int i = grow;
@@ -521,6 +677,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         wv[e] = pack_bf16x2(x.x * f, x.y * f);
                     }
                     *q = u;
+                }
+            }
+            if (PCH) {  // K rows to Gam . K for Kw (the Gram products have read them)
+                constexpr int QT = kPrepThreads / K, TPT = C / QT;
+                const int f = pt % K, grp = pt / K;
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int t = grp * TPT + i, off = sw_off(128, t, f);
+                    st_bf(sKQ, off, ld_bf(sKQ, off) * expf(sLref[t >> 4][f]));
                 }
             }
             ptx::tc_fence_before();
@@ -608,7 +773,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     float qv[16];
                     ld_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) qv[e] = fmaf(gt, qv[e], -d[c + e]);
+                    for (int e = 0; e < 16; ++e) {
+                        // PCH: Q rows hold (Gam_t / Gam_m) . q_t; Gam_m restores Gam . q
+                        const float ge = PCH ? expf(sLref[mrow >> 4][half * NH + c + e]) : gt;
+                        qv[e] = fmaf(ge, qv[e], -d[c + e]);
+                    }
                     st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
                 }
             }
@@ -630,7 +799,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (warp == 8) ptx::tmem_dealloc(tmem, kPrepCols);
 }
 
-template <int K, bool GATED, bool FUSED>
+template <int K, bool GATED, bool FUSED, bool PCH>
 cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const void *k,
                           const void *kt, const float *beta, const float *alpha, const Fused &fz,
                           __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae,
@@ -645,7 +814,7 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
     constexpr int smem = PrepLay<K>::kAlloc;
     static std::atomic<unsigned long long> attr_done{0};
     {
-        cudaError_t e = smem_attr_once((const void *)chunk_prep_kernel<K, GATED, FUSED>, smem, attr_done);
+        cudaError_t e = smem_attr_once((const void *)chunk_prep_kernel<K, GATED, FUSED, PCH>, smem, attr_done);
         if (e != cudaSuccess) return e;
     }
     PrepParams p;
@@ -657,12 +826,13 @@ cudaError_t prep_launch_t(int BH, int T, int c0, int c1, const void *q, const vo
     p.r = fz.r;
     p.ecoef = fz.ecoef;
     p.dchk = fz.dchk;
+    p.alpha_k = fz.alpha_k;
     p.gc = gc;
     p.status = status;
     p.BH = BH;
     p.ahead = 2 * sm_count();   // two CTAs per SM
     const dim3 grid = seq_grid(c1 - c0, BH);
-    chunk_prep_kernel<K, GATED, FUSED><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
+    chunk_prep_kernel<K, GATED, FUSED, PCH><<<grid, kPrepBlock, smem, stream>>>(mk, mq, mkt, mw, mm, mqe, mae, p);
     return cudaGetLastError();
 }
 
@@ -671,20 +841,23 @@ cudaError_t prep_launch_k(int BH, int T, int c0, int c1, const void *q, const vo
                           const void *kt, const float *beta, const float *alpha, const Fused &fz,
                           __nv_bfloat16 *w, __nv_bfloat16 *m, __nv_bfloat16 *qe, __nv_bfloat16 *ae,
                           float *gc, int *status, cudaStream_t stream) {
+    if (fz.alpha_k)
+        return prep_launch_t<K, false, false, true>(BH, T, c0, c1, q, k, kt, beta, nullptr, fz, w, m, qe, ae, gc, status, stream);
     if (fz.ecoef) {
         if (alpha)
-            return prep_launch_t<K, true, true>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
-        return prep_launch_t<K, false, true>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+            return prep_launch_t<K, true, true, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<K, false, true, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
     }
     if (alpha)
-        return prep_launch_t<K, true, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
-    return prep_launch_t<K, false, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+        return prep_launch_t<K, true, false, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
+    return prep_launch_t<K, false, false, false>(BH, T, c0, c1, q, k, kt, beta, alpha, fz, w, m, qe, ae, gc, status, stream);
 }
 
 }  // namespace
 
 // Chunks [c0, c1) of every sequence.  With fz.ecoef given (the fused forward
-// pass) Kt is rebuilt from the preconditioner's checkpoints instead of read.
+// pass) Kt is rebuilt from the preconditioner's checkpoints instead of read;
+// with fz.alpha_k the decay is per key channel.
 cudaError_t chunk_prep_launch(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
                               const void *kt, const float *beta, const float *alpha,
                               const Fused &fz, __nv_bfloat16 *w, __nv_bfloat16 *m,

@@ -121,7 +121,9 @@ struct Bars {
     uint64_t o_full[2], o_free[2];
 };
 
-template <int K, bool GATED>
+// GATED: a decay; PCH: the decay is per key channel (g_C is then a K-vector
+// per chunk, and row k of S^T decays by its own entry).
+template <int K, bool GATED, bool PCH>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_m,
                    const __grid_constant__ CUtensorMap tm_ae, const __grid_constant__ CUtensorMap tm_qe,
@@ -346,7 +348,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         const bool act = (K == 128) || lane < 16;
         const uint32_t tS = tmem + lane_off + kColS + c0;
         {  // initial state: TMEM S^T = g_C(0) S0^T, bf16 copy = S0^T
-            const float g0 = GATED ? p.gc[(size_t)seq * nch + cbase] : 1.0f;
+            const float g0 = !GATED ? 1.0f
+                             : PCH ? (act ? p.gc[((size_t)seq * nch + cbase) * K + krow] : 1.0f)
+                                   : p.gc[(size_t)seq * nch + cbase];
             float sv[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -370,7 +374,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         }
         for (int j = 0; j < ncs; ++j) {
             const bool last = (j == ncs - 1);
-            const float gN = (GATED && !last) ? p.gc[(size_t)seq * nch + cbase + j + 1] : 1.0f;
+            const float gN = (!GATED || last) ? 1.0f
+                             : PCH ? (act ? p.gc[((size_t)seq * nch + cbase + j + 1) * K + krow] : 1.0f)
+                                   : p.gc[(size_t)seq * nch + cbase + j + 1];
             // the copy entering chunk j+1 overwrites the one chunk j-2's output read
             const int n = j + 1;
             const bool okw = (last || n < NSB ||
@@ -429,7 +435,7 @@ struct ChainOpt {
 
 // Chunks [c0, c1) of every sequence, from the state S0 (NULL: zeros) to ST
 // (NULL: not written).
-template <int K, bool GATED>
+template <int K, bool GATED, bool PCH>
 cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
                            const __nv_bfloat16 *w, const __nv_bfloat16 *m,
                            const __nv_bfloat16 *qe, const __nv_bfloat16 *ae, const float *gc,
@@ -444,7 +450,7 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
     constexpr int smem = Lay<K>::kAlloc;
     static std::atomic<unsigned long long> attr_done{0};
     {
-        cudaError_t e = smem_attr_once((const void *)chunk_chain_kernel<K, GATED>, smem, attr_done);
+        cudaError_t e = smem_attr_once((const void *)chunk_chain_kernel<K, GATED, PCH>, smem, attr_done);
         if (e != cudaSuccess) return e;
     }
     Params p;
@@ -467,7 +473,7 @@ cudaError_t chain_launch_t(int BH, int T, int V, int c0, int c1, const void *v,
     p.BH = BH;
     const dim3 grid = seq_grid(V / BV, BH, opt.seg_len > 0 ? opt.nseg : 1);
     p.nz = (int)((BH + grid.y - 1) / grid.y);
-    chunk_chain_kernel<K, GATED><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
+    chunk_chain_kernel<K, GATED, PCH><<<grid, kThreads, smem, stream>>>(mw, mm, mae, mqe, mv, p);
     return cudaGetLastError();
 }
 
@@ -496,13 +502,13 @@ struct Carve {
     size_t bytes;
 };
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-Carve carve(void *base, int BH, int T, int K, int V) {
+Carve carve(void *base, int BH, int T, int K, int V, bool pch = false) {
     const size_t nch = (size_t)(T + C - 1) / C, Tp = nch * C;
     const int nseg = chain_segments(BH, T, V);
     const size_t segb = nseg > 1 ? round256((size_t)nseg * BH * V * K * 4) : 0;
     const size_t sz[9] = {round256((size_t)BH * nch * K * C * 2), round256((size_t)BH * nch * K * K * 2),
                           round256((size_t)BH * Tp * K * 2), round256((size_t)BH * Tp * C * 2),
-                          round256((size_t)BH * nch * 4), round256((size_t)BH * V * K * 4),
+                          round256((size_t)BH * nch * (pch ? K : 1) * 4), round256((size_t)BH * V * K * 4),
                           round256((size_t)BH * V * K * 4), segb, segb};
     char *b = static_cast<char *>(base);
     char *ptrs[9];
@@ -590,6 +596,10 @@ size_t delta_tc_scratch_bytes(int BH, int T, int K, int V) {
     return tc::carve(nullptr, BH, T, K, V).bytes;
 }
 
+size_t delta_tc_kda_scratch_bytes(int BH, int T, int K, int V) {
+    return tc::carve(nullptr, BH, T, K, V, true).bytes;
+}
+
 namespace {
 cudaError_t prep_range(int BH, int T, int K, int c0, int c1, const void *q, const void *k,
                        const void *kt, const float *beta, const float *alpha, const tc::Fused &fz,
@@ -597,17 +607,23 @@ cudaError_t prep_range(int BH, int T, int K, int c0, int c1, const void *q, cons
     return tc::chunk_prep_launch(BH, T, K, c0, c1, q, k, kt, beta, alpha, fz, w.w, w.m, w.qe, w.ae,
                                  w.gc, status, stream);
 }
-cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void *v, const float *alpha,
-                        const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
-                        cudaStream_t stream, const tc::ChainOpt &opt = tc::ChainOpt()) {
-    if (K == 128) {
-        if (alpha)
-            return tc::chain_launch_t<128, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
-        return tc::chain_launch_t<128, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
-    }
+template <int K>
+cudaError_t chain_range_k(int BH, int T, int V, int c0, int c1, const void *v, const float *alpha,
+                          bool pch, const tc::Carve &w, const float *S0, void *o, float *ST,
+                          int *status, cudaStream_t stream, const tc::ChainOpt &opt) {
+    if (pch)
+        return tc::chain_launch_t<K, true, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
     if (alpha)
-        return tc::chain_launch_t<64, true>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
-    return tc::chain_launch_t<64, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+        return tc::chain_launch_t<K, true, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+    return tc::chain_launch_t<K, false, false>(BH, T, V, c0, c1, v, w.w, w.m, w.qe, w.ae, w.gc, S0, o, ST, status, stream, opt);
+}
+// `alpha` is a scalar decay [BH][T] or, with pch, one per key channel [BH][T][K].
+cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void *v, const float *alpha,
+                        bool pch, const tc::Carve &w, const float *S0, void *o, float *ST,
+                        int *status, cudaStream_t stream, const tc::ChainOpt &opt = tc::ChainOpt()) {
+    if (K == 128)
+        return chain_range_k<128>(BH, T, V, c0, c1, v, alpha, pch, w, S0, o, ST, status, stream, opt);
+    return chain_range_k<64>(BH, T, V, c0, c1, v, alpha, pch, w, S0, o, ST, status, stream, opt);
 }
 
 // With a decay the state forgets where it started, so the chain can run in
@@ -618,7 +634,7 @@ cudaError_t chain_range(int BH, int T, int K, int V, int c0, int c1, const void 
 // the segment is recomputed from that exact end.  Every accepted start is
 // therefore that close to the state the unsegmented chain would carry in.
 cudaError_t chain_segmented(int BH, int T, int K, int V, int nch, const void *v, const float *alpha,
-                            const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
+                            bool pch, const tc::Carve &w, const float *S0, void *o, float *ST, int *status,
                             cudaStream_t stream) {
     const int nseg = w.nseg, L = (nch + nseg - 1) / nseg;
     const size_t sstride = (size_t)BH * V * K;
@@ -628,13 +644,13 @@ cudaError_t chain_segmented(int BH, int T, int K, int V, int nch, const void *v,
     spec.nseg = (nch + L - 1) / L;
     spec.seg_spec = w.seg_spec;
     spec.seg_end = w.seg_end;
-    cudaError_t e = chain_range(BH, T, K, V, 0, nch, v, alpha, w, S0, o, ST, status, stream, spec);
+    cudaError_t e = chain_range(BH, T, K, V, 0, nch, v, alpha, pch, w, S0, o, ST, status, stream, spec);
     for (int i = 1; e == cudaSuccess && i < spec.nseg; ++i) {
         tc::ChainOpt rep;
         rep.check = w.seg_spec + i * sstride;
         const int c0 = i * L, c1 = std::min(nch, c0 + L);
         float *sout = i == spec.nseg - 1 ? ST : w.seg_end + i * sstride;
-        e = chain_range(BH, T, K, V, c0, c1, v, alpha, w, w.seg_end + (i - 1) * sstride, o, sout,
+        e = chain_range(BH, T, K, V, c0, c1, v, alpha, pch, w, w.seg_end + (i - 1) * sstride, o, sout,
                         status, stream, rep);
     }
     return e;
@@ -647,7 +663,9 @@ cudaError_t delta_tc_impl(int BH, int T, int K, int V, const void *q, const void
                           const tc::Fused &fz, const float *S0, void *o, float *ST, void *scratch,
                           int *status, cudaStream_t stream) {
     if (!tc::tensor_map_encoder_ready()) return cudaErrorNotSupported;
-    const tc::Carve w = tc::carve(scratch, BH, T, K, V);
+    const bool pch = fz.alpha_k != nullptr;        // a decay per key channel
+    const float *decay = pch ? fz.alpha_k : alpha;
+    const tc::Carve w = tc::carve(scratch, BH, T, K, V, pch);
     const int nch = (T + tc::C - 1) / tc::C;
     int per = tc::kSlabChunks;
     while ((nch + per - 1) / per > tc::kMaxSlabs) per *= 2;
@@ -656,15 +674,15 @@ cudaError_t delta_tc_impl(int BH, int T, int K, int V, const void *q, const void
     if (nch <= per && nch >= 32 && (long long)BH * (V / tc::BV) * 2 <= tc::sm_count())
         per = (nch + 1) / 2;
     const int nslab = (nch + per - 1) / per;
-    if (alpha && w.nseg > 1) {  // a decay: every chunk prepared, then the chain in time segments
+    if (decay && w.nseg > 1) {  // a decay: every chunk prepared, then the chain in time segments
         cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, fz, w, status, stream);
         if (e != cudaSuccess) return e;
-        return chain_segmented(BH, T, K, V, nch, v, alpha, w, S0, o, ST, status, stream);
+        return chain_segmented(BH, T, K, V, nch, v, decay, pch, w, S0, o, ST, status, stream);
     }
     if (nslab <= 1) {  // one slab: preparation, then the chain, on the caller's stream
         cudaError_t e = prep_range(BH, T, K, 0, nch, q, k, kt, beta, alpha, fz, w, status, stream);
         if (e != cudaSuccess) return e;
-        return chain_range(BH, T, K, V, 0, nch, v, alpha, w, S0, o, ST, status, stream);
+        return chain_range(BH, T, K, V, 0, nch, v, decay, pch, w, S0, o, ST, status, stream);
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -691,7 +709,7 @@ cudaError_t delta_tc_impl(int BH, int T, int K, int V, const void *q, const void
         if (s >= 1 && (e = cudaStreamWaitEvent(ov->chain, ev[1 + s], 0)) != cudaSuccess) return e;
         const float *sin = s == 0 ? S0 : w.state[(s - 1) & 1];
         float *sout = s == nslab - 1 ? ST : w.state[s & 1];
-        if ((e = chain_range(BH, T, K, V, c0, c1, v, alpha, w, sin, o, sout, status, ov->chain)) !=
+        if ((e = chain_range(BH, T, K, V, c0, c1, v, decay, pch, w, sin, o, sout, status, ov->chain)) !=
             cudaSuccess)
             return e;
     }
@@ -723,6 +741,19 @@ cudaError_t delta_tc_fused_launch(int BH, int T, int K, int V, const void *q, co
     fz.ecoef = ecoef;
     fz.dchk = dchk;
     return delta_tc_impl(BH, T, K, V, q, k, nullptr, v, beta, alpha, fz, S0, o, ST, scratch, status,
+                         stream);
+}
+
+// Phase 2 with a decay per key channel (alpha_k [BH][T][K]) on the tensor
+// cores: the same preparation and chain, with the decay folded into the
+// operands per channel (see phase2_prep.cu) and applied per state row.
+cudaError_t delta_tc_kda_launch(int BH, int T, int K, int V, const void *q, const void *k,
+                                const void *kt, const void *v, const float *beta,
+                                const float *alpha_k, const float *S0, void *o, float *ST,
+                                void *scratch, int *status, cudaStream_t stream) {
+    tc::Fused fz;
+    fz.alpha_k = alpha_k;
+    return delta_tc_impl(BH, T, K, V, q, k, kt, v, beta, nullptr, fz, S0, o, ST, scratch, status,
                          stream);
 }
 

@@ -200,12 +200,14 @@ bool tensor_map_encoder_ready();
 bool make_map(CUtensorMap *m, const void *ptr, int BH, int rows, int width);
 // Streaming multiprocessors of the current device (152 if the query fails).
 int sm_count();
-// Inputs of the fused forward pass's chunk preparation, which rebuilds Kt
-// from the preconditioner scan's checkpoints (all NULL: Kt is read).
+// Extra inputs of the chunk preparation: the fused forward pass's
+// checkpoints, from which it rebuilds Kt (else Kt is read), or a decay per
+// key channel (all NULL: the plain or scalar-gated preparation).
 struct Fused {
     const float *r = nullptr;       // retention r_t [BH][T], or NULL (r = 1)
     const float *ecoef = nullptr;   // e_t [BH][T]
     const float *dchk = nullptr;    // d entering each 64-token chunk [BH][nch][K]
+    const float *alpha_k = nullptr; // a decay per key channel [BH][T][K] instead (not fused)
 };
 
 }  // namespace tc

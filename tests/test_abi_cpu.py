@@ -77,6 +77,10 @@ def test_bench_launch_count_rule():
         w = synth.WORKLOADS[name]
         x = {"r": 1 if w.apf else None, "alpha": 1 if w.gated else None}
         assert bench.launches_per_step(w, x, sms=152) == n, name
+    # a per-channel decay at the 1.3B shape: the scan (2), one preparation
+    # launch and a chain in two time segments (speculative pass + 1 repair)
+    w = synth.WORKLOADS["lm1p3b_apf_bf16"]
+    assert bench.launches_per_step(w, {"r": 1, "alpha": None}, per_channel=True, sms=152) == 5
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails validation first
@@ -288,16 +292,36 @@ def test_backward_workspace_size(L):
 
 
 def kda(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, kt=3 * FAKE, v=4 * FAKE,
-        beta=5 * FAKE, ak=None, S0=None, o=6 * FAKE, ST=None, ws=7 * FAKE, wsb=256):
+        beta=5 * FAKE, ak=None, S0=None, o=6 * FAKE, ST=None, ws=64 * FAKE, wsb=None):
+    if wsb is None:   # exactly what the shape needs (more than FAKE bytes for bf16)
+        wsb = L.osdn_chunk_fwd_kda_workspace_bytes(io, B, H, T, K, V)
     return L.osdn_chunk_fwd_kda(io, B, H, T, K, V, q, k, kt, v, beta, ak, S0, o, ST, ws, wsb,
                                 None)
 
 
+def test_chunk_fwd_kda_workspace_size(L):
+    # fp32 I/O (the FFMA recurrence) needs only the status word; bf16 needs
+    # osdn_chunk_fwd's workspace with the chunk's decay product per channel
+    # (K floats a chunk instead of one)
+    r = lambda x: -(-x // 256) * 256
+    assert L.osdn_chunk_fwd_kda_workspace_bytes(0, 2, 16, 8192, 128, 128) == 256
+    assert L.osdn_chunk_fwd_kda_workspace_bytes(1, 2, 16, 0, 128, 128) == 256
+    for B, H, T, K, V in [(2, 16, 8192, 128, 128), (1, 2, 100, 64, 128), (1, 16, 65536, 128, 64)]:
+        BH, nch = B * H, -(-T // 64)
+        want = (L.osdn_chunk_fwd_workspace_bytes(1, B, H, T, K, V) - r(BH * nch * 4)
+                + r(BH * nch * K * 4))
+        assert L.osdn_chunk_fwd_kda_workspace_bytes(1, B, H, T, K, V) == want, (B, H, T, K, V)
+
+
 def test_host_validation_chunk_fwd_kda(L):
-    assert L.osdn_chunk_fwd_kda_workspace_bytes(1, 2, 16, 8192, 128, 128) == 256
     assert kda(L, io=2) == -3
     assert kda(L, K=32) == -2 and kda(L, V=96) == -2 and kda(L, T=-1) == -2
     assert kda(L, ws=None) == -5 and kda(L, wsb=255) == -5
+    need = L.osdn_chunk_fwd_kda_workspace_bytes(1, 1, 1, 8, 64, 64)
+    assert need > 256 and kda(L, wsb=need - 1) == -5
+    cap = (0x7fffffff // 128) * 64           # the tensor-core path's cap on T
+    assert kda(L, T=cap + 1, wsb=1 << 62) == -2
+    assert kda(L, io=0, T=cap + 1, wsb=1 << 62) != -2
     assert kda(L, q=None) == -1 and kda(L, o=None) == -1 and kda(L, beta=None) == -1
     assert kda(L, ak=8 * FAKE + 4) == -4
     assert kda(L, o=FAKE) == -9                   # o aliases q

@@ -5,7 +5,11 @@ backbone named in section 4 of the gist.science summary), both phases through
 the C ABI against ``oracle.forward_kda``, and the gradients against the
 autograd reference with a per-channel alpha.  Normwise tolerances of the I/O
 type; both I/O types, every (K, V), ragged token counts, T = 0, no decay,
-equal channels against the scalar-gate call, determinism.
+equal channels against the scalar-gate call, determinism.  bf16 runs on the
+tensor cores (the decay folded into the chunk operands per channel against
+a reference point per 16-token block): long sequences cut into slabs and
+into time segments, decays down to the supported 2^-6, and a decay outside
+the supported range reported in the status word.
 """
 import numpy as np
 import pytest
@@ -85,6 +89,77 @@ def test_equal_channels_match_the_scalar_gate():
     # product), so they agree to the fp32 tolerance, not bit for bit
     assert rel_err(o2, o1.double().cpu().numpy()) <= TOL["f32"]
     assert rel_err(S2, S1.double().cpu().numpy()) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("K,V,T,low,high", [
+    (128, 128, 64 * 130 + 17, 0.6, 1.0),     # slabs of chunks, a ragged last chunk
+    (64, 64, 64 * 48, 0.9, 1.0),             # a time-segmented chain (3 segments)
+    (128, 64, 64 * 48, 0.999, 1.0),          # ... whose speculative starts are repaired
+    (128, 128, 300, 0.015625, 0.2),          # decays down to 2^-6: reference points matter
+    (64, 128, 150, 1.0, 1.0),                # alpha = 1 everywhere
+])
+def test_bf16_tensor_core_path(K, V, T, low, high):
+    x = synth.make_random(1, 2, T, K, V, io="bf16", apf=True, s0=True, d0=True, seed=T + K)
+    g = torch.Generator().manual_seed(T + V)
+    x["alpha"] = (low + (high - low) * torch.rand(1, 2, T, K, generator=g)).contiguous()
+    gx = to_cuda(x)
+    ws = ops.Workspace()
+    got = ops.forward_kda(gx["q"], gx["k"], gx["v"], gx["beta"], gx["r"], gx["eta"], gx["d0"],
+                          gx["alpha"], gx["S0"], workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, ops.status_string(ws.status())
+    ref = oracle.forward_kda(x["q"], x["k"], x["v"], x["beta"], x["r"], x["eta"], x["d0"],
+                             x["alpha"], x["S0"])
+    errs = {n: rel_err(a, b) for n, a, b in zip(("ktilde", "dT", "o", "ST"), got, ref)}
+    assert max(errs.values()) <= TOL["bf16"], errs
+    # Phase 2 alone from the GPU's own ktilde
+    o2, S2 = oracle.delta_fwd_kda(x["q"], x["k"], got[0].cpu(), x["v"], x["beta"], x["alpha"],
+                                  x["S0"])
+    assert rel_err(got[2], o2) <= TOL["bf16"] and rel_err(got[3], S2) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("bad", [0.0, 0.01, 100.0, float("nan")])
+def test_bf16_decay_outside_the_supported_range_is_reported(bad):
+    x = case("bf16", 64, 64, 100, 17)
+    g = to_cuda(x)
+    g["alpha"][0, 1, 70, 5] = bad
+    kt, _ = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"])
+    ws = ops.Workspace()
+    ops.chunk_fwd_kda(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"], workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == -8, ops.status_string(ws.status())
+    # the same inputs in fp32 run the FFMA recurrence, which takes any decay
+    ok = ops.Workspace()
+    ops.chunk_fwd_kda(g["q"].float(), g["k"].float(), kt.float(), g["v"].float(), g["beta"],
+                      g["alpha"].nan_to_num(0.5), g["S0"], workspace=ok)
+    torch.cuda.synchronize()
+    assert ok.status() == 0
+
+
+def test_bf16_equal_channels_match_the_scalar_gate():
+    x = synth.make_random(1, 2, 700, 128, 128, io="bf16", apf=True, gated=True, s0=True, seed=19)
+    g = to_cuda(x)
+    kt, _ = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"])
+    ak = g["alpha"][..., None].expand(1, 2, 700, 128).contiguous()
+    o1, S1 = ops.chunk_fwd(g["q"], g["k"], kt, g["v"], g["beta"], g["alpha"], g["S0"])
+    o2, S2 = ops.chunk_fwd_kda(g["q"], g["k"], kt, g["v"], g["beta"], ak, g["S0"])
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.delta_fwd(x["q"], x["k"], kt.cpu(), x["v"], x["beta"], x["alpha"],
+                                    x["S0"])
+    for a, b in ((o1, o_ref), (o2, o_ref), (S1, S_ref), (S2, S_ref)):
+        assert rel_err(a, b) <= TOL["bf16"]
+
+
+def test_bf16_deterministic():
+    x = case("bf16", 128, 128, 1000, 23)
+    g = to_cuda(x)
+    a = ops.forward_kda(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"], g["alpha"],
+                        g["S0"])
+    b = ops.forward_kda(g["q"], g["k"], g["v"], g["beta"], g["r"], g["eta"], g["d0"], g["alpha"],
+                        g["S0"])
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
 
 
 BWD = [("f32", 64, 64, 50), ("f32", 128, 64, 5), ("bf16", 128, 128, 100), ("bf16", 64, 128, 33)]
