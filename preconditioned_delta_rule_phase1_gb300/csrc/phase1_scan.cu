@@ -67,7 +67,7 @@ namespace p1 {
 
 constexpr int C = 16;          // tokens per chunk
 constexpr int NST = 4;         // key chunks in flight per warp
-constexpr int kWarm = 128;     // warm-up tokens in front of a speculative segment (fp32 I/O)
+constexpr int kWarm = 128;     // longest warm-up in front of a speculative segment
 constexpr int kMinSeg = 256;   // shortest segment
 constexpr int kMaxWarps = 4;   // warps (segments) per CTA
 constexpr int kDefaultSms = 152;  // GB300; used only when no device can be queried
@@ -756,6 +756,33 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
     }
 }
 
+// Warm-up length of speculative segment starting at tseg (all 32 lanes call
+// this).  The start is estimated by scanning the W tokens before it from
+// d = 0; the estimate's error is the exact state at tseg - W carried through
+// those W steps, whose maps have norm max(|r_t|, |r_t - lambda_t|) -- r_t
+// unless a step is so large that the map may expand, and then the verify
+// kernel recomputes every segment anyway.  So the error is at most the
+// product of r over the W tokens times the 2-norm of that state, which is
+// at most sqrt(K) <= 2^4 times its largest entry.  W is the shortest
+// multiple of 16 up to kWarm whose product of r lies below the acceptance
+// bound / 2^5 (a margin of 2 for the state's drift over the warm-up).  A
+// start that still misses the bound is recomputed, so W only decides speed.
+template <typename io_t>
+__device__ __forceinline__ int warm_tokens(const Params &p, int seq, int tseg, int lane) {
+    // lane l: the product of r over the four tokens tseg - 4 (l + 1) .. tseg - 4 l - 1
+    const float *rs = p.r + (size_t)seq * p.T + tseg - 4 * (lane + 1);
+    float pr = (rs[0] * rs[1]) * (rs[2] * rs[3]);
+    // inclusive product over lanes 0..l: the product of r over the last 4 (l + 1) tokens
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(kFullMask, pr, off);
+        if (lane >= off) pr *= y;
+    }
+    const float bound = Spec<io_t>::tol * (1.0f / 32.0f);
+    const unsigned ok = __ballot_sync(kFullMask, (lane & 3) == 3 && fabsf(pr) <= bound);
+    return ok ? 4 * (__ffs(ok)) : kWarm;   // first lane 4 m + 3 that passes: W = 16 (m + 1)
+}
+
 // One warp per (segment, sequence): warp id = segment + nseg * sequence.
 template <typename io_t, int K, bool HAS_R, bool LR>
 __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params p) {
@@ -781,7 +808,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) precond_segment_kernel(Params 
     } else {
 #pragma unroll
         for (int e = 0; e < EP; ++e) d[e] = make_float2(0.0f, 0.0f);   // the warm-up forgets this
-        tb = tseg - Spec<io_t>::warm;
+        tb = tseg - (HAS_R ? warm_tokens<io_t>(p, seq, tseg, lane) : Spec<io_t>::warm);
     }
     bool expand = false;
     float lr = 0.0f;   // warm-up tokens (< tseg) add nothing
