@@ -306,8 +306,9 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
  * Bytes of workspace osdn_backward needs for this shape (>= 256): the state
  * of each value row every 16 tokens (4 B*H*ceil(T/16)*V*K), one partial of
  * the row-summed gradients per block of 8 value rows (4 B*H*(V/8)*T*(3K+2)),
- * and 4 B*H*(T*(2K+1) + ceil(T/16)*K) for Phase 1's inputs and checkpoints,
- * each rounded up to 256 bytes.
+ * 4 B*H*(T*(2K+1) + ceil(T/16)*K) for Phase 1's inputs and checkpoints, the
+ * forward scan's segment scratch (as for osdn_precond_scan), and per time
+ * segment of the Phase 1 adjoint 8K + 8 bytes, each rounded up to 256 bytes.
  */
 size_t osdn_backward_workspace_bytes(int B, int H, int T, int K, int V);
 

@@ -302,95 +302,69 @@ partial_sum_kernel(int BH, int T, int nrb, const float *__restrict__ part,
 }
 
 // ---------------------------------------------------------------- kernel 3
+// Phase 1 adjoint over tokens [tlo, thi) of sequence `seq` (both multiples of
+// kBwdSub, or thi = T), walking sub-chunks backwards from lam at thi.  d_t is
+// recomputed forward over each 16-token sub-chunk from the checkpoints ck
+// (d every kBwdSub tokens, written by the forward scan).  With `emit` the
+// token outputs (dk, dbeta, dr) are written and deta accumulated (the same
+// value on every lane); `expand`
+// is set if some token's step map r_t I - mu_t w w^T (mu = eta beta^2 / n)
+// could expand (norm max(|r|, |r - mu |w|^2|) > 1).  One warp.
 template <typename io_t, int K>
-__global__ void __launch_bounds__(kBwdSeqs * 32)
-precond_adjoint_kernel(int BH, int T, int nsub, const io_t *__restrict__ k,
-                       const float *__restrict__ beta, const float *__restrict__ r, float eta,
-                       const float *__restrict__ d0, const float *__restrict__ dkt_tot,
-                       const float *__restrict__ ddT, const float *__restrict__ dk2,
-                       const float *__restrict__ db2, io_t *__restrict__ dk,
-                       float *__restrict__ dbeta, float *__restrict__ dr,
-                       float *__restrict__ dd0, float *__restrict__ deta,
-                       float *__restrict__ ck) {
+__device__ void adjoint_walk(int T, int nsub, size_t seq, int tlo, int thi, bool emit,
+                             const io_t *__restrict__ k, const float *__restrict__ beta,
+                             const float *__restrict__ r, float eta,
+                             const float *__restrict__ dkt_tot, const float *__restrict__ dk2,
+                             const float *__restrict__ db2, const float *__restrict__ ck,
+                             io_t *__restrict__ dk, float *__restrict__ dbeta,
+                             float *__restrict__ dr, float (*dsub)[K], float (&lam)[K / 32],
+                             float &deta_acc, bool &expand) {
     constexpr int NC = K / 32;
-    __shared__ __align__(16) float dsub[kBwdSeqs][kBwdSub][K];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sid = blockIdx.x * kBwdSeqs + warp;
-    if (sid >= BH) return;                     // whole warps only: no block barrier below
-    const size_t seq = sid;
+    const int lane = threadIdx.x & 31;
     const int c0 = lane * NC;
     const size_t tok0 = seq * (size_t)T;
-
-    // forward sweep: d every kBwdSub tokens
     float d[NC];
-    if (d0) {
-        load_cols<NC>(d0 + seq * K + c0, d);
-    } else {
-#pragma unroll
-        for (int m = 0; m < NC; ++m) d[m] = 1.0f;
-    }
-    for (int t = 0; t < T; ++t) {
-        if (t % kBwdSub == 0) store_cols<NC>(ck + (seq * nsub + t / kBwdSub) * K + c0, d);
-        float kc[NC];
-        load_cols<NC>(k + (tok0 + t) * K + c0, kc);
-        float2 na = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int m = 0; m < NC; ++m) {
-            const float w = kc[m] * kc[m];
-            na.x += w;
-            na.y = fmaf(d[m], w, na.y);
-        }
-        na = warp_sum2(na);
-        const float b = beta[tok0 + t];
-        const float c = na.x > 0.0f ? eta * b * (1.0f - b * na.y) / na.x : 0.0f;
-        const float rt = r ? r[tok0 + t] : 1.0f;
-#pragma unroll
-        for (int m = 0; m < NC; ++m) d[m] = fmaf(rt, d[m], c * (kc[m] * kc[m]));
-    }
-
-    // reverse sweep
-    float lam[NC];
-    if (ddT) {
-        load_cols<NC>(ddT + seq * K + c0, lam);
-    } else {
-#pragma unroll
-        for (int m = 0; m < NC; ++m) lam[m] = 0.0f;
-    }
-    float deta_acc = 0.0f;
-    for (int j = nsub - 1; j >= 0; --j) {
+    for (int j = (thi - 1) / kBwdSub; j >= tlo / kBwdSub; --j) {
         const int t0 = j * kBwdSub;
-        const int tn = min(kBwdSub, T - t0);
+        const int tn = min(kBwdSub, thi - t0);
         load_cols<NC>(ck + (seq * nsub + j) * K + c0, d);
         float my_n = 0.0f, my_a = 0.0f;
         for (int tt = 0; tt < tn; ++tt) {
             const size_t g = tok0 + t0 + tt;
-            store_cols<NC>(&dsub[warp][tt][c0], d);
+            store_cols<NC>(&dsub[tt][c0], d);
             float kc[NC];
             load_cols<NC>(k + g * K + c0, kc);
-            float2 na = make_float2(0.0f, 0.0f);
+            float na[3] = {0.0f, 0.0f, 0.0f};   // n, <d, w>, |w|^2
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
                 const float w = kc[m] * kc[m];
-                na.x += w;
-                na.y = fmaf(d[m], w, na.y);
+                na[0] += w;
+                na[1] = fmaf(d[m], w, na[1]);
+                na[2] = fmaf(w, w, na[2]);
             }
-            na = warp_sum2(na);
-            if (lane == tt) { my_n = na.x; my_a = na.y; }
+#pragma unroll
+            for (int x = 16; x > 0; x >>= 1) {
+#pragma unroll
+                for (int e = 0; e < 3; ++e) na[e] += __shfl_xor_sync(kFullMask, na[e], x);
+            }
+            if (lane == tt) { my_n = na[0]; my_a = na[1]; }
             const float b = beta[g];
-            const float c = na.x > 0.0f ? eta * b * (1.0f - b * na.y) / na.x : 0.0f;
+            const float c = na[0] > 0.0f ? eta * b * (1.0f - b * na[1]) / na[0] : 0.0f;
             const float rt = r ? r[g] : 1.0f;
+            const float mu = na[0] > 0.0f ? eta * b * b * na[2] / na[0] : 0.0f;
+            if (fmaxf(fabsf(rt), fabsf(rt - mu)) > 1.0f + 1e-6f) expand = true;
 #pragma unroll
             for (int m = 0; m < NC; ++m) d[m] = fmaf(rt, d[m], c * (kc[m] * kc[m]));
         }
+        __syncwarp();
         for (int tt = tn - 1; tt >= 0; --tt) {
             const size_t g = tok0 + t0 + tt;
             const float n = __shfl_sync(kFullMask, my_n, tt);
             const float a = __shfl_sync(kFullMask, my_a, tt);
-            float dc_[NC], kc[NC], gk[NC], k2[NC];
-            load_cols<NC>(&dsub[warp][tt][c0], dc_);
+            float dc_[NC], kc[NC], gk[NC];
+            load_cols<NC>(&dsub[tt][c0], dc_);
             load_cols<NC>(k + g * K + c0, kc);
             load_cols<NC>(dkt_tot + g * K + c0, gk);
-            load_cols<NC>(dk2 + g * K + c0, k2);
             float2 rc = make_float2(0.0f, 0.0f);       // (<lam, d_t>, <lam, w_t>)
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
@@ -406,47 +380,189 @@ precond_adjoint_kernel(int BH, int T, int nsub, const io_t *__restrict__ k,
                 c = eta * b * res / n;
                 da = -rc.y * eta * b * b / n;
                 db1 = rc.y * eta * (1.0f - 2.0f * b * a) / n;
-                deta_acc += rc.y * b * res / n;
+                if (emit) deta_acc += rc.y * b * res / n;
                 dn = -rc.y * c / n;
             }
-            float out[NC];
+            if (emit) {
+                float k2[NC], out[NC];
+                load_cols<NC>(dk2 + g * K + c0, k2);
 #pragma unroll
-            for (int m = 0; m < NC; ++m) {
-                out[m] = k2[m] + gk[m] * dc_[m] +
-                         2.0f * kc[m] * (c * lam[m] + da * dc_[m] + dn);
-                lam[m] = fmaf(rt, lam[m], fmaf(da, kc[m] * kc[m], gk[m] * kc[m]));
+                for (int m = 0; m < NC; ++m)
+                    out[m] = k2[m] + gk[m] * dc_[m] + 2.0f * kc[m] * (c * lam[m] + da * dc_[m] + dn);
+                store_cols<NC>(dk + g * K + c0, out);
+                if (lane == 0) {
+                    dbeta[g] = db2[g] + db1;
+                    if (dr) dr[g] = rc.x;
+                }
             }
-            store_cols<NC>(dk + g * K + c0, out);
-            if (lane == 0) {
-                dbeta[g] = db2[g] + db1;
-                if (dr) dr[g] = rc.x;
-            }
+#pragma unroll
+            for (int m = 0; m < NC; ++m) lam[m] = fmaf(rt, lam[m], fmaf(da, kc[m] * kc[m], gk[m] * kc[m]));
         }
+        __syncwarp();
     }
-    if (dd0) store_cols<NC>(dd0 + seq * K + c0, lam);
-    if (deta && lane == 0) deta[seq] = deta_acc;
+}
+
+// One warp per (time segment, sequence) of L tokens, walking backwards.  The
+// last segment starts from the exact lam_T = d_dT; every other one starts
+// from lam = 0 kWarmAdj tokens past its end (or from the exact lam_T when the
+// sequence ends sooner), walks that warm-up without output, records the lam
+// it reaches at its end (its speculative start), then walks its own tokens
+// with output and records lam at its first token, its share of deta and
+// whether a map could expand.  With one segment (nseg = 1) the results are
+// final: dd0 and deta are written here.
+constexpr int kWarmAdj = 128;
+template <typename io_t, int K>
+__global__ void __launch_bounds__(kBwdSeqs * 32)
+precond_adjoint_kernel(int BH, int T, int nsub, int L, int nseg, const io_t *__restrict__ k,
+                       const float *__restrict__ beta, const float *__restrict__ r, float eta,
+                       const float *__restrict__ dkt_tot, const float *__restrict__ ddT,
+                       const float *__restrict__ dk2, const float *__restrict__ db2,
+                       const float *__restrict__ ck, io_t *__restrict__ dk,
+                       float *__restrict__ dbeta, float *__restrict__ dr,
+                       float *__restrict__ dd0, float *__restrict__ deta,
+                       float *__restrict__ ws_start, float *__restrict__ ws_end,
+                       int *__restrict__ ws_flag, float *__restrict__ ws_eta) {
+    constexpr int NC = K / 32;
+    __shared__ __align__(16) float dsub[kBwdSeqs][kBwdSub][K];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t id = (size_t)blockIdx.x * kBwdSeqs + warp;
+    if (id >= (size_t)BH * nseg) return;        // whole warps only: no block barrier below
+    const size_t seq = id / nseg;
+    const int seg = (int)(id % nseg), c0 = lane * NC;
+    const int tlo = seg * L, thi = min(T, tlo + L);
+    float lam[NC];
+    const int tend = seg == nseg - 1 ? T : min(T, thi + kWarmAdj);
+    if (ddT && tend == T) {
+        load_cols<NC>(ddT + seq * K + c0, lam);
+    } else {
+#pragma unroll
+        for (int m = 0; m < NC; ++m) lam[m] = 0.0f;   // the warm-up forgets this
+    }
+    float deta_acc = 0.0f;
+    bool expand = false;
+    if (tend > thi)
+        adjoint_walk<io_t, K>(T, nsub, seq, thi, tend, false, k, beta, r, eta, dkt_tot, dk2, db2,
+                              ck, dk, dbeta, dr, dsub[warp], lam, deta_acc, expand);
+    if (nseg > 1) store_cols<NC>(ws_start + id * K + c0, lam);
+    adjoint_walk<io_t, K>(T, nsub, seq, tlo, thi, true, k, beta, r, eta, dkt_tot, dk2, db2, ck,
+                          dk, dbeta, dr, dsub[warp], lam, deta_acc, expand);
+    expand = __any_sync(kFullMask, expand);   // (deta_acc is the same on every lane)
+    if (nseg > 1) {
+        store_cols<NC>(ws_end + id * K + c0, lam);
+        if (lane == 0) {
+            ws_flag[id] = expand ? 1 : 0;
+            ws_eta[id] = deta_acc;
+        }
+    } else {
+        if (dd0) store_cols<NC>(dd0 + seq * K + c0, lam);
+        if (deta && lane == 0) deta[seq] = deta_acc;
+    }
+}
+
+// One warp per sequence: check each segment's speculative start (lam at its
+// end) against the lam its successor reached at its first token, walking
+// down from the last segment (whose start is exact), and recompute from that
+// exact value every segment whose start is off by more than the acceptance
+// bound relative to the largest entry (2^-21 fp32 I/O, 2^-13 bf16 I/O, as in
+// the forward scan), or every segment when some map could expand.  Then
+// dd0 = lam at token 0 and deta = the segments' shares in segment order.
+template <typename io_t, int K>
+__global__ void __launch_bounds__(32)
+precond_adjoint_verify_kernel(int BH, int T, int nsub, int L, int nseg, const io_t *__restrict__ k,
+                              const float *__restrict__ beta, const float *__restrict__ r,
+                              float eta, const float *__restrict__ dkt_tot,
+                              const float *__restrict__ dk2, const float *__restrict__ db2,
+                              const float *__restrict__ ck, io_t *__restrict__ dk,
+                              float *__restrict__ dbeta, float *__restrict__ dr,
+                              float *__restrict__ dd0, float *__restrict__ deta,
+                              const float *__restrict__ ws_start, float *__restrict__ ws_end,
+                              const int *__restrict__ ws_flag, float *__restrict__ ws_eta) {
+    constexpr int NC = K / 32;
+    constexpr float tol = sizeof(io_t) == 2 ? 1.220703125e-04f : 4.76837158203125e-07f;
+    __shared__ __align__(16) float dsub[kBwdSub][K];
+    const size_t seq = blockIdx.x;
+    const int lane = threadIdx.x, c0 = lane * NC;
+    const size_t base = seq * nseg;
+    int f = 0;
+    for (int i = lane; i < nseg; i += 32) f |= ws_flag[base + i];
+    const bool all = __any_sync(kFullMask, f != 0);
+    float prev[NC];   // the exact lam at the first token of segment i + 1
+    load_cols<NC>(ws_end + (base + nseg - 1) * K + c0, prev);
+    for (int i = nseg - 2; i >= 0; --i) {
+        float cur[NC];
+        load_cols<NC>(ws_start + (base + i) * K + c0, cur);
+        float diff = 0.0f, mag = 0.0f;
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+            diff = fmaxf(diff, fabsf(cur[m] - prev[m]));
+            mag = fmaxf(mag, fabsf(prev[m]));
+        }
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) {
+            diff = fmaxf(diff, __shfl_xor_sync(kFullMask, diff, x));
+            mag = fmaxf(mag, __shfl_xor_sync(kFullMask, mag, x));
+        }
+        if (all || !(diff <= tol * mag)) {   // recompute segment i from the exact start
+            const int tlo = i * L, thi = min(T, tlo + L);
+            float deta_acc = 0.0f;
+            bool unused = false;
+            adjoint_walk<io_t, K>(T, nsub, seq, tlo, thi, true, k, beta, r, eta, dkt_tot, dk2,
+                                  db2, ck, dk, dbeta, dr, dsub, prev, deta_acc, unused);
+            store_cols<NC>(ws_end + (base + i) * K + c0, prev);
+            if (lane == 0) ws_eta[base + i] = deta_acc;
+        } else {
+            load_cols<NC>(ws_end + (base + i) * K + c0, prev);
+        }
+        __syncwarp();
+    }
+    if (dd0) store_cols<NC>(dd0 + seq * K + c0, prev);
+    if (deta) {
+        __syncwarp();
+        float e = 0.0f;
+        for (int i = lane; i < nseg; i += 32) e += ws_eta[base + i];
+        e = warp_sum(e);
+        if (lane == 0) deta[seq] = e;
+    }
 }
 
 // ---------------------------------------------------------------- host side
 static size_t pad256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int precond_segments(int BH, int T, bool has_r, int *L_out);
+size_t precond_scratch_bytes(int BH, int T, int K);
+cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *k,
+                                      const float *beta, const float *r, float eta,
+                                      const float *d0, float *dT, float *ecoef, float *dchk,
+                                      int chk_shift, void *scratch, int *status,
+                                      cudaStream_t stream);
+
+// Scratch: Phase 2's state checkpoints (ck2) and row-block partials, the
+// summed dktilde, Phase 2's shares of dk and dbeta, Phase 1's checkpoints of
+// d every kBwdSub tokens (ck1) and the forward scan's segment scratch (p1),
+// and the adjoint's time segments: lam at each segment's end (speculative
+// start) and first token, flags and deta shares (the segments of the forward
+// scan's rule, with a retention gate; sized for it in any case).
 struct BwdScratch {
-    float *ck2, *part, *dkt_tot, *dk2, *db2, *ck1;
+    float *ck2, *part, *dkt_tot, *dk2, *db2, *ck1, *p1, *a_start, *a_end, *a_flag, *a_eta;
 };
 
 static size_t bwd_layout(int BH, int T, int K, int V, bool pch, char *base, BwdScratch *s) {
     const size_t nsub = ((size_t)T + kBwdSub - 1) / kBwdSub;
-    const size_t sz[6] = {
+    const size_t n = (size_t)BH * precond_segments(BH, T, true, nullptr);
+    const size_t sz[11] = {
         pad256((size_t)BH * nsub * V * K * 4),                                   // ck2
         pad256((size_t)BH * (V / kBwdRows) * T * bwd_part_width(K, pch) * 4),    // part
         pad256((size_t)BH * T * K * 4),                                           // dkt_tot
         pad256((size_t)BH * T * K * 4),                                           // dk2
         pad256((size_t)BH * T * 4),                                               // db2
         pad256((size_t)BH * nsub * K * 4),                                        // ck1
+        pad256(precond_scratch_bytes(BH, T, K)),                                  // p1
+        pad256(n * K * 4), pad256(n * K * 4), pad256(n * 4), pad256(n * 4),       // a_*
     };
     size_t off = 0;
-    float **dst[6] = {&s->ck2, &s->part, &s->dkt_tot, &s->dk2, &s->db2, &s->ck1};
-    for (int a = 0; a < 6; ++a) {
+    float **dst[11] = {&s->ck2, &s->part, &s->dkt_tot, &s->dk2, &s->db2, &s->ck1, &s->p1,
+                       &s->a_start, &s->a_end, &s->a_flag, &s->a_eta};
+    for (int a = 0; a < 11; ++a) {
         if (base) *dst[a] = reinterpret_cast<float *>(base + off);
         off += sz[a];
     }
@@ -466,15 +582,20 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
                                    const float *dST, const float *ddT, const void *dkt_ext,
                                    void *dq, void *dk, void *dv, float *dbeta, float *dr,
                                    float *dalpha, float *dd0, float *dS0, float *deta,
-                                   void *scratch, cudaStream_t stream) {
+                                   void *scratch, int *status, cudaStream_t stream) {
     static std::atomic<unsigned long long> attr_done{0};
     BwdScratch s;
     bwd_layout(BH, T, K, V, PCH, static_cast<char *>(scratch), &s);
+    // Phase 1's d every kBwdSub tokens, by the (time-parallel) forward scan
+    cudaError_t e = precond_checkpoint_launch(sizeof(io_t) == 2 ? OSDN_BF16 : OSDN_F32, BH, T, K, k,
+                                              beta, r, eta, d0, nullptr, nullptr, s.ck1, 4, s.p1,
+                                              status, stream);
+    if (e != cudaSuccess) return e;
     const int nsub = T / kBwdSub + (T % kBwdSub != 0);   // no overflow near INT_MAX
     const int nrb = V / kBwdRows;
     const int smem = (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4;
     auto *k1 = state_adjoint_kernel<io_t, K, PCH>;
-    cudaError_t e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
+    e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
     if (e != cudaSuccess) return e;
     k1<<<seq_grid(nrb, BH), kBwdRows * 32, smem, stream>>>(
         BH, T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
@@ -485,9 +606,21 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
         BH, T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
         s.dkt_tot, s.dk2, s.db2);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    precond_adjoint_kernel<io_t, K><<<(BH + kBwdSeqs - 1) / kBwdSeqs, kBwdSeqs * 32, 0, stream>>>(
-        BH, T, nsub, static_cast<const io_t *>(k), beta, r, eta, d0, s.dkt_tot, ddT, s.dk2,
-        s.db2, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.ck1);
+    // the Phase 1 adjoint in time segments (one per sequence without a
+    // retention gate), then their verification
+    int L = T;
+    const int nseg = precond_segments(BH, T, r != nullptr, &L);
+    const long long nw = (long long)BH * nseg;
+    int *aflag = reinterpret_cast<int *>(s.a_flag);
+    precond_adjoint_kernel<io_t, K><<<(unsigned)((nw + kBwdSeqs - 1) / kBwdSeqs), kBwdSeqs * 32, 0,
+                                      stream>>>(
+        BH, T, nsub, L, nseg, static_cast<const io_t *>(k), beta, r, eta, s.dkt_tot, ddT, s.dk2,
+        s.db2, s.ck1, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.a_start, s.a_end, aflag,
+        s.a_eta);
+    if ((e = cudaGetLastError()) != cudaSuccess || nseg == 1) return e;
+    precond_adjoint_verify_kernel<io_t, K><<<BH, 32, 0, stream>>>(
+        BH, T, nsub, L, nseg, static_cast<const io_t *>(k), beta, r, eta, s.dkt_tot, s.dk2, s.db2,
+        s.ck1, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.a_start, s.a_end, aflag, s.a_eta);
     return cudaGetLastError();
 }
 
@@ -497,11 +630,11 @@ cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, 
                             const void *dO, const float *dST, const float *ddT,
                             const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
                             float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
-                            bool per_channel, void *scratch, cudaStream_t stream) {
+                            bool per_channel, void *scratch, int *status, cudaStream_t stream) {
 #define OSDN_BWD(T_, K_, P_)                                                                  \
     return launch_backward<T_, K_, P_>(BH, T, V, q, k, kt, v, beta, r, eta, d0, alpha, S0,   \
                                        dO, dST, ddT, dkt_ext, dq, dk, dv, dbeta, dr, dalpha, \
-                                       dd0, dS0, deta, scratch, stream)
+                                       dd0, dS0, deta, scratch, status, stream)
 #define OSDN_BWD_K(T_, P_)          \
     do {                            \
         if (K == 64) OSDN_BWD(T_, 64, P_); \

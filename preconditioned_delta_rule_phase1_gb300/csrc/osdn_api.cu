@@ -15,7 +15,8 @@ size_t precond_scratch_bytes(int BH, int T, int K);
 cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *k,
                                       const float *beta, const float *r, float eta,
                                       const float *d0, float *dT, float *ecoef, float *dchk,
-                                      void *scratch, int *status, cudaStream_t stream);
+                                      int chk_shift, void *scratch, int *status,
+                                      cudaStream_t stream);
 cudaError_t delta_tc_fused_launch(int BH, int T, int K, int V, const void *q, const void *k,
                                   const void *v, const float *beta, const float *r,
                                   const float *ecoef, const float *dchk, const float *alpha,
@@ -51,7 +52,7 @@ cudaError_t backward_launch(int io, int BH, int T, int K, int V, const void *q, 
                             const void *dO, const float *dST, const float *ddT,
                             const void *dkt_ext, void *dq, void *dk, void *dv, float *dbeta,
                             float *dr, float *dalpha, float *dd0, float *dS0, float *deta,
-                            bool per_channel, void *scratch, cudaStream_t stream);
+                            bool per_channel, void *scratch, int *status, cudaStream_t stream);
 cudaError_t delta_simt_kda_launch(int io, int BH, int T, int K, int V, const void *q,
                                   const void *k, const void *kt, const void *v,
                                   const float *beta, const float *alpha_k, const float *S0,
@@ -399,7 +400,7 @@ int osdn_forward(int io, int B, int H, int T, int K, int V, const void *q, const
     const FwdCarve c = fwd_carve(static_cast<char *>(workspace) + kStatusBytes, io, (int)BH, T, K, V);
     if (io == OSDN_BF16) {
         e = osdn::precond_checkpoint_launch(io, (int)BH, T, K, k, beta, r, eta, d0, dT, c.ecoef,
-                                            c.dchk, c.p1, status, st);
+                                            c.dchk, 6, c.p1, status, st);
         if (e == cudaSuccess)
             e = osdn::delta_tc_fused_launch((int)BH, T, K, V, q, k, v, beta, r, c.ecoef, c.dchk,
                                             alpha, S0, o, ST, c.p2, status, st);
@@ -535,7 +536,8 @@ int backward_checked(int io, int B, int H, int T, int K, int V, const void *q, c
         e = osdn::backward_launch(io, (int)BH, T, K, V, q, k, ktilde, v, beta, r, eta, d0, alpha,
                                   S0, d_o, d_ST, d_dT, d_ktilde, dq, dk, dv, dbeta, dr, dalpha,
                                   dd0, dS0, deta, per_channel,
-                                  static_cast<char *>(workspace) + kStatusBytes, st);
+                                  static_cast<char *>(workspace) + kStatusBytes,
+                                  static_cast<int *>(workspace), st);
     }
     return e == cudaSuccess ? OSDN_OK : OSDN_ERR_CUDA;
 }

@@ -104,7 +104,8 @@ struct Params {
     void *ktilde;               // or NULL (checkpoint mode without ktilde)
     float *dT;
     float *ecoef;               // [BH][T] e_t, or NULL
-    float *dchk;                // [BH][ceil(T/64)][K] d at tokens 0, 64, 128, ..., or NULL
+    float *dchk;                // [BH][ceil(T/I)][K] d at tokens 0, I, 2 I, ..., or NULL
+    int chk_shift;              // log2 of the checkpoint interval I (6: 64 tokens; 4: 16)
     float *ws_start, *ws_end;   // [BH][nseg][K]
     int *ws_flag;               // [BH][nseg]
     float *ws_lr;               // [BH][nseg] residual log-ratio of each segment
@@ -348,7 +349,8 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
     const float *bseq = p.beta + (size_t)seq * p.T;
     const float *rseq = HAS_R ? p.r + (size_t)seq * p.T : nullptr;
     const int nc = (te - tb + C - 1) / C;
-    const size_t nchk = (size_t)(p.T + 63) / 64;   // checkpoints per sequence
+    const int cs = p.chk_shift;
+    const size_t nchk = ((size_t)p.T + (1u << cs) - 1) >> cs;   // checkpoints per sequence
 
     auto issue = [&](int j) {
         if (j < nc) {
@@ -445,8 +447,8 @@ __device__ void warp_scan(const Params &p, WarpSmem<io_t, K> &st, int seq, int t
             st.sER[t] = make_float4(et, et, rt, rt);
             if (p.ecoef && t < nv && t0 >= tseg) p.ecoef[(size_t)seq * p.T + t0 + t] = et;
         }
-        if (p.dchk && (t0 & 63) == 0 && t0 >= tseg)   // d entering a 64-token chunk
-            st_pairs<EP>(p.dchk + ((size_t)seq * nchk + (t0 >> 6)) * K + E * lane, d);
+        if (p.dchk && (t0 & ((1 << cs) - 1)) == 0 && t0 >= tseg)   // d entering a checkpoint interval
+            st_pairs<EP>(p.dchk + ((size_t)seq * nchk + (t0 >> cs)) * K + E * lane, d);
         __syncwarp();
 
         // ---- chain: this lane's columns through the chunk; emit ktilde ----------
@@ -639,7 +641,8 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
         // ================================================= chain warp
         const int w = warp, col = 32 * w + lane;
         io_t *ktseq = p.ktilde ? static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K : nullptr;
-        const size_t nchk = (size_t)(T + 63) / 64;   // checkpoints per sequence
+        const int chs = p.chk_shift;
+        const size_t nchk = ((size_t)T + (1u << chs) - 1) >> chs;   // checkpoints per sequence
         // this warp's 32 columns of a chunk's 16 keys, staged by cp.async:
         // 4-byte pieces, lane l copying piece l of every row (bf16: 16 lanes
         // cover the 64-byte row, fp32: 32 lanes the 128-byte row)
@@ -711,8 +714,8 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
             const float et = t < nv ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
             if (lane < C) sm.be[w][1][t] = et;
             if (p.ecoef && w == 0 && lane < C && t < nv) p.ecoef[(size_t)seq * T + t0 + t] = et;
-            if (p.dchk && (t0 & 63) == 0)   // d entering a 64-token chunk
-                p.dchk[((size_t)seq * nchk + (t0 >> 6)) * K + col] = d;
+            if (p.dchk && (t0 & ((1 << chs) - 1)) == 0)   // d entering a checkpoint interval
+                p.dchk[((size_t)seq * nchk + (t0 >> chs)) * K + col] = d;
             __syncwarp();
             if (LR) {   // the residual factor y_t = 1 - b_t rho_t p_t - sum_u Ny_tu e_u
                 float y4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1022,7 +1025,7 @@ size_t precond_scratch_bytes(int BH, int T, int K) {
 static cudaError_t scan_launch(int io, int BH, int T, int K, const void *k, const float *beta,
                                const float *r, float eta, const float *d0, void *ktilde,
                                float *dT, float *logratio, float *ecoef, float *dchk,
-                               void *scratch, int *status, cudaStream_t stream) {
+                               int chk_shift, void *scratch, int *status, cudaStream_t stream) {
     if (T == 0) {   // d_T = d_0; an empty product of residual ratios is 1
         if (logratio) {
             p1::copy_or_fill_kernel<<<(unsigned)((BH + 255) / 256), 256, 0, stream>>>(
@@ -1048,6 +1051,7 @@ static cudaError_t scan_launch(int io, int BH, int T, int K, const void *k, cons
     p.dT = dT;
     p.ecoef = ecoef;
     p.dchk = dchk;
+    p.chk_shift = chk_shift;
     p.logratio = logratio;
     p.status = status;
     float *f = static_cast<float *>(scratch);
@@ -1068,17 +1072,19 @@ cudaError_t precond_scan_launch(int io, int BH, int T, int K, const void *k, con
                                 float *dT, float *logratio, void *scratch, int *status,
                                 cudaStream_t stream) {
     return scan_launch(io, BH, T, K, k, beta, r, eta, d0, ktilde, dT, logratio, nullptr, nullptr,
-                       scratch, status, stream);
+                       6, scratch, status, stream);
 }
 
-// Checkpoint mode: e_t of every token ([BH][T]) and d entering every 64-token
-// chunk ([BH][ceil(T/64)][K]) instead of ktilde; d_T as usual.
+// Checkpoint mode: e_t of every token ([BH][T]) and d entering every
+// interval of 2^chk_shift tokens ([BH][ceil(T / 2^chk_shift)][K]) instead of
+// ktilde (either may be NULL); d_T as usual.
 cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *k,
                                       const float *beta, const float *r, float eta,
                                       const float *d0, float *dT, float *ecoef, float *dchk,
-                                      void *scratch, int *status, cudaStream_t stream) {
+                                      int chk_shift, void *scratch, int *status,
+                                      cudaStream_t stream) {
     return scan_launch(io, BH, T, K, k, beta, r, eta, d0, nullptr, dT, nullptr, ecoef, dchk,
-                       scratch, status, stream);
+                       chk_shift, scratch, status, stream);
 }
 
 // ---------------------------------------------------------------------------

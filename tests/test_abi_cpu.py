@@ -281,14 +281,21 @@ def test_host_validation_backward(L):
 def test_backward_workspace_size(L):
     # the state of each value row every 16 tokens, one partial of the row sums
     # (3K + 2 values a token) per block of 8 rows, Phase 1's inputs and
-    # checkpoints; each array padded to 256 bytes
+    # checkpoints, the forward scan's segment scratch (as osdn_precond_scan's),
+    # and per time segment of the adjoint two K-vectors and two words; each
+    # array padded to 256 bytes
+    import bench
     r = lambda x: -(-x // 256) * 256
     assert L.osdn_backward_workspace_bytes(1, 2, 0, 64, 64) == 256
-    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (2, 16, 8192, 128, 128)]:
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (2, 16, 8192, 128, 128),
+                          (1, 4, 3000, 64, 64)]:
         BH, ns = B * H, -(-T // 16)
+        n = BH * bench.precond_segments(BH, T, True, 152)
+        p1 = L.osdn_precond_scan_workspace_bytes(B, H, T, K) - 256
         want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (3 * K + 2) * 4)
-                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
-        assert L.osdn_backward_workspace_bytes(B, H, T, K, V) == want
+                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4) + r(p1)
+                + 2 * r(n * K * 4) + 2 * r(n * 4))
+        assert L.osdn_backward_workspace_bytes(B, H, T, K, V) == want, (B, H, T, K, V)
 
 
 def kda(L, io=1, B=1, H=1, T=8, K=64, V=64, q=FAKE, k=2 * FAKE, kt=3 * FAKE, v=4 * FAKE,
@@ -356,11 +363,16 @@ def test_host_validation_backward_kda(L):
 
 
 def test_backward_kda_workspace_size(L):
+    # as osdn_backward's, with the row-block partials carrying 4K + 1 values
+    import bench
     r = lambda x: -(-x // 256) * 256
-    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64)]:
+    for B, H, T, K, V in [(1, 1, 1, 64, 64), (2, 3, 100, 128, 64), (1, 4, 3000, 64, 64)]:
         BH, ns = B * H, -(-T // 16)
+        n = BH * bench.precond_segments(BH, T, True, 152)
+        p1 = L.osdn_precond_scan_workspace_bytes(B, H, T, K) - 256
         want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (4 * K + 1) * 4)
-                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4))
+                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4) + r(p1)
+                + 2 * r(n * K * 4) + 2 * r(n * 4))
         assert L.osdn_backward_kda_workspace_bytes(B, H, T, K, V) == want
 
 

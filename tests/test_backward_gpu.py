@@ -12,8 +12,9 @@ of ``oracle.backward``), so that the comparison is about the backward alone.
 alone moves the eta gradient of an 8192-token head by about 1.6e-2: its sum
 over tokens cancels heavily.)  Cases cover both I/O types, every (K, V) pair,
 one and several 16-token sub-chunks with ragged tails, T = 1 and T = 0,
-optional inputs and cotangents left out, a zero key, and determinism; and
-the full shape the benchmark times, with its last head checked.
+optional inputs and cotangents left out, a zero key, the time segments of
+the Phase 1 adjoint (accepted, repaired, all recomputed), and determinism;
+and the full shape the benchmark times, with its last head checked.
 """
 import numpy as np
 import pytest
@@ -123,6 +124,23 @@ def test_longer_sequence():
     x = synth.make_random(1, 2, 700, 128, 128, io="bf16", apf=True, gated=True, s0=True,
                           seed=81)
     check(x, cotangents(1, 2, 700, 128, 128, "bf16", 82), "bf16")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["accepted", "slow_retention", "expansive_token"])
+def test_phase1_adjoint_time_segments(io, case):
+    # with a retention gate the Phase 1 adjoint runs in time segments of 256
+    # tokens, each started from lam = 0 128 tokens past its end and verified
+    # against its successor's exact start: accepted as is, every start
+    # repaired (a retention of 0.99995 forgets nothing in 128 tokens), or
+    # every segment recomputed (one step map with norm above 1)
+    x = synth.make_random(1, 2, 1500, 64, 64, io=io, apf=True, gated=True, s0=True, d0=True,
+                          seed=101)
+    if case == "slow_retention":
+        x["r"] = torch.full_like(x["r"], 0.99995)
+    if case == "expansive_token":
+        x["r"][:, :, 900] = 1.5
+    check(x, cotangents(1, 2, 1500, 64, 64, io, 102), io)
 
 
 def test_deterministic():
