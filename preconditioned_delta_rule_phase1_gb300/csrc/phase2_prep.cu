@@ -75,12 +75,6 @@ constexpr float kMinDecay = 0.015625f, kMaxDecay = 64.0f;   // per-channel decay
 __device__ __forceinline__ int sw_off(int rows, int r, int c) {
     return (c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
 }
-__device__ __forceinline__ float ld_bf(const uint8_t *tile, int off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
-}
-__device__ __forceinline__ void st_bf(uint8_t *tile, int off, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(v);
-}
 
 struct PrepParams {
     int BH, T, nch, c0;   // sequences, sequence length, its chunks, first chunk of this launch
@@ -228,7 +222,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // per-channel decay: log Gam at the four reference points (0 for block 0)
     // and at the chunk's end, and the per-group partial sums of log alpha
     __shared__ float sLref[PCH ? 4 : 1][PCH ? K : 1], sLamC[PCH ? K : 1];
-    __shared__ float sGrp[PCH ? 256 / K : 1][PCH ? K : 1];
+    __shared__ float sGrp[PCH ? 512 / K : 1][PCH ? K : 1];
     __shared__ uint32_t tmem_base_sh;
     __shared__ float sBeta[C], sLg[C], sD[C];
     // fused: e_t, r_t, and sPre[b][t] = prod_{16 b <= v < t} r_v (1 for t <= 16 b):
@@ -462,88 +456,118 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
         bool fok = true;
         if (PCH) {
-            // ---- log Gam per channel: thread (f, grp) sums log alpha over its tokens
-            constexpr int QT = kPrepThreads / K, TPT = C / QT;
-            const int f = pt % K, grp = pt / K;
-            float lam[TPT];
+            // ---- log Gam per channel: thread (column pair fp, token group grp)
+            // sums log alpha over its tokens for columns 2 fp and 2 fp + 1
+            constexpr int CP = K / 2, QT = kPrepThreads / CP, TPT = C / QT;
+            const int fp = pt % CP, grp = pt / CP, f0 = 2 * fp;
+            float lam[TPT][2];
             {
-                float run = 0.0f;
+                float run0 = 0.0f, run1 = 0.0f;
                 bool bad = false;
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
                     const int t = grp * TPT + i;
-                    float a = t < nvalid ? p.alpha_k[((size_t)seq * T + t0 + t) * K + f] : 1.0f;
-                    if (!(a >= kMinDecay && a <= kMaxDecay)) {   // NaN fails too
-                        bad = true;
-                        a = 1.0f;
-                    }
-                    run += logf(a);
-                    lam[i] = run;
+                    float2 a = make_float2(1.0f, 1.0f);
+                    if (t < nvalid)
+                        a = *reinterpret_cast<const float2 *>(p.alpha_k + ((size_t)seq * T + t0 + t) * K + f0);
+                    if (!(a.x >= kMinDecay && a.x <= kMaxDecay)) { bad = true; a.x = 1.0f; }   // NaN fails too
+                    if (!(a.y >= kMinDecay && a.y <= kMaxDecay)) { bad = true; a.y = 1.0f; }
+                    run0 += __logf(a.x);
+                    run1 += __logf(a.y);
+                    lam[i][0] = run0;
+                    lam[i][1] = run1;
                 }
                 if (bad) report_status(p.status, OSDN_ERR_DEVICE);
-                sGrp[grp][f] = run;
+                sGrp[grp][f0] = run0;
+                sGrp[grp][f0 + 1] = run1;
             }
             ptx::named_bar(1, kPrepThreads);
             {
-                float off = 0.0f;
-                for (int g2 = 0; g2 < grp; ++g2) off += sGrp[g2][f];
+                float off0 = 0.0f, off1 = 0.0f;
+                for (int g2 = 0; g2 < grp; ++g2) {
+                    off0 += sGrp[g2][f0];
+                    off1 += sGrp[g2][f0 + 1];
+                }
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    lam[i] += off;
+                    lam[i][0] += off0;
+                    lam[i][1] += off1;
                     const int t = grp * TPT + i;
-                    if ((t & 15) == 15 && t < C - 1) sLref[(t >> 4) + 1][f] = lam[i];
+                    if ((t & 15) == 15 && t < C - 1) {
+                        sLref[(t >> 4) + 1][f0] = lam[i][0];
+                        sLref[(t >> 4) + 1][f0 + 1] = lam[i][1];
+                    }
                     if (t == C - 1) {   // tokens past T add nothing: this is the chunk's Gam_C
-                        sLamC[f] = lam[i];
-                        p.gc[((size_t)seq * nch + j) * K + f] = expf(lam[i]);
+                        sLamC[f0] = lam[i][0];
+                        sLamC[f0 + 1] = lam[i][1];
+                        *reinterpret_cast<float2 *>(p.gc + ((size_t)seq * nch + j) * K + f0) =
+                            make_float2(expf(lam[i][0]), expf(lam[i][1]));
                     }
                 }
-                if (grp == 0) sLref[0][f] = 0.0f;
+                if (grp == 0) {
+                    sLref[0][f0] = 0.0f;
+                    sLref[0][f0 + 1] = 0.0f;
+                }
             }
             ptx::named_bar(1, kPrepThreads);
-            // ---- once the tiles have landed: [K;Q] rows relative to their block's
-            // reference, then the reference copies of Kt, two at a time
-            fok = vote_all(wait_poll(&bar_full, 0, &s_abort, st), 1, kPrepThreads);
-            uint8_t *bufs[2] = {smem + LY::oL, sXb};
-            auto copy_kt = [&](int b) {
-                uint8_t *buf = bufs[b & 1];
-                const float ref = sLref[b][f];
-#pragma unroll
-                for (int i = 0; i < TPT; ++i) {
-                    const int s_ = grp * TPT + i, off = sw_off(C, s_, f);
-                    const float v = s_ < 16 * (b + 1) ? ld_bf(sKt, off) * expf(ref - lam[i]) : 0.0f;
-                    st_bf(buf, off, v);
-                }
+            // bf16 pairs in the swizzled tiles (columns f0, f0 + 1 share a 4-byte word)
+            auto ld2 = [](const uint8_t *tile, int off) {
+                return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(tile + off));
             };
+            auto st2 = [](uint8_t *tile, int off, float x, float y) {
+                *reinterpret_cast<__nv_bfloat162 *>(tile + off) = __floats2bfloat162_rn(x, y);
+            };
+            uint8_t *bufs[2] = {smem + LY::oL, sXb};
+            // the reference copy b of Kt's pair at token s (0 past block b)
+            auto copy_val = [&](int b, int s_, int i, float2 raw) {
+                if (s_ >= 16 * (b + 1)) return make_float2(0.0f, 0.0f);
+                return make_float2(raw.x * __expf(sLref[b][f0] - lam[i][0]),
+                                   raw.y * __expf(sLref[b][f0 + 1] - lam[i][1]));
+            };
+            // ---- once the tiles have landed: [K;Q] rows relative to their block's
+            // reference, and the first two reference copies of Kt
+            fok = vote_all(wait_poll(&bar_full, 0, &s_abort, st), 1, kPrepThreads);
             if (fok) {
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int t = grp * TPT + i;
-                    const float fac = expf(lam[i] - sLref[t >> 4][f]);
-                    const int ok_ = sw_off(128, t, f), oq = sw_off(128, C + t, f);
-                    st_bf(sKQ, ok_, ld_bf(sKQ, ok_) * fac);
-                    st_bf(sKQ, oq, ld_bf(sKQ, oq) * fac);
+                    const int t = grp * TPT + i, b = t >> 4;
+                    const float fx = __expf(lam[i][0] - sLref[b][f0]);
+                    const float fy = __expf(lam[i][1] - sLref[b][f0 + 1]);
+                    const int ok_ = sw_off(128, t, f0), oq = sw_off(128, C + t, f0), ot = sw_off(C, t, f0);
+                    const float2 kv = ld2(sKQ, ok_), qv = ld2(sKQ, oq), raw = ld2(sKt, ot);
+                    st2(sKQ, ok_, kv.x * fx, kv.y * fy);
+                    st2(sKQ, oq, qv.x * fx, qv.y * fy);
+                    const float2 c0v = copy_val(0, t, i, raw), c1v = copy_val(1, t, i, raw);
+                    st2(bufs[0], ot, c0v.x, c0v.y);
+                    st2(bufs[1], ot, c1v.x, c1v.y);
                 }
-                copy_kt(0);
-                copy_kt(1);
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
                 if (pt == 0) ptx::mbar_arrive(&bar_c01);
             }
             fok = fok && vote_all(wait_poll(&bar_r0, 0, &s_abort, st), 1, kPrepThreads);
             if (fok) {   // reference 0's product has read its buffer
-                copy_kt(2);
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int t = grp * TPT + i, ot = sw_off(C, t, f0);
+                    const float2 v = copy_val(2, t, i, ld2(sKt, ot));
+                    st2(bufs[0], ot, v.x, v.y);
+                }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
                 if (pt == 0) ptx::mbar_arrive(&bar_c2);
             }
             fok = fok && vote_all(wait_poll(&bar_r1, 0, &s_abort, st), 1, kPrepThreads);
             if (fok) {
-                copy_kt(3);
-                // Kt itself to (Gam_C / Gam_s) . kt for W and M (no product reads it raw)
+                // copy 3, and Kt itself to (Gam_C / Gam_s) . kt for W and M
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int off = sw_off(C, grp * TPT + i, f);
-                    st_bf(sKt, off, ld_bf(sKt, off) * expf(sLamC[f] - lam[i]));
+                    const int t = grp * TPT + i, ot = sw_off(C, t, f0);
+                    const float2 raw = ld2(sKt, ot);
+                    const float2 v = copy_val(3, t, i, raw);
+                    st2(bufs[1], ot, v.x, v.y);
+                    st2(sKt, ot, raw.x * __expf(sLamC[f0] - lam[i][0]),
+                        raw.y * __expf(sLamC[f0 + 1] - lam[i][1]));
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
@@ -680,12 +704,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
             }
             if (PCH) {  // K rows to Gam . K for Kw (the Gram products have read them)
-                constexpr int QT = kPrepThreads / K, TPT = C / QT;
-                const int f = pt % K, grp = pt / K;
+                constexpr int CP = K / 2, QT = kPrepThreads / CP, TPT = C / QT;
+                const int f0 = 2 * (pt % CP), grp = pt / CP;
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int t = grp * TPT + i, off = sw_off(128, t, f);
-                    st_bf(sKQ, off, ld_bf(sKQ, off) * expf(sLref[t >> 4][f]));
+                    const int t = grp * TPT + i, off = sw_off(128, t, f0);
+                    __nv_bfloat162 *w2 = reinterpret_cast<__nv_bfloat162 *>(sKQ + off);
+                    const float2 kv = __bfloat1622float2(*w2);
+                    *w2 = __floats2bfloat162_rn(kv.x * __expf(sLref[t >> 4][f0]),
+                                                kv.y * __expf(sLref[t >> 4][f0 + 1]));
                 }
             }
             ptx::tc_fence_before();
@@ -775,7 +802,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         // PCH: Q rows hold (Gam_t / Gam_m) . q_t; Gam_m restores Gam . q
-                        const float ge = PCH ? expf(sLref[mrow >> 4][half * NH + c + e]) : gt;
+                        const float ge = PCH ? __expf(sLref[mrow >> 4][half * NH + c + e]) : gt;
                         qv[e] = fmaf(ge, qv[e], -d[c + e]);
                     }
                     st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
