@@ -529,7 +529,8 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, volatil
     return false;
 }
 
-template <typename io_t, int K, bool HAS_R, bool LR>
+// CHK: checkpoint mode (e_t and d every 2^chk_shift tokens; ktilde may be NULL).
+template <typename io_t, int K, bool HAS_R, bool LR, bool CHK>
 __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(Params p) {
     using SM = CtaSmem<io_t, K>;
     constexpr int NW = K / 32;
@@ -640,7 +641,7 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
     } else {
         // ================================================= chain warp
         const int w = warp, col = 32 * w + lane;
-        io_t *ktseq = p.ktilde ? static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K : nullptr;
+        io_t *ktseq = (!CHK || p.ktilde) ? static_cast<io_t *>(p.ktilde) + (size_t)seq * T * K : nullptr;
         const int chs = p.chk_shift;
         const size_t nchk = ((size_t)T + (1u << chs) - 1) >> chs;   // checkpoints per sequence
         // this warp's 32 columns of a chunk's 16 keys, staged by cp.async:
@@ -713,8 +714,8 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
             }
             const float et = t < nv ? (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]) : 0.0f;
             if (lane < C) sm.be[w][1][t] = et;
-            if (p.ecoef && w == 0 && lane < C && t < nv) p.ecoef[(size_t)seq * T + t0 + t] = et;
-            if (p.dchk && (t0 & ((1 << chs) - 1)) == 0)   // d entering a checkpoint interval
+            if (CHK && p.ecoef && w == 0 && lane < C && t < nv) p.ecoef[(size_t)seq * T + t0 + t] = et;
+            if (CHK && p.dchk && (t0 & ((1 << chs) - 1)) == 0)   // d entering a checkpoint interval
                 p.dchk[((size_t)seq * nchk + (t0 >> chs)) * K + col] = d;
             __syncwarp();
             if (LR) {   // the residual factor y_t = 1 - b_t rho_t p_t - sum_u Ny_tu e_u
@@ -732,7 +733,8 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
                 if (w == 0 && lane < C && t < nv) lr += logf(y * y);
             }
             // this column through the chunk
-            io_t *kst = ktseq ? ktseq + (size_t)t0 * K + col : nullptr;
+            io_t *kst = (!CHK || ktseq) ? ktseq + (size_t)t0 * K + col : nullptr;
+            const int nst = (!CHK || ktseq) ? nv : 0;   // tokens of this chunk to emit
 #pragma unroll
             for (int u4 = 0; u4 < C; u4 += 4) {
                 const float4 e4 = *reinterpret_cast<const float4 *>(&sm.be[w][1][u4]);
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(32 * (K / 32 + kSolvers)) precond_cta_kernel(P
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int u = u4 + e;
-                    if (kst && u < nv) from_f32(kst[(size_t)u * K], d * kk[u]);
+                    if (u < nst) from_f32(kst[(size_t)u * K], d * kk[u]);
                     d = fmaf(ev[e], ww[u], HAS_R ? rv[e] * d : d);
                 }
             }
@@ -951,14 +953,24 @@ static int sm_count() {
 template <typename io_t, int K, bool HAS_R, bool LR>
 static cudaError_t launch_t(const Params &p, cudaStream_t stream) {
     constexpr int kStage = (int)sizeof(WarpSmem<io_t, K>);
-    static std::atomic<unsigned long long> attr_seg{0}, attr_ver{0}, attr_cta{0};
+    static std::atomic<unsigned long long> attr_seg{0}, attr_ver{0}, attr_cta{0}, attr_chk{0};
     if (p.nseg == 1 && p.BH <= 2 * sm_count()) {
         // one segment a sequence and few sequences: a CTA per sequence
         constexpr int kCta = (int)sizeof(CtaSmem<io_t, K>);
-        cudaError_t e = smem_attr_once((const void *)precond_cta_kernel<io_t, K, HAS_R, LR>, kCta,
-                                       attr_cta);
+        if constexpr (!LR) {
+            if (p.ecoef || p.dchk) {   // checkpoint mode (never with the residual sums)
+                cudaError_t e = smem_attr_once(
+                    (const void *)precond_cta_kernel<io_t, K, HAS_R, false, true>, kCta, attr_chk);
+                if (e != cudaSuccess) return e;
+                precond_cta_kernel<io_t, K, HAS_R, false, true>
+                    <<<p.BH, 32 * (K / 32 + kSolvers), kCta, stream>>>(p);
+                return cudaGetLastError();
+            }
+        }
+        cudaError_t e = smem_attr_once((const void *)precond_cta_kernel<io_t, K, HAS_R, LR, false>,
+                                       kCta, attr_cta);
         if (e != cudaSuccess) return e;
-        precond_cta_kernel<io_t, K, HAS_R, LR><<<p.BH, 32 * (K / 32 + kSolvers), kCta, stream>>>(p);
+        precond_cta_kernel<io_t, K, HAS_R, LR, false><<<p.BH, 32 * (K / 32 + kSolvers), kCta, stream>>>(p);
         return cudaGetLastError();
     }
     cudaError_t e0 = smem_attr_once((const void *)precond_segment_kernel<io_t, K, HAS_R, LR>,
