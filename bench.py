@@ -151,6 +151,16 @@ def launches_per_step(w, x, per_channel=False, sms=None):
     return p1 + 2 * nslab
 
 
+def backward_launches(w, x, sms=None):
+    """Kernels one osdn_backward call enqueues: the forward scan in checkpoint
+    mode (segments + verify with a retention gate and several segments, else
+    one launch), the state adjoint and the partial sums, and the Phase 1
+    adjoint (its time segments, plus their verify kernel when there are
+    several)."""
+    nseg = precond_segments(w.B * w.H, w.T, x["r"] is not None, sms)
+    return (2 if nseg > 1 else 1) + 2 + (2 if nseg > 1 else 1)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -729,7 +739,7 @@ def run_backward(args, local_rank):
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "algorithmic_bytes": nbytes,
                      "peak_source": peak_src, "traffic": None},
-        "clocks": clk, "gpu_launches": 3 * args.steps}), flush=True)
+        "clocks": clk, "gpu_launches": backward_launches(w, x) * args.steps}), flush=True)
 
 
 def run_fused(args, local_rank):

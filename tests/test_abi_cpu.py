@@ -81,6 +81,11 @@ def test_bench_launch_count_rule():
     # launch and a chain in two time segments (speculative pass + 1 repair)
     w = synth.WORKLOADS["lm1p3b_apf_bf16"]
     assert bench.launches_per_step(w, {"r": 1, "alpha": None}, per_channel=True, sms=152) == 5
+    # the backward at that shape: checkpoint scan (2), state adjoint, partial
+    # sums, Phase 1 adjoint segments and their verify kernel (the launch list
+    # shows 6 a step); without a retention gate 4
+    assert bench.backward_launches(w, {"r": 1}, sms=152) == 6
+    assert bench.backward_launches(w, {"r": None}, sms=152) == 4
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails validation first
