@@ -654,12 +654,16 @@ def run_decode(args, local_rank):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
+    clocks = ClockSampler(gpu_smi_id(dev, local_rank))
+    clocks.start()
+    time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     assert ws.status(stream) == 0
     ms = e0.elapsed_time(e1) / args.steps
     BH = B * H
@@ -676,7 +680,7 @@ def run_decode(args, local_rank):
         "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "algorithmic_bytes": nbytes, "peak_source": peak_src},
-        "gpu_launches": args.steps}), flush=True)
+        "clocks": clk, "gpu_launches": args.steps}), flush=True)
 
 
 def backward_bytes(w, x):
