@@ -38,6 +38,12 @@
  *  - stream is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls are asynchronous: they validate on the host, enqueue
  *    their kernels and return.
+ *  - The compute calls may be captured into a CUDA graph on `stream`
+ *    (stream capture), after one call of the same kind and shape outside
+ *    the capture has set the kernels' attributes and created the library's
+ *    streams; the bf16 Phase 2's library streams then join the capture.  The
+ *    workspace and every buffer must outlive the graph, and the status word
+ *    is read (osdn_check_status) only outside the capture.
  *  - Return value: OSDN_OK, or a negative osdn_status.  Every argument check
  *    happens before anything is enqueued, so a non-zero return means nothing
  *    ran.  OSDN_ERR_CUDA means a launch was rejected by the CUDA runtime.
