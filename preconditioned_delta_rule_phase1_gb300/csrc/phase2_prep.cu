@@ -222,6 +222,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // per-channel decay: log Gam at the four reference points (0 for block 0)
     // and at the chunk's end, and the per-group partial sums of log alpha
     __shared__ float sLref[PCH ? 4 : 1][PCH ? K : 1], sLamC[PCH ? K : 1];
+    __shared__ float sGref[PCH ? 4 : 1][PCH ? K : 1];   // exp(sLref): Gam at the references
     __shared__ float sGrp[PCH ? 512 / K : 1][PCH ? K : 1];
     __shared__ uint32_t tmem_base_sh;
     __shared__ float sBeta[C], sLg[C], sD[C];
@@ -518,28 +519,41 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 *reinterpret_cast<__nv_bfloat162 *>(tile + off) = __floats2bfloat162_rn(x, y);
             };
             uint8_t *bufs[2] = {smem + LY::oL, sXb};
-            // the reference copy b of Kt's pair at token s (0 past block b)
-            auto copy_val = [&](int b, int s_, int i, float2 raw) {
-                if (s_ >= 16 * (b + 1)) return make_float2(0.0f, 0.0f);
-                return make_float2(raw.x * __expf(sLref[b][f0] - lam[i][0]),
-                                   raw.y * __expf(sLref[b][f0 + 1] - lam[i][1]));
-            };
+            // This thread's tokens lie in one 16-token block bs (m = 16 bs - 1 its
+            // reference, e = 16 bs + 15 its last token).  With E_s = Gam_e / Gam_s
+            // (<= 1; one exp a token), every factor is E_s times a per-column
+            // constant: the row factor Gam_s / Gam_m = (Gam_e / Gam_m) / E_s, the
+            // copy b >= bs factor Gam_m(b) / Gam_s = (Gam_m(b) / Gam_e) E_s, and
+            // Gam_C / Gam_s = (Gam_C / Gam_e) E_s.
+            const int bs = (grp * TPT) / 16;
+            const float le0 = bs < 3 ? sLref[bs + 1][f0] : sLamC[f0];
+            const float le1 = bs < 3 ? sLref[bs + 1][f0 + 1] : sLamC[f0 + 1];
+            const float2 cblk = make_float2(__expf(le0 - sLref[bs][f0]), __expf(le1 - sLref[bs][f0 + 1]));
+            const float2 cdk = make_float2(__expf(sLamC[f0] - le0), __expf(sLamC[f0 + 1] - le1));
+            float2 cb[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                cb[b] = b >= bs ? make_float2(__expf(sLref[b][f0] - le0), __expf(sLref[b][f0 + 1] - le1))
+                                : make_float2(0.0f, 0.0f);
+            for (int x = pt; x < 4 * K; x += kPrepThreads) sGref[x / K][x % K] = __expf(sLref[x / K][x % K]);
+            float2 E[TPT];
+#pragma unroll
+            for (int i = 0; i < TPT; ++i) E[i] = make_float2(__expf(le0 - lam[i][0]), __expf(le1 - lam[i][1]));
             // ---- once the tiles have landed: [K;Q] rows relative to their block's
             // reference, and the first two reference copies of Kt
             fok = vote_all(wait_poll(&bar_full, 0, &s_abort, st), 1, kPrepThreads);
             if (fok) {
+                const float2 c0v = cb[0], c1v = cb[1];
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int t = grp * TPT + i, b = t >> 4;
-                    const float fx = __expf(lam[i][0] - sLref[b][f0]);
-                    const float fy = __expf(lam[i][1] - sLref[b][f0 + 1]);
+                    const int t = grp * TPT + i;
+                    const float fx = __fdividef(cblk.x, E[i].x), fy = __fdividef(cblk.y, E[i].y);
                     const int ok_ = sw_off(128, t, f0), oq = sw_off(128, C + t, f0), ot = sw_off(C, t, f0);
                     const float2 kv = ld2(sKQ, ok_), qv = ld2(sKQ, oq), raw = ld2(sKt, ot);
                     st2(sKQ, ok_, kv.x * fx, kv.y * fy);
                     st2(sKQ, oq, qv.x * fx, qv.y * fy);
-                    const float2 c0v = copy_val(0, t, i, raw), c1v = copy_val(1, t, i, raw);
-                    st2(bufs[0], ot, c0v.x, c0v.y);
-                    st2(bufs[1], ot, c1v.x, c1v.y);
+                    st2(bufs[0], ot, raw.x * c0v.x * E[i].x, raw.y * c0v.y * E[i].y);
+                    st2(bufs[1], ot, raw.x * c1v.x * E[i].x, raw.y * c1v.y * E[i].y);
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
@@ -549,9 +563,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (fok) {   // reference 0's product has read its buffer
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int t = grp * TPT + i, ot = sw_off(C, t, f0);
-                    const float2 v = copy_val(2, t, i, ld2(sKt, ot));
-                    st2(bufs[0], ot, v.x, v.y);
+                    const int ot = sw_off(C, grp * TPT + i, f0);
+                    const float2 raw = ld2(sKt, ot);
+                    st2(bufs[0], ot, raw.x * cb[2].x * E[i].x, raw.y * cb[2].y * E[i].y);
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
@@ -562,12 +576,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 // copy 3, and Kt itself to (Gam_C / Gam_s) . kt for W and M
 #pragma unroll
                 for (int i = 0; i < TPT; ++i) {
-                    const int t = grp * TPT + i, ot = sw_off(C, t, f0);
+                    const int ot = sw_off(C, grp * TPT + i, f0);
                     const float2 raw = ld2(sKt, ot);
-                    const float2 v = copy_val(3, t, i, raw);
-                    st2(bufs[1], ot, v.x, v.y);
-                    st2(sKt, ot, raw.x * __expf(sLamC[f0] - lam[i][0]),
-                        raw.y * __expf(sLamC[f0 + 1] - lam[i][1]));
+                    st2(bufs[1], ot, raw.x * cb[3].x * E[i].x, raw.y * cb[3].y * E[i].y);
+                    st2(sKt, ot, raw.x * cdk.x * E[i].x, raw.y * cdk.y * E[i].y);
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, kPrepThreads);
@@ -711,8 +723,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     const int t = grp * TPT + i, off = sw_off(128, t, f0);
                     __nv_bfloat162 *w2 = reinterpret_cast<__nv_bfloat162 *>(sKQ + off);
                     const float2 kv = __bfloat1622float2(*w2);
-                    *w2 = __floats2bfloat162_rn(kv.x * __expf(sLref[t >> 4][f0]),
-                                                kv.y * __expf(sLref[t >> 4][f0 + 1]));
+                    *w2 = __floats2bfloat162_rn(kv.x * sGref[t >> 4][f0], kv.y * sGref[t >> 4][f0 + 1]);
                 }
             }
             ptx::tc_fence_before();
@@ -802,7 +813,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         // PCH: Q rows hold (Gam_t / Gam_m) . q_t; Gam_m restores Gam . q
-                        const float ge = PCH ? __expf(sLref[mrow >> 4][half * NH + c + e]) : gt;
+                        const float ge = PCH ? sGref[mrow >> 4][half * NH + c + e] : gt;
                         qv[e] = fmaf(ge, qv[e], -d[c + e]);
                     }
                     st_row_sw128(sKQ, 128, C + mrow, half * NH + c, qv, 16);
