@@ -23,6 +23,7 @@ CPU oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -188,14 +189,22 @@ def gpu_smi_id(dev, fallback):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock and the throttle reasons, one row
+    every PERIOD_MS, each stamped with the host time of its query.  start()
+    returns once the first row is in; only the rows stamped between begin()
+    and end() (the timed region) are summarised.  A region shorter than one
+    sampling period may hold no row; the rows within 0.1 s of it are used
+    then, and `window` says which."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 10
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -204,10 +213,22 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            return
+        deadline = time.time() + 3.0
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -218,22 +239,44 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows)}
+        return summarize_clock_rows(lines, self.t0, self.t1)
+
+
+def summarize_clock_rows(lines, t0, t1):
+    """Median SM clock, the largest max clock and the throttle reasons seen
+    in the ClockSampler rows stamped within [t0, t1] (host seconds); the rows
+    within 0.1 s of it when none is inside.  None without a usable row."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            continue
+        rows.append((ts, parts))
+    lo = t0 if t0 is not None else float("-inf")
+    hi = t1 if t1 is not None else float("inf")
+    window = "timed region"
+    sel = [r for ts, r in rows if lo <= ts <= hi]
+    if not sel:
+        window = "within 0.1 s of the timed region"
+        sel = [r for ts, r in rows if lo - 0.1 <= ts <= hi + 0.1]
+    if not sel:
+        return None
+    num = lambda v: float(v) if v.replace(".", "").isdigit() else None
+    sm = [x for x in (num(r[2]) for r in sel) if x is not None]
+    smax = [x for x in (num(r[3]) for r in sel) if x is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for r in sel for n, v in zip(names, r[6:10]) if v == "Active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+            "samples": len(sel), "window": window,
+            "timed_s": (t1 - t0) if t0 is not None and t1 is not None else None}
 
 
 # ---------------------------------------------------------------------------
@@ -437,7 +480,7 @@ def run_ours(args, w, x, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    time.sleep(0.3)  # let the sampler attach before the timed region
+    clocks.begin()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.zero_()
@@ -448,6 +491,7 @@ def run_ours(args, w, x, rank, world, local_rank):
                           stream)
             ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -656,13 +700,14 @@ def run_decode(args, local_rank):
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(gpu_smi_id(dev, local_rank))
     clocks.start()
-    time.sleep(0.3)
+    clocks.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     clk = clocks.stop()
     assert ws.status(stream) == 0
     ms = e0.elapsed_time(e1) / args.steps
@@ -720,12 +765,14 @@ def run_backward(args, local_rank):
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(gpu_smi_id(dev, local_rank))
     clocks.start()
+    clocks.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     clk = clocks.stop()
     assert ws.status(stream) == 0
     ms = e0.elapsed_time(e1) / args.steps
@@ -773,15 +820,16 @@ def run_fused(args, local_rank):
         step()
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(gpu_smi_id(dev, local_rank))
-    clocks.start()
-    time.sleep(0.3)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks.start()
+    clocks.begin()
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     clk = clocks.stop()
     st = ws.status(stream)
     if st != 0:
@@ -825,12 +873,14 @@ def run_kda(args, local_rank):
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(gpu_smi_id(dev, local_rank))
     clocks.start()
+    clocks.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     clk = clocks.stop()
     assert ws.status(stream) == 0
     ms = e0.elapsed_time(e1) / args.steps
