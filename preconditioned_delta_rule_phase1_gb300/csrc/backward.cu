@@ -121,6 +121,49 @@ __device__ __forceinline__ float decayed_pred(const float (&S)[NC], const float 
 }
 
 // ---------------------------------------------------------------- kernel 1
+// The CTA's 8 rows all read the same keys, ktilde and queries, so each
+// 16-token sub-chunk is staged once in shared memory by cp.async, one
+// sub-chunk ahead: keys, ktilde, the CTA's rows of v and dO, beta and a scalar
+// decay in two slots, the queries (read by the reverse walk only) in one,
+// fetched while the sub-chunk is recomputed.  The arithmetic is the same as
+// with the loads from global memory; only where the operands come from moves.
+__device__ __forceinline__ void bwd_cp16(void *dst, const void *src, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void bwd_cp4(void *dst, const void *src, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void bwd_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bwd_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Byte layout of the staging area (after the recomputed states and the
+// reduction buffer): slots [2] of the per-token operands, one query tile.
+template <typename io_t, int K>
+struct BwdStage {
+    static constexpr int ROW = K * (int)sizeof(io_t);                       // one token's key row
+    static constexpr int VROW = kBwdRows * (int)sizeof(io_t);               // one token's v (or dO) of the rows
+    static constexpr int SK = 0;                                            // [2][kBwdSub][K]
+    static constexpr int SKT = SK + 2 * kBwdSub * ROW;                      // [2][kBwdSub][K]
+    static constexpr int SQ = SKT + 2 * kBwdSub * ROW;                      // [kBwdSub][K]
+    static constexpr int SV = SQ + kBwdSub * ROW;                           // [2][kBwdSub][kBwdRows]
+    static constexpr int SDO = SV + 2 * kBwdSub * VROW;                     // [2][kBwdSub][kBwdRows]
+    static constexpr int SB = SDO + 2 * kBwdSub * VROW;                     // [2][kBwdSub] beta
+    static constexpr int SA = SB + 2 * kBwdSub * 4;                         // [2][kBwdSub] scalar decay
+    static constexpr int BYTES = SA + 2 * kBwdSub * 4;
+    static_assert(VROW % 16 == 0, "a token's rows of v must be whole 16-byte pieces");
+};
+
+template <typename io_t, int K, bool PCH>
+constexpr int state_adjoint_smem_bytes() {
+    return (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4 +
+           BwdStage<io_t, K>::BYTES;
+}
+
 template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(kBwdRows * 32)
 state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
@@ -133,18 +176,77 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     constexpr int NC = K / 32;
     constexpr int P = bwd_part_width(K, PCH);
     constexpr int PS = bwd_red_stride(K, PCH);
+    using SG = BwdStage<io_t, K>;
+    constexpr int EPP = 16 / (int)sizeof(io_t);   // elements per 16-byte piece
+    constexpr int PR = K / EPP;                   // pieces per key row
+    constexpr int VP = SG::VROW / 16;             // pieces per token of the rows' v
+    constexpr int NT = kBwdRows * 32;
     extern __shared__ __align__(16) float smem[];
     float *Sp = smem;                                  // [kBwdRows][kBwdSub][K]
     float *red = smem + kBwdRows * kBwdSub * K;        // [2][kBwdRows][PS]
+    uint8_t *stg = reinterpret_cast<uint8_t *>(red + 2 * kBwdRows * PS);
+    auto sk = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SK) + (s * kBwdSub + tt) * K; };
+    auto skt = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SKT) + (s * kBwdSub + tt) * K; };
+    auto sq = [&](int tt) { return reinterpret_cast<io_t *>(stg + SG::SQ) + tt * K; };
+    auto sv = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SV) + (s * kBwdSub + tt) * kBwdRows; };
+    auto sdo = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SDO) + (s * kBwdSub + tt) * kBwdRows; };
+    auto sb = [&](int s) { return reinterpret_cast<float *>(stg + SG::SB) + s * kBwdSub; };
+    auto sa = [&](int s) { return reinterpret_cast<float *>(stg + SG::SA) + s * kBwdSub; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x, nrb = gridDim.x;
-    const int i = rb * kBwdRows + warp;               // this warp's value row
+    const int i0 = rb * kBwdRows, i = i0 + warp;      // the CTA's first row; this warp's row
     const size_t seq = grid_seq();
     if (seq >= (size_t)BH) return;
     const int c0 = lane * NC;
     const size_t tok0 = seq * (size_t)T;               // first token of the sequence
     float *Spw = Sp + warp * kBwdSub * K;
+
+    // sub-chunk j's keys, ktilde, rows of v (and dO with `rev`), beta and a
+    // scalar decay into slot s; tokens past T are zero-filled
+    auto stage = [&](int s, int j, bool rev) {
+        const int t0 = j * kBwdSub;
+        for (int x = threadIdx.x; x < kBwdSub * PR; x += NT) {
+            const int tt = x / PR, pc = x % PR;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(sk(s, tt) + pc * EPP, k + g * K + pc * EPP, ok);
+            bwd_cp16(skt(s, tt) + pc * EPP, kt + g * K + pc * EPP, ok);
+        }
+        for (int x = threadIdx.x; x < kBwdSub * VP; x += NT) {
+            const int tt = x / VP, pc = x % VP;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(sv(s, tt) + pc * EPP, v + g * V + i0 + pc * EPP, ok);
+            if (rev && dO) bwd_cp16(sdo(s, tt) + pc * EPP, dO + g * V + i0 + pc * EPP, ok);
+        }
+        if (threadIdx.x < kBwdSub) {
+            const int tt = threadIdx.x;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp4(sb(s) + tt, beta + g, ok);
+            if (!PCH && alpha) bwd_cp4(sa(s) + tt, alpha + g, ok);
+        }
+    };
+    auto stage_q = [&](int j) {
+        const int t0 = j * kBwdSub;
+        for (int x = threadIdx.x; x < kBwdSub * PR; x += NT) {
+            const int tt = x / PR, pc = x % PR;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(sq(tt) + pc * EPP, q + g * K + pc * EPP, ok);
+        }
+    };
+    // the decay of token tt of the sub-chunk in slot s for this lane's columns
+    auto decay = [&](int s, int tt, size_t g, float (&a)[NC]) {
+        if constexpr (PCH) {
+            decay_cols<true, NC>(alpha, g, K, c0, a);
+        } else {
+            const float x = alpha ? sa(s)[tt] : 1.0f;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) a[m] = x;
+        }
+    };
 
     // forward sweep: the row's state every kBwdSub tokens
     float S[NC];
@@ -154,17 +256,25 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
 #pragma unroll
         for (int m = 0; m < NC; ++m) S[m] = 0.0f;
     }
-    for (int t = 0; t < T; ++t) {
-        if (t % kBwdSub == 0)
-            store_cols<NC>(ck + ((seq * nsub + t / kBwdSub) * V + i) * (size_t)K + c0, S);
-        float kc[NC], tc[NC], a[NC];
-        load_cols<NC>(k + (tok0 + t) * K + c0, kc);
-        load_cols<NC>(kt + (tok0 + t) * K + c0, tc);
-        decay_cols<PCH, NC>(alpha, tok0 + t, K, c0, a);
-        const float u = beta[tok0 + t] * (to_f32(v[(tok0 + t) * V + i]) -
-                                          decayed_pred<PCH, NC>(S, a, kc));
+    if (nsub > 0) stage(0, 0, false);
+    bwd_commit();
+    for (int j = 0; j < nsub; ++j) {
+        __syncthreads();   // every warp is done with the other slot
+        if (j + 1 < nsub) stage((j + 1) & 1, j + 1, false);
+        bwd_commit();
+        bwd_wait<1>();
+        __syncthreads();   // sub-chunk j is in
+        const int s = j & 1, t0 = j * kBwdSub, tn = min(kBwdSub, T - t0);
+        store_cols<NC>(ck + ((seq * nsub + j) * V + i) * (size_t)K + c0, S);
+        for (int tt = 0; tt < tn; ++tt) {
+            float kc[NC], tc[NC], a[NC];
+            load_cols<NC>(sk(s, tt) + c0, kc);
+            load_cols<NC>(skt(s, tt) + c0, tc);
+            decay(s, tt, tok0 + t0 + tt, a);
+            const float u = sb(s)[tt] * (to_f32(sv(s, tt)[warp]) - decayed_pred<PCH, NC>(S, a, kc));
 #pragma unroll
-        for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
+            for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
+        }
     }
 
     // reverse sweep
@@ -175,8 +285,19 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
 #pragma unroll
         for (int m = 0; m < NC; ++m) G[m] = 0.0f;
     }
+    __syncthreads();   // the forward sweep is done with both slots
+    int slot = 0;
+    if (nsub > 0) stage(slot, nsub - 1, true);
+    bwd_commit();
     int buf = 0;
     for (int j = nsub - 1; j >= 0; --j) {
+        __syncthreads();   // every warp is done with the other slot and the queries
+        if (j >= 1) stage(slot ^ 1, j - 1, true);
+        bwd_commit();
+        bwd_wait<1>();
+        __syncthreads();   // sub-chunk j is in
+        stage_q(j);        // for the walk, while the sub-chunk is recomputed
+        bwd_commit();
         const int t0 = j * kBwdSub;
         const int tn = min(kBwdSub, T - t0);
         // recompute the sub-chunk: S_{t-1} of each token into shared memory,
@@ -187,15 +308,17 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             const size_t g = tok0 + t0 + tt;
             store_cols<NC>(Spw + tt * K + c0, S);
             float kc[NC], tc[NC], a[NC];
-            load_cols<NC>(k + g * K + c0, kc);
-            load_cols<NC>(kt + g * K + c0, tc);
-            decay_cols<PCH, NC>(alpha, g, K, c0, a);
-            const float e = to_f32(v[g * V + i]) - decayed_pred<PCH, NC>(S, a, kc);
-            const float u = beta[g] * e;
+            load_cols<NC>(sk(slot, tt) + c0, kc);
+            load_cols<NC>(skt(slot, tt) + c0, tc);
+            decay(slot, tt, g, a);
+            const float e = to_f32(sv(slot, tt)[warp]) - decayed_pred<PCH, NC>(S, a, kc);
+            const float u = sb(slot)[tt] * e;
             if (lane == tt) { my_e = e; my_u = u; }
 #pragma unroll
             for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
         }
+        bwd_wait<0>();
+        __syncthreads();   // the queries are in
         // walk it backwards (each lane reads back only its own columns of Spw)
         for (int tt = tn - 1; tt >= 0; --tt) {
             const size_t g = tok0 + t0 + tt;
@@ -203,12 +326,12 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             const float u = __shfl_sync(kFullMask, my_u, tt);
             float sp[NC], qc[NC], kc[NC], tc[NC], a[NC];
             load_cols<NC>(Spw + tt * K + c0, sp);
-            load_cols<NC>(q + g * K + c0, qc);
-            load_cols<NC>(k + g * K + c0, kc);
-            load_cols<NC>(kt + g * K + c0, tc);
-            decay_cols<PCH, NC>(alpha, g, K, c0, a);
-            const float b = beta[g];
-            const float dOi = dO ? to_f32(dO[g * V + i]) : 0.0f;
+            load_cols<NC>(sq(tt) + c0, qc);
+            load_cols<NC>(sk(slot, tt) + c0, kc);
+            load_cols<NC>(skt(slot, tt) + c0, tc);
+            decay(slot, tt, g, a);
+            const float b = sb(slot)[tt];
+            const float dOi = dO ? to_f32(sdo(slot, tt)[warp]) : 0.0f;
             float du = 0.0f;
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
@@ -263,7 +386,9 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             }
             buf ^= 1;
         }
+        slot ^= 1;
     }
+    bwd_wait<0>();
     if (dS0) store_cols<NC>(dS0 + (seq * V + i) * (size_t)K + c0, G);
 }
 
@@ -593,7 +718,7 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
     if (e != cudaSuccess) return e;
     const int nsub = T / kBwdSub + (T % kBwdSub != 0);   // no overflow near INT_MAX
     const int nrb = V / kBwdRows;
-    const int smem = (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4;
+    const int smem = state_adjoint_smem_bytes<io_t, K, PCH>();
     auto *k1 = state_adjoint_kernel<io_t, K, PCH>;
     e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
     if (e != cudaSuccess) return e;
