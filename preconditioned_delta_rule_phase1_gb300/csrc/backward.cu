@@ -436,29 +436,78 @@ partial_sum_kernel(int BH, int T, int nrb, const float *__restrict__ part,
 // is set if some token's step map r_t I - mu_t w w^T (mu = eta beta^2 / n)
 // could expand (norm max(|r|, |r - mu |w|^2|) > 1).  One warp.
 template <typename io_t, int K>
+struct WalkStage {   // one warp's staging area (about 28 KB: two CTAs of 4 warps per SM)
+    alignas(16) float dsub[kBwdSub][K];    // d_t of the sub-chunk, recomputed
+    alignas(16) io_t sk[kBwdSub][K];       // keys
+    alignas(16) float sg[kBwdSub][K];      // the total ktilde cotangent
+    alignas(16) float s2[kBwdSub][K];      // Phase 2's share of dk
+    alignas(16) float sb[kBwdSub];         // beta
+    alignas(16) float sr[kBwdSub];         // r
+    alignas(16) float sdb[kBwdSub];        // Phase 2's share of dbeta
+};
+
+template <typename io_t, int K>
 __device__ void adjoint_walk(int T, int nsub, size_t seq, int tlo, int thi, bool emit,
                              const io_t *__restrict__ k, const float *__restrict__ beta,
                              const float *__restrict__ r, float eta,
                              const float *__restrict__ dkt_tot, const float *__restrict__ dk2,
                              const float *__restrict__ db2, const float *__restrict__ ck,
                              io_t *__restrict__ dk, float *__restrict__ dbeta,
-                             float *__restrict__ dr, float (*dsub)[K], float (&lam)[K / 32],
+                             float *__restrict__ dr, WalkStage<io_t, K> &ws, float (&lam)[K / 32],
                              float &deta_acc, bool &expand) {
     constexpr int NC = K / 32;
+    constexpr int EPP = 16 / (int)sizeof(io_t);   // key elements per 16-byte piece
+    constexpr int PR = K / EPP;                   // pieces per key row
+    constexpr int PF = K / 4;                     // pieces per fp32 row
     const int lane = threadIdx.x & 31;
     const int c0 = lane * NC;
     const size_t tok0 = seq * (size_t)T;
+    // sub-chunk j's keys, beta and r (tokens past T zero-filled)
+    auto stage_keys = [&](int j) {
+        const int t0 = j * kBwdSub;
+        for (int x = lane; x < kBwdSub * PR; x += 32) {
+            const int tt = x / PR, pc = x % PR;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(&ws.sk[tt][pc * EPP], k + g * K + pc * EPP, ok);
+        }
+        const int tt = lane & (kBwdSub - 1);
+        const bool ok = t0 + tt < T && (lane < kBwdSub || r);
+        const size_t g = tok0 + (ok ? t0 + tt : 0);
+        if (lane < kBwdSub) bwd_cp4(&ws.sb[tt], beta + g, ok);
+        else if (r) bwd_cp4(&ws.sr[tt], r + g, ok);
+    };
+    // sub-chunk j's cotangents (and, when emitting, Phase 2's shares)
+    auto stage_grads = [&](int j) {
+        const int t0 = j * kBwdSub;
+        for (int x = lane; x < kBwdSub * PF; x += 32) {
+            const int tt = x / PF, pc = x % PF;
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(&ws.sg[tt][4 * pc], dkt_tot + g * K + 4 * pc, ok);
+            if (emit) bwd_cp16(&ws.s2[tt][4 * pc], dk2 + g * K + 4 * pc, ok);
+        }
+        if (emit && lane < kBwdSub) {
+            const bool ok = t0 + lane < T;
+            bwd_cp4(&ws.sdb[lane], db2 + tok0 + (ok ? t0 + lane : 0), ok);
+        }
+    };
     float d[NC];
     for (int j = (thi - 1) / kBwdSub; j >= tlo / kBwdSub; --j) {
         const int t0 = j * kBwdSub;
         const int tn = min(kBwdSub, thi - t0);
+        stage_keys(j);
+        bwd_commit();
+        stage_grads(j);    // for the walk, while the sub-chunk is recomputed
+        bwd_commit();
+        bwd_wait<1>();     // the keys of sub-chunk j are in
+        __syncwarp();
         load_cols<NC>(ck + (seq * nsub + j) * K + c0, d);
         float my_n = 0.0f, my_a = 0.0f;
         for (int tt = 0; tt < tn; ++tt) {
-            const size_t g = tok0 + t0 + tt;
-            store_cols<NC>(&dsub[tt][c0], d);
+            store_cols<NC>(&ws.dsub[tt][c0], d);
             float kc[NC];
-            load_cols<NC>(k + g * K + c0, kc);
+            load_cols<NC>(&ws.sk[tt][c0], kc);
             float na[3] = {0.0f, 0.0f, 0.0f};   // n, <d, w>, |w|^2
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
@@ -473,23 +522,24 @@ __device__ void adjoint_walk(int T, int nsub, size_t seq, int tlo, int thi, bool
                 for (int e = 0; e < 3; ++e) na[e] += __shfl_xor_sync(kFullMask, na[e], x);
             }
             if (lane == tt) { my_n = na[0]; my_a = na[1]; }
-            const float b = beta[g];
+            const float b = ws.sb[tt];
             const float c = na[0] > 0.0f ? eta * b * (1.0f - b * na[1]) / na[0] : 0.0f;
-            const float rt = r ? r[g] : 1.0f;
+            const float rt = r ? ws.sr[tt] : 1.0f;
             const float mu = na[0] > 0.0f ? eta * b * b * na[2] / na[0] : 0.0f;
             if (fmaxf(fabsf(rt), fabsf(rt - mu)) > 1.0f + 1e-6f) expand = true;
 #pragma unroll
             for (int m = 0; m < NC; ++m) d[m] = fmaf(rt, d[m], c * (kc[m] * kc[m]));
         }
+        bwd_wait<0>();     // this sub-chunk's cotangents are in
         __syncwarp();
         for (int tt = tn - 1; tt >= 0; --tt) {
             const size_t g = tok0 + t0 + tt;
             const float n = __shfl_sync(kFullMask, my_n, tt);
             const float a = __shfl_sync(kFullMask, my_a, tt);
             float dc_[NC], kc[NC], gk[NC];
-            load_cols<NC>(&dsub[tt][c0], dc_);
-            load_cols<NC>(k + g * K + c0, kc);
-            load_cols<NC>(dkt_tot + g * K + c0, gk);
+            load_cols<NC>(&ws.dsub[tt][c0], dc_);
+            load_cols<NC>(&ws.sk[tt][c0], kc);
+            load_cols<NC>(&ws.sg[tt][c0], gk);
             float2 rc = make_float2(0.0f, 0.0f);       // (<lam, d_t>, <lam, w_t>)
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
@@ -497,8 +547,8 @@ __device__ void adjoint_walk(int T, int nsub, size_t seq, int tlo, int thi, bool
                 rc.y = fmaf(lam[m], kc[m] * kc[m], rc.y);
             }
             rc = warp_sum2(rc);
-            const float b = beta[g];
-            const float rt = r ? r[g] : 1.0f;
+            const float b = ws.sb[tt];
+            const float rt = r ? ws.sr[tt] : 1.0f;
             float c = 0.0f, da = 0.0f, db1 = 0.0f, dn = 0.0f;
             if (n > 0.0f) {
                 const float res = 1.0f - b * a;
@@ -510,20 +560,20 @@ __device__ void adjoint_walk(int T, int nsub, size_t seq, int tlo, int thi, bool
             }
             if (emit) {
                 float k2[NC], out[NC];
-                load_cols<NC>(dk2 + g * K + c0, k2);
+                load_cols<NC>(&ws.s2[tt][c0], k2);
 #pragma unroll
                 for (int m = 0; m < NC; ++m)
                     out[m] = k2[m] + gk[m] * dc_[m] + 2.0f * kc[m] * (c * lam[m] + da * dc_[m] + dn);
                 store_cols<NC>(dk + g * K + c0, out);
                 if (lane == 0) {
-                    dbeta[g] = db2[g] + db1;
+                    dbeta[g] = ws.sdb[tt] + db1;
                     if (dr) dr[g] = rc.x;
                 }
             }
 #pragma unroll
             for (int m = 0; m < NC; ++m) lam[m] = fmaf(rt, lam[m], fmaf(da, kc[m] * kc[m], gk[m] * kc[m]));
         }
-        __syncwarp();
+        __syncwarp();      // every lane is done with this sub-chunk's buffers
     }
 }
 
@@ -548,7 +598,8 @@ precond_adjoint_kernel(int BH, int T, int nsub, int L, int nseg, const io_t *__r
                        float *__restrict__ ws_start, float *__restrict__ ws_end,
                        int *__restrict__ ws_flag, float *__restrict__ ws_eta) {
     constexpr int NC = K / 32;
-    __shared__ __align__(16) float dsub[kBwdSeqs][kBwdSub][K];
+    extern __shared__ __align__(16) uint8_t smem_walk[];
+    WalkStage<io_t, K> *stages = reinterpret_cast<WalkStage<io_t, K> *>(smem_walk);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t id = (size_t)blockIdx.x * kBwdSeqs + warp;
     if (id >= (size_t)BH * nseg) return;        // whole warps only: no block barrier below
@@ -567,10 +618,10 @@ precond_adjoint_kernel(int BH, int T, int nsub, int L, int nseg, const io_t *__r
     bool expand = false;
     if (tend > thi)
         adjoint_walk<io_t, K>(T, nsub, seq, thi, tend, false, k, beta, r, eta, dkt_tot, dk2, db2,
-                              ck, dk, dbeta, dr, dsub[warp], lam, deta_acc, expand);
+                              ck, dk, dbeta, dr, stages[warp], lam, deta_acc, expand);
     if (nseg > 1) store_cols<NC>(ws_start + id * K + c0, lam);
     adjoint_walk<io_t, K>(T, nsub, seq, tlo, thi, true, k, beta, r, eta, dkt_tot, dk2, db2, ck,
-                          dk, dbeta, dr, dsub[warp], lam, deta_acc, expand);
+                          dk, dbeta, dr, stages[warp], lam, deta_acc, expand);
     expand = __any_sync(kFullMask, expand);   // (deta_acc is the same on every lane)
     if (nseg > 1) {
         store_cols<NC>(ws_end + id * K + c0, lam);
@@ -604,7 +655,8 @@ precond_adjoint_verify_kernel(int BH, int T, int nsub, int L, int nseg, const io
                               const int *__restrict__ ws_flag, float *__restrict__ ws_eta) {
     constexpr int NC = K / 32;
     constexpr float tol = sizeof(io_t) == 2 ? 1.220703125e-04f : 4.76837158203125e-07f;
-    __shared__ __align__(16) float dsub[kBwdSub][K];
+    extern __shared__ __align__(16) uint8_t smem_walk[];
+    WalkStage<io_t, K> &stage = *reinterpret_cast<WalkStage<io_t, K> *>(smem_walk);
     const size_t seq = blockIdx.x;
     const int lane = threadIdx.x, c0 = lane * NC;
     const size_t base = seq * nseg;
@@ -632,7 +684,7 @@ precond_adjoint_verify_kernel(int BH, int T, int nsub, int L, int nseg, const io
             float deta_acc = 0.0f;
             bool unused = false;
             adjoint_walk<io_t, K>(T, nsub, seq, tlo, thi, true, k, beta, r, eta, dkt_tot, dk2,
-                                  db2, ck, dk, dbeta, dr, dsub, prev, deta_acc, unused);
+                                  db2, ck, dk, dbeta, dr, stage, prev, deta_acc, unused);
             store_cols<NC>(ws_end + (base + i) * K + c0, prev);
             if (lane == 0) ws_eta[base + i] = deta_acc;
         } else {
@@ -737,13 +789,20 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
     const int nseg = precond_segments(BH, T, r != nullptr, &L);
     const long long nw = (long long)BH * nseg;
     int *aflag = reinterpret_cast<int *>(s.a_flag);
-    precond_adjoint_kernel<io_t, K><<<(unsigned)((nw + kBwdSeqs - 1) / kBwdSeqs), kBwdSeqs * 32, 0,
-                                      stream>>>(
+    static std::atomic<unsigned long long> attr_adj{0}, attr_ver{0};
+    constexpr int kWalk = (int)sizeof(WalkStage<io_t, K>);
+    if ((e = smem_attr_once(reinterpret_cast<const void *>(precond_adjoint_kernel<io_t, K>),
+                            kBwdSeqs * kWalk, attr_adj)) != cudaSuccess ||
+        (e = smem_attr_once(reinterpret_cast<const void *>(precond_adjoint_verify_kernel<io_t, K>),
+                            kWalk, attr_ver)) != cudaSuccess)
+        return e;
+    precond_adjoint_kernel<io_t, K><<<(unsigned)((nw + kBwdSeqs - 1) / kBwdSeqs), kBwdSeqs * 32,
+                                      kBwdSeqs * kWalk, stream>>>(
         BH, T, nsub, L, nseg, static_cast<const io_t *>(k), beta, r, eta, s.dkt_tot, ddT, s.dk2,
         s.db2, s.ck1, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.a_start, s.a_end, aflag,
         s.a_eta);
     if ((e = cudaGetLastError()) != cudaSuccess || nseg == 1) return e;
-    precond_adjoint_verify_kernel<io_t, K><<<BH, 32, 0, stream>>>(
+    precond_adjoint_verify_kernel<io_t, K><<<BH, 32, kWalk, stream>>>(
         BH, T, nsub, L, nseg, static_cast<const io_t *>(k), beta, r, eta, s.dkt_tot, s.dk2, s.db2,
         s.ck1, static_cast<io_t *>(dk), dbeta, dr, dd0, deta, s.a_start, s.a_end, aflag, s.a_eta);
     return cudaGetLastError();
