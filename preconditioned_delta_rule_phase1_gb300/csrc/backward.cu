@@ -142,8 +142,9 @@ template <int N>
 __device__ __forceinline__ void bwd_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Byte layout of the staging area (after the recomputed states and the
-// reduction buffer): slots [2] of the per-token operands, one query tile.
-template <typename io_t, int K>
+// reduction buffer): slots [2] of the per-token operands, one query tile,
+// and with a decay per key channel two slots of its [kBwdSub][K] rows.
+template <typename io_t, int K, bool PCH>
 struct BwdStage {
     static constexpr int ROW = K * (int)sizeof(io_t);                       // one token's key row
     static constexpr int VROW = kBwdRows * (int)sizeof(io_t);               // one token's v (or dO) of the rows
@@ -154,14 +155,15 @@ struct BwdStage {
     static constexpr int SDO = SV + 2 * kBwdSub * VROW;                     // [2][kBwdSub][kBwdRows]
     static constexpr int SB = SDO + 2 * kBwdSub * VROW;                     // [2][kBwdSub] beta
     static constexpr int SA = SB + 2 * kBwdSub * 4;                         // [2][kBwdSub] scalar decay
-    static constexpr int BYTES = SA + 2 * kBwdSub * 4;
+    static constexpr int SAK = SA + 2 * kBwdSub * 4;                        // [2][kBwdSub][K] per-channel decay
+    static constexpr int BYTES = SAK + (PCH ? 2 * kBwdSub * K * 4 : 0);
     static_assert(VROW % 16 == 0, "a token's rows of v must be whole 16-byte pieces");
 };
 
 template <typename io_t, int K, bool PCH>
 constexpr int state_adjoint_smem_bytes() {
     return (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4 +
-           BwdStage<io_t, K>::BYTES;
+           BwdStage<io_t, K, PCH>::BYTES;
 }
 
 template <typename io_t, int K, bool PCH>
@@ -176,7 +178,7 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     constexpr int NC = K / 32;
     constexpr int P = bwd_part_width(K, PCH);
     constexpr int PS = bwd_red_stride(K, PCH);
-    using SG = BwdStage<io_t, K>;
+    using SG = BwdStage<io_t, K, PCH>;
     constexpr int EPP = 16 / (int)sizeof(io_t);   // elements per 16-byte piece
     constexpr int PR = K / EPP;                   // pieces per key row
     constexpr int VP = SG::VROW / 16;             // pieces per token of the rows' v
@@ -192,6 +194,7 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     auto sdo = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SDO) + (s * kBwdSub + tt) * kBwdRows; };
     auto sb = [&](int s) { return reinterpret_cast<float *>(stg + SG::SB) + s * kBwdSub; };
     auto sa = [&](int s) { return reinterpret_cast<float *>(stg + SG::SA) + s * kBwdSub; };
+    auto sak = [&](int s, int tt) { return reinterpret_cast<float *>(stg + SG::SAK) + (s * kBwdSub + tt) * K; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x, nrb = gridDim.x;
@@ -227,6 +230,14 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             bwd_cp4(sb(s) + tt, beta + g, ok);
             if (!PCH && alpha) bwd_cp4(sa(s) + tt, alpha + g, ok);
         }
+        if (PCH && alpha) {
+            for (int x = threadIdx.x; x < kBwdSub * (K / 4); x += NT) {
+                const int tt = x / (K / 4), pc = x % (K / 4);
+                const bool ok = t0 + tt < T;
+                const size_t g = tok0 + (ok ? t0 + tt : 0);
+                bwd_cp16(sak(s, tt) + 4 * pc, alpha + g * K + 4 * pc, ok);
+            }
+        }
     };
     auto stage_q = [&](int j) {
         const int t0 = j * kBwdSub;
@@ -240,7 +251,12 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     // the decay of token tt of the sub-chunk in slot s for this lane's columns
     auto decay = [&](int s, int tt, size_t g, float (&a)[NC]) {
         if constexpr (PCH) {
-            decay_cols<true, NC>(alpha, g, K, c0, a);
+            if (alpha) {
+                load_cols<NC>(sak(s, tt) + c0, a);
+            } else {
+#pragma unroll
+                for (int m = 0; m < NC; ++m) a[m] = 1.0f;
+            }
         } else {
             const float x = alpha ? sa(s)[tt] : 1.0f;
 #pragma unroll
