@@ -53,40 +53,73 @@ delta_simt_kernel(int BH, int T, int V, const io_t *__restrict__ q, const io_t *
         for (int m = 0; m < KP; ++m) S[m] = s0 ? s0[p + 4 * m] : 0.0f;
     }
 
+    // The next group of tokens is loaded into registers while the current one
+    // is computed, and written to shared memory at the top of the next pass.
+    constexpr int NKV = kStage * K / (128 * 4);      // float4 pieces of each key tile a thread loads
+    constexpr int NVV = kStage * kRows / 128;         // values a thread loads
+    float rk[NKV][4], rkt[NKV][4], rq[NKV][4], rak[PCH ? NKV : 1][4], rv[NVV];
+    float rb = 0.0f, ra = 1.0f;
+    auto fetch = [&](int t0) {   // tokens t0 .. t0 + kStage - 1 (zero past T; decay 1)
+        const int tn = min(kStage, T - t0);
+#pragma unroll
+        for (int n = 0; n < NKV; ++n) {
+            const int idx = tid * 4 + n * 128 * 4;
+            const int tt = idx / K, j = idx % K;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rk[n][e] = rkt[n][e] = rq[n][e] = 0.0f;
+            if (tt < tn) {
+                const size_t g = kbase + (size_t)(t0 + tt) * K + j;
+                load4(k + g, rk[n]);
+                load4(ktilde + g, rkt[n]);
+                load4(q + g, rq[n]);
+            }
+            if constexpr (PCH) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) rak[n][e] = 1.0f;
+                if (alpha && tt < tn) load4(alpha + kbase + (size_t)(t0 + tt) * K + j, rak[n]);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NVV; ++n) {
+            const int idx = tid + n * 128;
+            const int tt = idx / kRows, i = idx % kRows;
+            rv[n] = tt < tn ? to_f32(v[vbase + (size_t)(t0 + tt) * V + row0 + i]) : 0.0f;
+        }
+        if (tid < kStage) {
+            rb = tid < tn ? beta[seq * T + t0 + tid] : 0.0f;
+            ra = (!PCH && alpha && tid < tn) ? alpha[seq * T + t0 + tid] : 1.0f;
+        }
+    };
+    fetch(0);
     for (int t0 = 0; t0 < T; t0 += kStage) {
         const int tn = min(kStage, T - t0);
         // stage k, ktilde, q (fp32 in shared memory), the value slice and the gates
-        for (int idx = tid * 4; idx < kStage * K; idx += 128 * 4) {
+#pragma unroll
+        for (int n = 0; n < NKV; ++n) {
+            const int idx = tid * 4 + n * 128 * 4;
             const int tt = idx / K, j = idx % K;
-            float a4[4] = {0, 0, 0, 0}, b4[4] = {0, 0, 0, 0}, c4[4] = {0, 0, 0, 0};
-            if (tt < tn) {
-                const size_t g = kbase + (size_t)(t0 + tt) * K + j;
-                load4(k + g, a4);
-                load4(ktilde + g, b4);
-                load4(q + g, c4);
-            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                ks[tt][j + e] = a4[e];
-                kts[tt][j + e] = b4[e];
-                qs[tt][j + e] = c4[e];
+                ks[tt][j + e] = rk[n][e];
+                kts[tt][j + e] = rkt[n][e];
+                qs[tt][j + e] = rq[n][e];
             }
             if constexpr (PCH) {
-                float d4[4] = {1, 1, 1, 1};
-                if (alpha && tt < tn) load4(alpha + kbase + (size_t)(t0 + tt) * K + j, d4);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) aks[tt][j + e] = d4[e];
+                for (int e = 0; e < 4; ++e) aks[tt][j + e] = rak[n][e];
             }
         }
-        for (int idx = tid; idx < kStage * kRows; idx += 128) {
-            const int tt = idx / kRows, i = idx % kRows;
-            vs[tt][i] = tt < tn ? to_f32(v[vbase + (size_t)(t0 + tt) * V + row0 + i]) : 0.0f;
+#pragma unroll
+        for (int n = 0; n < NVV; ++n) {
+            const int idx = tid + n * 128;
+            vs[idx / kRows][idx % kRows] = rv[n];
         }
         if (tid < kStage) {
-            bs[tid] = tid < tn ? beta[seq * T + t0 + tid] : 0.0f;
-            as[tid] = (!PCH && alpha && tid < tn) ? alpha[seq * T + t0 + tid] : 1.0f;
+            bs[tid] = rb;
+            as[tid] = ra;
         }
         __syncthreads();
+        if (t0 + kStage < T) fetch(t0 + kStage);   // in flight during this group's tokens
 
         for (int tt = 0; tt < tn; ++tt) {
             if constexpr (PCH) {   // decay the key columns first; the scalar gate below is 1
