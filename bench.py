@@ -502,6 +502,7 @@ def run_ours(args, w, x, rank, world, local_rank):
     p2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     ms = [a + b for a, b in zip(p1, p2)]
     ms_step = sum(ms) / len(ms)
+    ms_stats = {"median": statistics.median(ms), "min": min(ms), "max": max(ms)}   # this rank's
     if world > 1:
         t = torch.tensor([ms_step], dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -617,6 +618,7 @@ def run_ours(args, w, x, rank, world, local_rank):
         "dtype": w.io, "data": "synthetic (seeded)",
         "config": workload_config(w, world),
         "phases_ms": {"precond_scan": t1, "chunk_fwd": t2},
+        "step_ms": ms_stats,
         "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "algorithmic_bytes": dom[1], "peak_source": peak_src},
