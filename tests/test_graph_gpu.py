@@ -122,3 +122,55 @@ def test_decode_steps_in_a_graph():
     torch.cuda.synchronize()
     assert ws.status() == 0
     assert torch.equal(got_d, d) and torch.equal(got_S, S) and torch.equal(got_o, o)
+
+
+def test_backward_in_a_graph():
+    # the three backward kernels and the checkpoint scan, replayed on fresh
+    # inputs and cotangents, against an eager call on the same inputs
+    B, H, T, K, V = 1, 2, 300, 128, 64
+    xs = []
+    for seed in (21, 22):
+        x = to_cuda(synth.make_random(B, H, T, K, V, io="bf16", apf=True, gated=True, s0=True,
+                                      d0=True, seed=seed))
+        x["kt"], _ = ops.precond_scan(x["k"], x["beta"], x["r"], x["eta"], x["d0"])
+        gen = torch.Generator().manual_seed(seed)
+        x["do"] = torch.randn(B, H, T, V, generator=gen).to(torch.bfloat16).cuda()
+        xs.append(x)
+    a, b = xs
+    ws = ops.Workspace()
+    ws.ensure(ops.backward_workspace_bytes(B, H, T, K, V))
+    fn = lambda: ops.backward(a["q"], a["k"], a["kt"], a["v"], a["beta"], a["r"], a["eta"],
+                              a["d0"], a["alpha"], a["S0"], do=a["do"], workspace=ws)
+    names = ("q", "k", "kt", "v", "beta", "r", "d0", "alpha", "S0", "do")
+    got = captured(fn, a, {n: b[n] for n in names})
+    assert ws.status() == 0
+    ref = ops.backward(b["q"], b["k"], b["kt"], b["v"], b["beta"], b["r"], b["eta"], b["d0"],
+                       b["alpha"], b["S0"], do=b["do"])
+    torch.cuda.synchronize()
+    assert set(got) == set(ref)
+    for n in ref:
+        assert torch.equal(got[n], ref[n]), n
+
+
+def test_per_channel_decay_forward_in_a_graph():
+    # the tensor-core Phase 2 with a decay per key channel over several slabs
+    B, H, T, K, V = 1, 2, 64 * 70 + 9, 128, 128
+    xs = []
+    for seed in (23, 24):
+        x = to_cuda(synth.make_random(B, H, T, K, V, io="bf16", apf=True, s0=True, d0=True,
+                                      seed=seed))
+        gen = torch.Generator().manual_seed(seed)
+        x["ak"] = (0.9 + 0.1 * torch.rand(B, H, T, K, generator=gen)).cuda()
+        xs.append(x)
+    a, b = xs
+    ws = ops.Workspace()
+    fn = lambda: ops.forward_kda(a["q"], a["k"], a["v"], a["beta"], a["r"], a["eta"], a["d0"],
+                                 a["ak"], a["S0"], workspace=ws)
+    names = ("q", "k", "v", "beta", "r", "d0", "ak", "S0")
+    got = captured(fn, a, {n: b[n] for n in names})
+    assert ws.status() == 0
+    ref = ops.forward_kda(b["q"], b["k"], b["v"], b["beta"], b["r"], b["eta"], b["d0"], b["ak"],
+                         b["S0"])
+    torch.cuda.synchronize()
+    for x, y in zip(got, ref):
+        assert torch.equal(x, y)
