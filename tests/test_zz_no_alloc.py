@@ -89,3 +89,32 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
                                        0.1, None, ops._ptr(kt), None, None)
     torch.cuda.synchronize()
     assert code == 0, ops.status_string(code)
+
+
+def test_noalloc_in_a_graph_with_preallocated_outputs():
+    # the use the entry point exists for: a capture into which nothing is
+    # allocated (outputs given), replayed on fresh keys and gates, equal to
+    # an eager call bit for bit
+    B, H, T, K = 2, 8, 3000, 128
+    xs = [to_cuda(synth.make_random(B, H, T, K, 64, io="bf16", apf=True, d0=True, seed=s))
+          for s in (41, 42)]
+    a, b = xs
+    kt = torch.empty_like(a["k"])
+    dT = torch.empty(B, H, K, device="cuda")
+    fn = lambda: ops.precond_scan_noalloc(a["k"], a["beta"], a["r"], a["eta"], a["d0"], kt, dT)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()   # sets the kernels' attributes outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for n in ("k", "beta", "r", "d0"):
+        a[n].copy_(b[n])
+    g.replay()
+    torch.cuda.synchronize()
+    kt_ref, dT_ref = ops.precond_scan_noalloc(b["k"], b["beta"], b["r"], b["eta"], b["d0"])
+    torch.cuda.synchronize()
+    assert torch.equal(kt, kt_ref) and torch.equal(dT, dT_ref)
