@@ -155,11 +155,12 @@ def launches_per_step(w, x, per_channel=False, sms=None):
 def backward_launches(w, x, sms=None):
     """Kernels one osdn_backward call enqueues: the forward scan in checkpoint
     mode (segments + verify with a retention gate and several segments, else
-    one launch), the state adjoint and the partial sums, and the Phase 1
-    adjoint (its time segments, plus their verify kernel when there are
-    several)."""
+    one launch), the state adjoint's forward sweep, its reverse sweep and the
+    partial sums once per window of 1024 tokens, and the Phase 1 adjoint (its
+    time segments, plus their verify kernel when there are several)."""
     nseg = precond_segments(w.B * w.H, w.T, x["r"] is not None, sms)
-    return (2 if nseg > 1 else 1) + 2 + (2 if nseg > 1 else 1)
+    windows = -(-w.T // 1024)
+    return (2 if nseg > 1 else 1) + 1 + 2 * windows + (2 if nseg > 1 else 1)
 
 
 def load_peaks():

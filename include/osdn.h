@@ -311,7 +311,9 @@ int osdn_decode_step(int io, int B, int H, int K, int V, const void *q, const vo
 /*
  * Bytes of workspace osdn_backward needs for this shape (>= 256): the state
  * of each value row every 16 tokens (4 B*H*ceil(T/16)*V*K), one partial of
- * the row-summed gradients per block of 8 value rows (4 B*H*(V/8)*T*(3K+2)),
+ * the row-summed gradients per block of 8 value rows for one window of up to
+ * 1024 tokens (4 B*H*(V/8)*min(T,1024)*(3K+2); the reverse sweep runs window
+ * by window), the state gradient carried between windows (4 B*H*V*K),
  * 4 B*H*(T*(2K+1) + ceil(T/16)*K) for Phase 1's inputs and checkpoints, the
  * forward scan's segment scratch (as for osdn_precond_scan), and per time
  * segment of the Phase 1 adjoint 8K + 8 bytes, each rounded up to 256 bytes.
@@ -396,8 +398,9 @@ int osdn_chunk_fwd_kda(int io, int B, int H, int T, int K, int V, const void *q,
  * arguments and outputs, with alpha_k [B][H][T][K] fp32 (or NULL) in place
  * of alpha and dalpha_k [B][H][T][K] fp32 (or NULL) in place of dalpha.
  * Its workspace holds K + 1 rather than 2 values of dalpha and dbeta per
- * token in each row-block partial: 4 B*H*(V/8)*T*(4K+1) bytes instead of
- * 4 B*H*(V/8)*T*(3K+2), the rest as osdn_backward_workspace_bytes.
+ * token in each row-block partial: 4 B*H*(V/8)*min(T,1024)*(4K+1) bytes
+ * instead of 4 B*H*(V/8)*min(T,1024)*(3K+2), the rest as
+ * osdn_backward_workspace_bytes.
  */
 size_t osdn_backward_kda_workspace_bytes(int B, int H, int T, int K, int V);
 int osdn_backward_kda(int io, int B, int H, int T, int K, int V, const void *q, const void *k,

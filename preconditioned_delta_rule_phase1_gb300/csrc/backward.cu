@@ -52,6 +52,7 @@
 namespace osdn {
 
 constexpr int kBwdSub = 16;    // tokens per recomputed sub-chunk
+constexpr int kBwdWindow = 1024;   // tokens per reverse-sweep launch (the partials hold one window)
 constexpr int kBwdRows = 8;    // value rows (one warp each) per state-adjoint CTA
 constexpr int kBwdSeqs = 4;    // sequences (one warp each) per precond-adjoint CTA
 constexpr int kSumTok = 8;     // tokens per partial-sum CTA
@@ -174,7 +175,8 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
                      const float *__restrict__ alpha, const float *__restrict__ S0,
                      const io_t *__restrict__ dO, const float *__restrict__ dST,
                      io_t *__restrict__ dv, float *__restrict__ dS0, float *__restrict__ ck,
-                     float *__restrict__ part) {
+                     float *__restrict__ part, int fwd, int tw0, int tw1, int Tw,
+                     float *__restrict__ gcarry) {
     constexpr int NC = K / 32;
     constexpr int P = bwd_part_width(K, PCH);
     constexpr int PS = bwd_red_stride(K, PCH);
@@ -264,8 +266,9 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
         }
     };
 
-    // forward sweep: the row's state every kBwdSub tokens
+    // forward sweep (its own launch): the row's state every kBwdSub tokens
     float S[NC];
+    if (fwd) {
     if (S0) {
         load_cols<NC>(S0 + (seq * V + i) * (size_t)K + c0, S);
     } else {
@@ -292,23 +295,31 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             for (int m = 0; m < NC; ++m) S[m] = fmaf(a[m], S[m], u * tc[m]);
         }
     }
+    bwd_wait<0>();
+    return;
+    }
 
-    // reverse sweep
+    // reverse sweep over the window [tw0, tw1) (tw0 a multiple of kBwdWindow,
+    // tw1 the next one or T), starting from the state gradient the later
+    // window left in gcarry (from d_ST for the last window)
     float G[NC];
-    if (dST) {
+    float *grow = gcarry + (seq * V + i) * (size_t)K + c0;
+    if (tw1 < T) {
+        load_cols<NC>(grow, G);
+    } else if (dST) {
         load_cols<NC>(dST + (seq * V + i) * (size_t)K + c0, G);
     } else {
 #pragma unroll
         for (int m = 0; m < NC; ++m) G[m] = 0.0f;
     }
-    __syncthreads();   // the forward sweep is done with both slots
+    const int jhi = (tw1 - 1) / kBwdSub, jlo = tw0 / kBwdSub;
     int slot = 0;
-    if (nsub > 0) stage(slot, nsub - 1, true);
+    stage(slot, jhi, true);
     bwd_commit();
     int buf = 0;
-    for (int j = nsub - 1; j >= 0; --j) {
+    for (int j = jhi; j >= jlo; --j) {
         __syncthreads();   // every warp is done with the other slot and the queries
-        if (j >= 1) stage(slot ^ 1, j - 1, true);
+        if (j > jlo) stage(slot ^ 1, j - 1, true);
         bwd_commit();
         bwd_wait<1>();
         __syncthreads();   // sub-chunk j is in
@@ -393,7 +404,7 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             // writes the other buffer, and its barrier orders these reads
             // before this buffer is written again
             const float *rsum = red + buf * kBwdRows * PS;
-            float *dst = part + ((seq * nrb + rb) * (size_t)T + t0 + tt) * P;
+            float *dst = part + ((seq * nrb + rb) * (size_t)Tw + (t0 + tt - tw0)) * P;
             for (int x = threadIdx.x; x < P; x += kBwdRows * 32) {
                 float s = 0.0f;
 #pragma unroll
@@ -405,26 +416,27 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
         slot ^= 1;
     }
     bwd_wait<0>();
-    if (dS0) store_cols<NC>(dS0 + (seq * V + i) * (size_t)K + c0, G);
+    if (tw0 > 0) store_cols<NC>(grow, G);
+    else if (dS0) store_cols<NC>(dS0 + (seq * V + i) * (size_t)K + c0, G);
 }
 
 // ---------------------------------------------------------------- kernel 2
 template <typename io_t, int K, bool PCH>
 __global__ void __launch_bounds__(256)
-partial_sum_kernel(int BH, int T, int nrb, const float *__restrict__ part,
+partial_sum_kernel(int BH, int T, int nrb, int tw0, int tn, int Tw, const float *__restrict__ part,
                    const io_t *__restrict__ dkt_ext, io_t *__restrict__ dq,
                    float *__restrict__ dalpha, float *__restrict__ dkt_tot,
                    float *__restrict__ dk2, float *__restrict__ db2) {
     constexpr int P = bwd_part_width(K, PCH);
     const size_t seq = grid_seq();
     if (seq >= (size_t)BH) return;
-    const int tb = blockIdx.x * kSumTok;
+    const int tb = blockIdx.x * kSumTok;   // within the window
     for (int x = threadIdx.x; x < kSumTok * P; x += blockDim.x) {
         const int tt = x / P, col = x % P;
-        const int t = tb + tt;
-        if (t >= T) continue;
+        const int tl = tb + tt, t = tw0 + tl;
+        if (tl >= tn) continue;
         float s = 0.0f;
-        for (int r = 0; r < nrb; ++r) s += part[((seq * nrb + r) * (size_t)T + t) * P + col];
+        for (int r = 0; r < nrb; ++r) s += part[((seq * nrb + r) * (size_t)Tw + tl) * P + col];
         const size_t g = seq * (size_t)T + t;
         if (col < K) {
             from_f32(dq[g * K + col], s);
@@ -736,15 +748,17 @@ cudaError_t precond_checkpoint_launch(int io, int BH, int T, int K, const void *
 // start) and first token, flags and deta shares (the segments of the forward
 // scan's rule, with a retention gate; sized for it in any case).
 struct BwdScratch {
-    float *ck2, *part, *dkt_tot, *dk2, *db2, *ck1, *p1, *a_start, *a_end, *a_flag, *a_eta;
+    float *ck2, *part, *gcarry, *dkt_tot, *dk2, *db2, *ck1, *p1, *a_start, *a_end, *a_flag, *a_eta;
 };
 
 static size_t bwd_layout(int BH, int T, int K, int V, bool pch, char *base, BwdScratch *s) {
     const size_t nsub = ((size_t)T + kBwdSub - 1) / kBwdSub;
+    const size_t tw = T < kBwdWindow ? (size_t)T : (size_t)kBwdWindow;   // tokens of one window
     const size_t n = (size_t)BH * precond_segments(BH, T, true, nullptr);
-    const size_t sz[11] = {
+    const size_t sz[12] = {
         pad256((size_t)BH * nsub * V * K * 4),                                   // ck2
-        pad256((size_t)BH * (V / kBwdRows) * T * bwd_part_width(K, pch) * 4),    // part
+        pad256((size_t)BH * (V / kBwdRows) * tw * bwd_part_width(K, pch) * 4),   // part
+        pad256((size_t)BH * V * K * 4),                                           // gcarry
         pad256((size_t)BH * T * K * 4),                                           // dkt_tot
         pad256((size_t)BH * T * K * 4),                                           // dk2
         pad256((size_t)BH * T * 4),                                               // db2
@@ -753,9 +767,9 @@ static size_t bwd_layout(int BH, int T, int K, int V, bool pch, char *base, BwdS
         pad256(n * K * 4), pad256(n * K * 4), pad256(n * 4), pad256(n * 4),       // a_*
     };
     size_t off = 0;
-    float **dst[11] = {&s->ck2, &s->part, &s->dkt_tot, &s->dk2, &s->db2, &s->ck1, &s->p1,
-                       &s->a_start, &s->a_end, &s->a_flag, &s->a_eta};
-    for (int a = 0; a < 11; ++a) {
+    float **dst[12] = {&s->ck2, &s->part, &s->gcarry, &s->dkt_tot, &s->dk2, &s->db2, &s->ck1,
+                       &s->p1, &s->a_start, &s->a_end, &s->a_flag, &s->a_eta};
+    for (int a = 0; a < 12; ++a) {
         if (base) *dst[a] = reinterpret_cast<float *>(base + off);
         off += sz[a];
     }
@@ -790,15 +804,28 @@ static cudaError_t launch_backward(int BH, int T, int V, const void *q, const vo
     auto *k1 = state_adjoint_kernel<io_t, K, PCH>;
     e = smem_attr_once(reinterpret_cast<const void *>(k1), smem, attr_done);
     if (e != cudaSuccess) return e;
-    k1<<<seq_grid(nrb, BH), kBwdRows * 32, smem, stream>>>(
-        BH, T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
-        static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
-        static_cast<const io_t *>(dO), dST, static_cast<io_t *>(dv), dS0, s.ck2, s.part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    partial_sum_kernel<io_t, K, PCH><<<seq_grid(T / kSumTok + (T % kSumTok != 0), BH), 256, 0, stream>>>(
-        BH, T, nrb, s.part, static_cast<const io_t *>(dkt_ext), static_cast<io_t *>(dq), dalpha,
-        s.dkt_tot, s.dk2, s.db2);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the forward sweep, then the reverse sweep window by window (newest
+    // first), each window's row-block partials summed before the next one
+    // reuses their buffer
+    const int Tw = T < kBwdWindow ? T : kBwdWindow;
+    auto sweep = [&](int fwd, int tw0, int tw1) {
+        k1<<<seq_grid(nrb, BH), kBwdRows * 32, smem, stream>>>(
+            BH, T, V, nsub, static_cast<const io_t *>(q), static_cast<const io_t *>(k),
+            static_cast<const io_t *>(kt), static_cast<const io_t *>(v), beta, alpha, S0,
+            static_cast<const io_t *>(dO), dST, static_cast<io_t *>(dv), dS0, s.ck2, s.part, fwd,
+            tw0, tw1, Tw, s.gcarry);
+        return cudaGetLastError();
+    };
+    if ((e = sweep(1, 0, T)) != cudaSuccess) return e;
+    for (int tw1 = T; tw1 > 0;) {
+        const int tw0 = ((tw1 - 1) / kBwdWindow) * kBwdWindow, tn = tw1 - tw0;
+        if ((e = sweep(0, tw0, tw1)) != cudaSuccess) return e;
+        partial_sum_kernel<io_t, K, PCH><<<seq_grid(tn / kSumTok + (tn % kSumTok != 0), BH), 256, 0, stream>>>(
+            BH, T, nrb, tw0, tn, Tw, s.part, static_cast<const io_t *>(dkt_ext),
+            static_cast<io_t *>(dq), dalpha, s.dkt_tot, s.dk2, s.db2);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        tw1 = tw0;
+    }
     // the Phase 1 adjoint in time segments (one per sequence without a
     // retention gate), then their verification
     int L = T;

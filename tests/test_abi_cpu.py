@@ -81,11 +81,12 @@ def test_bench_launch_count_rule():
     # launch and a chain in two time segments (speculative pass + 1 repair)
     w = synth.WORKLOADS["lm1p3b_apf_bf16"]
     assert bench.launches_per_step(w, {"r": 1, "alpha": None}, per_channel=True, sms=152) == 5
-    # the backward at that shape: checkpoint scan (2), state adjoint, partial
-    # sums, Phase 1 adjoint segments and their verify kernel (the launch list
-    # shows 6 a step); without a retention gate 4
-    assert bench.backward_launches(w, {"r": 1}, sms=152) == 6
-    assert bench.backward_launches(w, {"r": None}, sms=152) == 4
+    # the backward at that shape: checkpoint scan (2), the state adjoint's
+    # forward sweep, its reverse sweep and the partial sums for each of the 8
+    # windows of 1024 tokens, Phase 1 adjoint segments and their verify kernel
+    # (21 a step); without a retention gate 19
+    assert bench.backward_launches(w, {"r": 1}, sms=152) == 21
+    assert bench.backward_launches(w, {"r": None}, sms=152) == 19
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails validation first
@@ -285,7 +286,8 @@ def test_host_validation_backward(L):
 
 def test_backward_workspace_size(L):
     # the state of each value row every 16 tokens, one partial of the row sums
-    # (3K + 2 values a token) per block of 8 rows, Phase 1's inputs and
+    # (3K + 2 values a token) per block of 8 rows for one window of up to 1024
+    # tokens, the state gradient carried between windows, Phase 1's inputs and
     # checkpoints, the forward scan's segment scratch (as osdn_precond_scan's),
     # and per time segment of the adjoint two K-vectors and two words; each
     # array padded to 256 bytes
@@ -297,9 +299,10 @@ def test_backward_workspace_size(L):
         BH, ns = B * H, -(-T // 16)
         n = BH * bench.precond_segments(BH, T, True, 152)
         p1 = L.osdn_precond_scan_workspace_bytes(B, H, T, K) - 256
-        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (3 * K + 2) * 4)
-                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4) + r(p1)
-                + 2 * r(n * K * 4) + 2 * r(n * 4))
+        tw = min(T, 1024)
+        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * tw * (3 * K + 2) * 4)
+                + r(BH * V * K * 4) + 2 * r(BH * T * K * 4) + r(BH * T * 4)
+                + r(BH * ns * K * 4) + r(p1) + 2 * r(n * K * 4) + 2 * r(n * 4))
         assert L.osdn_backward_workspace_bytes(B, H, T, K, V) == want, (B, H, T, K, V)
 
 
@@ -375,9 +378,10 @@ def test_backward_kda_workspace_size(L):
         BH, ns = B * H, -(-T // 16)
         n = BH * bench.precond_segments(BH, T, True, 152)
         p1 = L.osdn_precond_scan_workspace_bytes(B, H, T, K) - 256
-        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * T * (4 * K + 1) * 4)
-                + 2 * r(BH * T * K * 4) + r(BH * T * 4) + r(BH * ns * K * 4) + r(p1)
-                + 2 * r(n * K * 4) + 2 * r(n * 4))
+        tw = min(T, 1024)
+        want = (256 + r(BH * ns * V * K * 4) + r(BH * (V // 8) * tw * (4 * K + 1) * 4)
+                + r(BH * V * K * 4) + 2 * r(BH * T * K * 4) + r(BH * T * 4)
+                + r(BH * ns * K * 4) + r(p1) + 2 * r(n * K * 4) + 2 * r(n * 4))
         assert L.osdn_backward_kda_workspace_bytes(B, H, T, K, V) == want
 
 
