@@ -126,6 +126,16 @@ def test_longer_sequence():
     check(x, cotangents(1, 2, 700, 128, 128, "bf16", 82), "bf16")
 
 
+@pytest.mark.parametrize("io,T", [("f32", 1025), ("bf16", 2048), ("f32", 2100)])
+def test_reverse_sweep_windows(io, T):
+    # the state adjoint's reverse sweep runs in windows of 1024 tokens, the
+    # state gradient carried between them: a last window of one token, two
+    # full windows, and a ragged third one
+    x = synth.make_random(1, 2, T, 64, 64, io=io, apf=True, gated=True, s0=True, d0=True,
+                          seed=90 + T)
+    check(x, cotangents(1, 2, T, 64, 64, io, 91 + T), io)
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("case", ["accepted", "slow_retention", "expansive_token"])
 def test_phase1_adjoint_time_segments(io, case):
