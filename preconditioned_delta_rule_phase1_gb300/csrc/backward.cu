@@ -383,15 +383,18 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             // dalpha = <dSbar, S_{t-1}[i]>: per key column with a per-channel
             // decay (scalar stores: the columns start at the odd offset 3K + 1),
             // else summed over the row
+            // (without a decay there is no dalpha: its columns are left at 0)
             if constexpr (PCH) {
 #pragma unroll
-                for (int m = 0; m < NC; ++m) rw[3 * K + 1 + c0 + m] = dSb[m] * sp[m];
-            } else {
+                for (int m = 0; m < NC; ++m) rw[3 * K + 1 + c0 + m] = alpha ? dSb[m] * sp[m] : 0.0f;
+            } else if (alpha) {
                 float dal = 0.0f;
 #pragma unroll
                 for (int m = 0; m < NC; ++m) dal = fmaf(dSb[m], sp[m], dal);
                 dal = warp_sum(dal);
                 if (lane == 0) rw[3 * K + 1] = dal;
+            } else if (lane == 0) {
+                rw[3 * K + 1] = 0.0f;
             }
             if (lane == 0) {
                 rw[3 * K] = du * e;
