@@ -748,7 +748,10 @@ def run_backward(args, local_rank):
     """--backward: the gradients of both phases (osdn_backward) at the
     workload's shape, with the output cotangent dO given.  The forward runs
     once, untimed, for ktilde.  Inputs are larger than L2, so no flush is
-    needed between steps; one JSON line with the pass's HBM roofline."""
+    needed between steps; one JSON line with the pass's HBM roofline.  With
+    --kda as well: osdn_backward_kda, the decay drawn per token and channel in
+    [0.9, 1) as --kda draws it (its bytes read and its gradient written count
+    in the roofline)."""
     from preconditioned_delta_rule_phase1_gb300 import ops
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -761,8 +764,15 @@ def run_backward(args, local_rank):
     ws = ops.Workspace(device=dev)
     kt, _ = ops.precond_scan(g["k"], g["beta"], g["r"], g["eta"], g["d0"], workspace=ws,
                              stream=stream)
-    step = lambda: ops.backward(g["q"], g["k"], kt, g["v"], g["beta"], g["r"], g["eta"], g["d0"],
-                                g["alpha"], g["S0"], do=dO, workspace=ws, stream=stream)
+    if args.kda:
+        gen_a = torch.Generator().manual_seed(2)
+        ak = (0.9 + 0.1 * torch.rand(w.B, w.H, w.T, w.K, generator=gen_a)).to(dev)
+        step = lambda: ops.backward_kda(g["q"], g["k"], kt, g["v"], g["beta"], g["r"], g["eta"],
+                                        g["d0"], ak, g["S0"], do=dO, workspace=ws, stream=stream)
+    else:
+        step = lambda: ops.backward(g["q"], g["k"], kt, g["v"], g["beta"], g["r"], g["eta"],
+                                    g["d0"], g["alpha"], g["S0"], do=dO, workspace=ws,
+                                    stream=stream)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -779,17 +789,19 @@ def run_backward(args, local_rank):
     clk = clocks.stop()
     assert ws.status(stream) == 0
     ms = e0.elapsed_time(e1) / args.steps
-    nbytes = backward_bytes(w, x)
+    nbytes = backward_bytes(w, x) + (2 * w.B * w.H * w.T * w.K * 4 if args.kda else 0)
     hbm_peak, _, peak_src = load_peaks()
     achieved = nbytes / (ms * 1e-3) / 1e9
     print(json.dumps({
-        "metric": "OSDN backward tokens/s (gradients of phase1+2)",
+        "metric": ("OSDN backward tokens/s with a per-channel decay" if args.kda
+                   else "OSDN backward tokens/s (gradients of phase1+2)"),
         "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
         "higher_is_better": True, "dtype": w.io, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.K, "d_v": w.V,
-                   "l2": "inputs larger than L2"},
-        "roofline": {"kernel": "osdn_backward (3 kernels)", "bound": "hbm",
+        "config": {"workload": w.name + ("_kda" if args.kda else ""), "B": w.B, "H": w.H,
+                   "T": w.T, "d_k": w.K, "d_v": w.V, "l2": "inputs larger than L2"},
+        "roofline": {"kernel": "osdn_backward_kda" if args.kda else "osdn_backward",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "algorithmic_bytes": nbytes,
                      "peak_source": peak_src, "traffic": None},
@@ -920,7 +932,7 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="time the gradients of both phases instead of the forward pass")
     ap.add_argument("--kda", action="store_true",
-                    help="time both phases with a per-channel decay instead")
+                    help="time both phases with a per-channel decay instead (with --backward: its gradients)")
     ap.add_argument("--fused", action="store_true",
                     help="time the one-call forward pass (ktilde kept on chip) instead")
     args = ap.parse_args()
