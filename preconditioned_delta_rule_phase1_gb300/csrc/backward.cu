@@ -144,7 +144,7 @@ __device__ __forceinline__ void bwd_wait() { asm volatile("cp.async.wait_group %
 
 // Byte layout of the staging area (after the recomputed states and the
 // reduction buffer): slots [2] of the per-token operands, one query tile,
-// and with a decay per key channel two slots of its [kBwdSub][K] rows.
+// and with a decay per key channel one tile of its [kBwdSub][K] rows.
 template <typename io_t, int K, bool PCH>
 struct BwdStage {
     static constexpr int ROW = K * (int)sizeof(io_t);                       // one token's key row
@@ -156,14 +156,20 @@ struct BwdStage {
     static constexpr int SDO = SV + 2 * kBwdSub * VROW;                     // [2][kBwdSub][kBwdRows]
     static constexpr int SB = SDO + 2 * kBwdSub * VROW;                     // [2][kBwdSub] beta
     static constexpr int SA = SB + 2 * kBwdSub * 4;                         // [2][kBwdSub] scalar decay
-    static constexpr int SAK = SA + 2 * kBwdSub * 4;                        // [2][kBwdSub][K] per-channel decay
-    static constexpr int BYTES = SAK + (PCH ? 2 * kBwdSub * K * 4 : 0);
+    static constexpr int SAK = SA + 2 * kBwdSub * 4;                        // [kBwdSub][K] per-channel decay
+    static constexpr int BYTES = SAK + (PCH ? kBwdSub * K * 4 : 0);
     static_assert(VROW % 16 == 0, "a token's rows of v must be whole 16-byte pieces");
 };
 
+// The reduction tile is double-buffered (one barrier a token); with a decay
+// per key channel, whose rows are wider, it is single-buffered (two
+// barriers a token) so that two CTAs still fit on an SM.
+template <bool PCH>
+constexpr int bwd_red_bufs() { return PCH ? 1 : 2; }
+
 template <typename io_t, int K, bool PCH>
 constexpr int state_adjoint_smem_bytes() {
-    return (kBwdRows * kBwdSub * K + 2 * kBwdRows * bwd_red_stride(K, PCH)) * 4 +
+    return (kBwdRows * kBwdSub * K + bwd_red_bufs<PCH>() * kBwdRows * bwd_red_stride(K, PCH)) * 4 +
            BwdStage<io_t, K, PCH>::BYTES;
 }
 
@@ -187,8 +193,9 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     constexpr int NT = kBwdRows * 32;
     extern __shared__ __align__(16) float smem[];
     float *Sp = smem;                                  // [kBwdRows][kBwdSub][K]
-    float *red = smem + kBwdRows * kBwdSub * K;        // [2][kBwdRows][PS]
-    uint8_t *stg = reinterpret_cast<uint8_t *>(red + 2 * kBwdRows * PS);
+    constexpr int NRED = bwd_red_bufs<PCH>();
+    float *red = smem + kBwdRows * kBwdSub * K;        // [NRED][kBwdRows][PS]
+    uint8_t *stg = reinterpret_cast<uint8_t *>(red + NRED * kBwdRows * PS);
     auto sk = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SK) + (s * kBwdSub + tt) * K; };
     auto skt = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SKT) + (s * kBwdSub + tt) * K; };
     auto sq = [&](int tt) { return reinterpret_cast<io_t *>(stg + SG::SQ) + tt * K; };
@@ -196,7 +203,7 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     auto sdo = [&](int s, int tt) { return reinterpret_cast<io_t *>(stg + SG::SDO) + (s * kBwdSub + tt) * kBwdRows; };
     auto sb = [&](int s) { return reinterpret_cast<float *>(stg + SG::SB) + s * kBwdSub; };
     auto sa = [&](int s) { return reinterpret_cast<float *>(stg + SG::SA) + s * kBwdSub; };
-    auto sak = [&](int s, int tt) { return reinterpret_cast<float *>(stg + SG::SAK) + (s * kBwdSub + tt) * K; };
+    auto sak = [&](int tt) { return reinterpret_cast<float *>(stg + SG::SAK) + tt * K; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x, nrb = gridDim.x;
@@ -232,14 +239,18 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
             bwd_cp4(sb(s) + tt, beta + g, ok);
             if (!PCH && alpha) bwd_cp4(sa(s) + tt, alpha + g, ok);
         }
-        if (PCH && alpha) {
-            for (int x = threadIdx.x; x < kBwdSub * (K / 4); x += NT) {
-                const int tt = x / (K / 4), pc = x % (K / 4);
-                const bool ok = t0 + tt < T;
-                const size_t g = tok0 + (ok ? t0 + tt : 0);
-                bwd_cp16(sak(s, tt) + 4 * pc, alpha + g * K + 4 * pc, ok);
-            }
+    };
+    // sub-chunk j's per-channel decay rows into their one tile (issued when
+    // the previous sub-chunk is done with it, ahead of the next prefetch)
+    auto stage_alpha = [&](int j) {
+        const int t0 = j * kBwdSub;
+        for (int x = threadIdx.x; x < kBwdSub * (K / 4); x += NT) {
+            const int tt = x / (K / 4), pc = x % (K / 4);
+            const bool ok = t0 + tt < T;
+            const size_t g = tok0 + (ok ? t0 + tt : 0);
+            bwd_cp16(sak(tt) + 4 * pc, alpha + g * K + 4 * pc, ok);
         }
+        bwd_commit();
     };
     auto stage_q = [&](int j) {
         const int t0 = j * kBwdSub;
@@ -254,7 +265,7 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     auto decay = [&](int s, int tt, size_t g, float (&a)[NC]) {
         if constexpr (PCH) {
             if (alpha) {
-                load_cols<NC>(sak(s, tt) + c0, a);
+                load_cols<NC>(sak(tt) + c0, a);
             } else {
 #pragma unroll
                 for (int m = 0; m < NC; ++m) a[m] = 1.0f;
@@ -278,7 +289,8 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     if (nsub > 0) stage(0, 0, false);
     bwd_commit();
     for (int j = 0; j < nsub; ++j) {
-        __syncthreads();   // every warp is done with the other slot
+        __syncthreads();   // every warp is done with the other slot (and the decay tile)
+        if (PCH && alpha) stage_alpha(j);
         if (j + 1 < nsub) stage((j + 1) & 1, j + 1, false);
         bwd_commit();
         bwd_wait<1>();
@@ -318,7 +330,8 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
     bwd_commit();
     int buf = 0;
     for (int j = jhi; j >= jlo; --j) {
-        __syncthreads();   // every warp is done with the other slot and the queries
+        __syncthreads();   // every warp is done with the other slot, the queries (and the decay tile)
+        if (PCH && alpha) stage_alpha(j);
         if (j > jlo) stage(slot ^ 1, j - 1, true);
         bwd_commit();
         bwd_wait<1>();
@@ -414,7 +427,8 @@ state_adjoint_kernel(int BH, int T, int V, int nsub, const io_t *__restrict__ q,
                 for (int w = 0; w < kBwdRows; ++w) s += rsum[w * PS + x];
                 dst[x] = s;
             }
-            buf ^= 1;
+            if (NRED == 1) __syncthreads();   // the tile is read before the next token writes it
+            else buf ^= 1;
         }
         slot ^= 1;
     }
